@@ -1,0 +1,439 @@
+"""CPU oracle for one MoE layer: route, pack, simulated expert-parallel layout,
+dispatch, grouped SwiGLU experts, combine, and the backward of each.
+
+TEST INFRASTRUCTURE ONLY. This module is the slow, obviously-correct statement
+of what the GPU library computes. Only the test suite, the smoke check and the
+benchmark's CPU-baseline leg may import it; the library itself never does. It
+shares no code with the CUDA path: plain NumPy, float64 arithmetic, and a
+library primitive (argsort, lexsort, matmul) as a single step wherever one fits.
+
+Sources (cited by page title and section):
+
+[TAS]  "Three axes of Parallelism" (nanoTitan blog), section "Expert Parallel (EP)":
+       subsections "Mapping experts to EP ranks", "Producing assignments",
+       "Dispatch, expert computation and combine", "EP backward pass".
+[MOD]  modalities PR "feat(parallelism): expert parallelism for the Nemotron-3
+       Nano MoE layers", sections "Design" and "Tests".
+[SF]   SpecForge PR "(fsdp2 dev.) feat(moe): expert parallelism for MoE drafters
+       on the FSDP2 backend", section "What this adds".
+
+Readings where the pages are silent (each listed in the design notes):
+
+* top-k selects on the raw fp32 logits, ties to the lower expert id; slot j of
+  a token is its j-th best expert. Weights are the softmax over all E experts
+  taken at the selected ids; with ``renorm`` they are divided by their sum over
+  the K selected (equivalently a softmax over the K selected logits).
+* inside one expert's segment, assignments keep ascending flat index
+  a = t*K + j (the order the pages' per-expert ``argwhere`` loop produces).
+* SwiGLU: h = silu(x W_gate) * (x W_val), y = h W_out, no biases.
+* bf16 rounding points: the saved [G|U], H, Y, the combined output, and in the
+  backward dY, dG, dU, dX. Everything else is exact (float64 here; fp32
+  accumulation on the GPU).
+* simulated rank s owns tokens [s*T/R, (s+1)*T/R); expert e lives on rank
+  e // (E/R).
+
+Parity status: every function here is pinned by the CPU tests against
+invariants, brute force, closed forms or an independent library (torch
+autograd / matmul); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "round_bf16", "route_topk", "softmax", "expert_counts_offsets", "stable_permutation",
+    "permutation_by_expert_loop", "ep_layout", "dispatch", "swiglu_expert", "grouped_ffn",
+    "combine", "combine_backward", "swiglu_expert_backward", "grouped_ffn_backward",
+    "dispatch_backward", "route_topk_backward", "layer_forward", "layer_backward",
+]
+
+
+# --------------------------------------------------------------------------- #
+# bf16 rounding (storage precision of activations and weights)
+# --------------------------------------------------------------------------- #
+def round_bf16(x):
+    """Round to the nearest bfloat16 value, ties to even, returned as float64.
+
+    bfloat16 keeps 8 significant bits and float32's exponent range. For a
+    finite x with |x| in [2^(q-1), 2^q) the spacing of bf16 values is
+    2^(q-8), but never finer than the subnormal spacing 2^-133. Scaling by a
+    power of two is exact in float64, so rint (which rounds halves to even)
+    of x/spacing gives the correctly rounded multiple. Results at or beyond
+    2^128 overflow to infinity.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x, dtype=np.float64, copy=True)
+    finite = np.isfinite(x) & (x != 0)
+    xf = x[finite]
+    _, q = np.frexp(xf)                       # xf = m * 2^q, 0.5 <= |m| < 1
+    step_exp = np.maximum(q - 8, -133)
+    r = np.ldexp(np.rint(np.ldexp(xf, -step_exp)), step_exp)
+    r = np.where(np.abs(r) >= 2.0 ** 128, np.copysign(np.inf, r), r)
+    out[finite] = r
+    return out
+
+
+def _identity(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _rounder(exact: bool):
+    return _identity if exact else round_bf16
+
+
+# --------------------------------------------------------------------------- #
+# A1: router top-k  ([TAS] "Producing assignments")
+# --------------------------------------------------------------------------- #
+def softmax(logits):
+    """Row-wise softmax in float64 (max-shifted)."""
+    l = np.asarray(logits, dtype=np.float64)
+    z = np.exp(l - l.max(axis=-1, keepdims=True))
+    return z / z.sum(axis=-1, keepdims=True)
+
+
+def route_topk(logits, K: int, renorm: int = 1):
+    """Router scores [T,E] -> expert ids [T,K] (int32) and weights [T,K] (float64).
+
+    Each token is scored against all E experts and the top-K are kept
+    ([TAS] "Producing assignments": expert_IDs and router_weights, both [T,K]).
+    Selection is on the raw logits: a stable descending sort, so equal logits
+    keep ascending expert id (ties go to the lower id; -0.0 equals +0.0).
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    T, E = l.shape
+    if not (1 <= K <= E):
+        raise ValueError("need 1 <= K <= E")
+    order = np.argsort(-l, axis=1, kind="stable")
+    idx = order[:, :K]
+    p = softmax(l)
+    w = np.take_along_axis(p, idx, axis=1)
+    if renorm:
+        w = w / w.sum(axis=1, keepdims=True)
+    return idx.astype(np.int32), w
+
+
+def route_topk_backward(logits, idx, w, dw, renorm: int = 1):
+    """d(loss)/d(logits) [T,E] given d(loss)/d(weights) [T,K].
+
+    The weights are a differentiable function of the logits through the
+    softmax; the selected ids are not. This writes out the Jacobian of that
+    map explicitly, token by token, and applies its transpose to dw:
+
+    * renorm=0: w_j = p_{e_j}, p = softmax(all logits),
+      dw_j/dl_i = p_{e_j} * ([i == e_j] - p_i).
+    * renorm=1: w_j = softmax over the K selected logits,
+      dw_j/dl_{e_m} = w_j * ([j == m] - w_m), and 0 for unselected i.
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    idx = np.asarray(idx)
+    w = np.asarray(w, dtype=np.float64)
+    dw = np.asarray(dw, dtype=np.float64)
+    T, E = l.shape
+    K = idx.shape[1]
+    dl = np.zeros((T, E), dtype=np.float64)
+    if renorm:
+        for t in range(T):
+            J = np.diag(w[t]) - np.outer(w[t], w[t])          # J[j, m] = dw_j / dl_{e_m}
+            g = J.T @ dw[t]
+            np.add.at(dl[t], idx[t], g)
+    else:
+        p = softmax(l)
+        for t in range(T):
+            J = np.zeros((K, E))
+            for j in range(K):
+                J[j] = -p[t, idx[t, j]] * p[t]
+                J[j, idx[t, j]] += p[t, idx[t, j]]
+            dl[t] = J.T @ dw[t]
+    return dl
+
+
+# --------------------------------------------------------------------------- #
+# A2, A3: histogram, offsets and stable expert-major permutation
+# ([TAS] "Producing assignments"; [MOD] "Design", item 1)
+# --------------------------------------------------------------------------- #
+def expert_counts_offsets(idx, E: int):
+    """c_e = number of assignments routed to expert e; offsets[0] = 0,
+    offsets[1:] = cumulative counts, so offsets[E] = T*K."""
+    flat = np.asarray(idx).reshape(-1)
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    return counts, offsets
+
+
+def stable_permutation(idx, E: int):
+    """Expert-major packing of the token-major assignment buffer.
+
+    The assignment buffer is [T*K] with token 0's K slots first (flat index
+    a = t*K + j). perm[p] = a lists assignments sorted by expert id, ties kept
+    in ascending a (a stable sort), so expert e's rows occupy
+    [offsets[e], offsets[e+1]). inv_perm[a] = p is its inverse.
+    """
+    flat = np.asarray(idx).reshape(-1)
+    if flat.size and (flat.min() < 0 or flat.max() >= E):
+        raise ValueError("expert id out of range")
+    perm = np.argsort(flat, kind="stable")
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size)
+    return perm.astype(np.int64), inv.astype(np.int64)
+
+
+def permutation_by_expert_loop(idx, E: int):
+    """The pages' own packing procedure, restated as a second reference: for
+    each expert in turn, take the (token, slot) pairs that chose it in row-major
+    order and append them ([TAS] "Producing assignments", the per-expert
+    argwhere loop)."""
+    idx = np.asarray(idx)
+    T, K = idx.shape
+    out = []
+    for e in range(E):
+        hits = np.argwhere(idx == e)              # row-major (t, j) pairs
+        out.extend(int(t) * K + int(j) for t, j in hits)
+    return np.asarray(out, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------- #
+# A4: layout of a simulated all-to-all over R expert-parallel ranks
+# ([TAS] "Mapping experts to EP ranks", "Dispatch, expert computation and
+#  combine"; [MOD] "Design", items 1-2)
+# --------------------------------------------------------------------------- #
+def _inverse(order):
+    inv = np.empty_like(order)
+    inv[order] = np.arange(order.size)
+    return inv
+
+
+def ep_layout(idx, T: int, E: int, K: int, R: int):
+    """Counts, splits and index arrays of one dispatch over R simulated ranks.
+
+    Rank s holds tokens [s*T/R, (s+1)*T/R) (a disjoint shard of the data) and
+    experts [s*E/R, (s+1)*E/R) (contiguous ownership). Returns
+
+    * ep_counts [R,E]: C[s,e] = assignments on rank s routed to expert e
+      (row s is rank s's expert_counts; reshaped [R, E/R] it is send_matrix);
+    * send_splits [R,R]: S[s,d] = assignments rank s sends to rank d
+      (= row sums of rank s's send_matrix);
+    * send_index [TK]: send buffer position q -> flat assignment a. Rank s's
+      block starts at s*T*K/R and is packed expert-major, so within a block the
+      order is (expert, a);
+    * a2a_index [TK]: receive position r -> send position q. Receive buffers
+      are concatenated over destinations; each one is laid out by source rank
+      ("assignments from rank 0 are contiguous, followed by rank 1"), and each
+      source's rows arrive in that source's packed (expert, a) order;
+    * regroup_index [TK]: expert-major position -> receive position. Each
+      destination regroups its buffer so that each local expert's rows are
+      contiguous; within a local expert the rows stay in (source, a) order.
+
+    Every array is built by its own sort of the stated key; nothing is derived
+    in closed form.
+    """
+    idx = np.asarray(idx)
+    if E % R or T % R:
+        raise ValueError("R must divide E and T")
+    El = E // R
+    TK = T * K
+    a = np.arange(TK)
+    e = idx.reshape(-1).astype(np.int64)
+    s = (a // K) // (T // R)
+    dst = e // El
+    C = np.zeros((R, E), dtype=np.int64)
+    np.add.at(C, (s, e), 1)
+    S = C.reshape(R, R, El).sum(axis=2)
+    send_order = np.lexsort((a, e, s))                # q -> a, key (s, e, a)
+    qpos = _inverse(send_order)                       # a -> q
+    recv_order = np.lexsort((a, e, s, dst))           # r -> a, key (dst, s, e, a)
+    a2a_index = qpos[recv_order]                      # r -> q
+    rpos = _inverse(recv_order)                       # a -> r
+    group_order = np.lexsort((a, s, e % El, dst))     # p -> a, key (dst, local e, s, a)
+    regroup_index = rpos[group_order]                 # p -> r
+    return {
+        "ep_counts": C, "send_splits": S, "send_index": send_order.astype(np.int64),
+        "a2a_index": a2a_index.astype(np.int64), "regroup_index": regroup_index.astype(np.int64),
+        "group_order": group_order.astype(np.int64),
+    }
+
+
+# --------------------------------------------------------------------------- #
+# A5: dispatch gather ([TAS] "Producing assignments"; [MOD] index_select)
+# --------------------------------------------------------------------------- #
+def dispatch(x, perm, K: int):
+    """xp[p] = x[perm[p] // K]: the packed copy of each assignment's token row."""
+    x = np.asarray(x)
+    return x[np.asarray(perm) // K].copy()
+
+
+# --------------------------------------------------------------------------- #
+# A6: grouped SwiGLU experts ([TAS] "Mapping experts to EP ranks" for the
+# W_gate / W_val / W_out stacks; "Dispatch, expert computation and combine":
+# the experts are independent MLPs over contiguous rows)
+# --------------------------------------------------------------------------- #
+def _silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_expert(X, Wg, Wu, Wd, exact: bool = False):
+    """One expert MLP on rows X [M,d]: G = X Wg, U = X Wu (exact sums),
+    saved GU = bf16([G | U]), H = bf16(silu(G) * U), Y = bf16(H Wd)."""
+    rnd = _rounder(exact)
+    X = np.asarray(X, dtype=np.float64)
+    G = X @ np.asarray(Wg, dtype=np.float64)
+    U = X @ np.asarray(Wu, dtype=np.float64)
+    GU = rnd(np.concatenate([G, U], axis=1))
+    H = rnd(_silu(G) * U)
+    Y = rnd(H @ np.asarray(Wd, dtype=np.float64))
+    return Y, GU, H
+
+
+def grouped_ffn(xp, offsets, Wg, Wu, Wd, exact: bool = False):
+    """Expert e runs on packed rows [offsets[e], offsets[e+1]); empty experts
+    produce no rows. Returns y [TK,d], gu [TK,2I], h [TK,I]."""
+    xp = np.asarray(xp, dtype=np.float64)
+    E = len(offsets) - 1
+    I = np.asarray(Wg).shape[-1]
+    d = np.asarray(Wd).shape[-1]
+    n = xp.shape[0]
+    y = np.zeros((n, d))
+    gu = np.zeros((n, 2 * I))
+    h = np.zeros((n, I))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        y[lo:hi], gu[lo:hi], h[lo:hi] = swiglu_expert(xp[lo:hi], Wg[e], Wu[e], Wd[e], exact)
+    return y, gu, h
+
+
+def swiglu_expert_backward(dY, X, GU, H, Wg, Wu, Wd, exact: bool = False):
+    """Backward of one expert MLP, G and U taken from the saved GU.
+
+    dH = dY Wd^T; with s = sigmoid(G): dG = bf16(dH * U * s * (1 + G (1 - s))),
+    dU = bf16(dH * G * s); dX = bf16(dG Wg^T + dU Wu^T);
+    dWd = H^T dY, dWg = X^T dG, dWu = X^T dU (exact sums).
+    """
+    rnd = _rounder(exact)
+    dY = np.asarray(dY, dtype=np.float64)
+    X = np.asarray(X, dtype=np.float64)
+    GU = np.asarray(GU, dtype=np.float64)
+    H = np.asarray(H, dtype=np.float64)
+    Wg = np.asarray(Wg, dtype=np.float64)
+    Wu = np.asarray(Wu, dtype=np.float64)
+    Wd = np.asarray(Wd, dtype=np.float64)
+    I = Wg.shape[1]
+    G, U = GU[:, :I], GU[:, I:]
+    dH = dY @ Wd.T
+    s = 1.0 / (1.0 + np.exp(-G))
+    dG = rnd(dH * U * s * (1.0 + G * (1.0 - s)))
+    dU = rnd(dH * G * s)
+    dX = rnd(dG @ Wg.T + dU @ Wu.T)
+    return dX, X.T @ dG, X.T @ dU, H.T @ dY
+
+
+def grouped_ffn_backward(dy, xp, gu, h, offsets, Wg, Wu, Wd, exact: bool = False):
+    """Per-expert backward over the packed segments. Experts with no rows get
+    zero weight gradients. Returns dxp [TK,d], dWg, dWu [E,d,I], dWd [E,I,d]."""
+    E = len(offsets) - 1
+    Wg = np.asarray(Wg)
+    d, I = Wg.shape[1], Wg.shape[2]
+    n = np.asarray(dy).shape[0]
+    dxp = np.zeros((n, d))
+    dWg = np.zeros((E, d, I))
+    dWu = np.zeros((E, d, I))
+    dWd = np.zeros((E, I, d))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        dxp[lo:hi], dWg[e], dWu[e], dWd[e] = swiglu_expert_backward(
+            dy[lo:hi], xp[lo:hi], gu[lo:hi], h[lo:hi], Wg[e], Wu[e], Wd[e], exact)
+    return dxp, dWg, dWu, dWd
+
+
+# --------------------------------------------------------------------------- #
+# A7 / B1 / B3: combine and the transposes of dispatch and combine
+# ([TAS] "Dispatch, expert computation and combine", last paragraph;
+#  [MOD] index_select / index_copy pair; [SF] shared expert on local tokens)
+# --------------------------------------------------------------------------- #
+def combine(y, w, inv_perm, K: int, shared_y=None, exact: bool = False):
+    """out[t] = bf16( sum_j w[t,j] * y[inv_perm[t*K+j]] (+ shared_y[t]) ):
+    undo the packing, weight each expert output by its router weight and sum
+    the K outputs of each token; the shared experts' output is added unweighted."""
+    rnd = _rounder(exact)
+    y = np.asarray(y, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    T = w.shape[0]
+    rows = y[np.asarray(inv_perm).reshape(T, K)]        # [T,K,d]
+    acc = np.einsum("tk,tkd->td", w, rows)
+    if shared_y is not None:
+        acc = acc + np.asarray(shared_y, dtype=np.float64)
+    return rnd(acc)
+
+
+def combine_backward(dout, y, w, inv_perm, K: int, exact: bool = False):
+    """dy[inv_perm[a]] = bf16(w[a] * dout[t]); dw[a] = <dout[t], y[inv_perm[a]]>."""
+    rnd = _rounder(exact)
+    dout = np.asarray(dout, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    T = w.shape[0]
+    ip = np.asarray(inv_perm).reshape(T, K)
+    dy = np.zeros_like(y)
+    dy[ip.reshape(-1)] = rnd((w[:, :, None] * dout[:, None, :]).reshape(T * K, -1))
+    dw = np.einsum("td,tkd->tk", dout, y[ip])
+    return dy, dw
+
+
+def dispatch_backward(dxp, inv_perm, K: int, T: int, dx_shared=None, exact: bool = False):
+    """dx[t] = bf16( sum_j dxp[inv_perm[t*K+j]] (+ dx_shared[t]) )."""
+    rnd = _rounder(exact)
+    dxp = np.asarray(dxp, dtype=np.float64)
+    acc = dxp[np.asarray(inv_perm).reshape(T, K)].sum(axis=1)
+    if dx_shared is not None:
+        acc = acc + np.asarray(dx_shared, dtype=np.float64)
+    return rnd(acc)
+
+
+# --------------------------------------------------------------------------- #
+# Whole layer
+# --------------------------------------------------------------------------- #
+def layer_forward(inp, K: int, R: int, renorm: int = 1, exact: bool = False):
+    """One MoE layer's forward on the inputs of ``workloads.make_inputs``
+    converted to float64 numpy arrays (keys logits, x, w_gate, w_up, w_down,
+    optional ws_gate/ws_up/ws_down). Returns a dict of every intermediate."""
+    logits = inp["logits"]
+    T, E = logits.shape
+    idx, w = route_topk(logits, K, renorm)
+    counts, offsets = expert_counts_offsets(idx, E)
+    perm, inv_perm = stable_permutation(idx, E)
+    ep = ep_layout(idx, T, E, K, R)
+    xp = dispatch(inp["x"], perm, K)
+    y, gu, h = grouped_ffn(xp, offsets, inp["w_gate"], inp["w_up"], inp["w_down"], exact)
+    ys = gus = hs = None
+    if "ws_gate" in inp:
+        ys, gus, hs = swiglu_expert(inp["x"], inp["ws_gate"], inp["ws_up"], inp["ws_down"], exact)
+    out = combine(y, w, inv_perm, K, ys, exact)
+    res = dict(topk_idx=idx, topk_w=w, counts=counts, offsets=offsets, perm=perm,
+               inv_perm=inv_perm, xp=xp, y=y, gu=gu, h=h, out=out)
+    res.update(ep)
+    if ys is not None:
+        res.update(ys=ys, gus=gus, hs=hs)
+    return res
+
+
+def layer_backward(inp, fwd, dout, K: int, renorm: int = 1, exact: bool = False):
+    """Backward of ``layer_forward`` for upstream gradient dout [T,d]."""
+    T, E = inp["logits"].shape
+    dy, dw = combine_backward(dout, fwd["y"], fwd["topk_w"], fwd["inv_perm"], K, exact)
+    dxp, dWg, dWu, dWd = grouped_ffn_backward(dy, fwd["xp"], fwd["gu"], fwd["h"], fwd["offsets"],
+                                              inp["w_gate"], inp["w_up"], inp["w_down"], exact)
+    dxs = None
+    res = {}
+    if "ws_gate" in inp:
+        dxs, dWgs, dWus, dWds = swiglu_expert_backward(dout, inp["x"], fwd["gus"], fwd["hs"],
+                                                       inp["ws_gate"], inp["ws_up"],
+                                                       inp["ws_down"], exact)
+        res.update(dx_shared=dxs, dws_gate=dWgs, dws_up=dWus, dws_down=dWds)
+    dx = dispatch_backward(dxp, fwd["inv_perm"], K, T, dxs, exact)
+    dlogits = route_topk_backward(inp["logits"], fwd["topk_idx"], fwd["topk_w"], dw, renorm)
+    res.update(dy=dy, dtopk_w=dw, dxp=dxp, dw_gate=dWg, dw_up=dWu, dw_down=dWd, dx=dx,
+               dlogits=dlogits)
+    return res

@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Throughput of one MoE layer's forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config qwen3|dsv2lite|skew|drafter|tiny]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+route top-k, histogram/offsets/permutation, the simulated expert-parallel
+layout (with its one device-to-host copy), dispatch, grouped SwiGLU experts,
+combine, and the backward of each. Rank 0 prints one JSON line.
+
+* value: tokens/s over all ranks, inputs resident in HBM, per-step CUDA events
+  on the launching stream; L2 is flushed (a 256 MiB write) before every timed
+  step, outside the step's events.
+* e2e: the same metric through the layer API with pinned host buffers: each
+  step copies logits, x and dout in and the output and input gradient out.
+* roofline: the dominant kernel's algorithmic flops (or bytes) per launch over
+  its average launch duration, from per-launch events the library records on
+  the launching stream during the timed steps.
+* cpu_baseline: the CPU oracle timed on a bounded sample of the same workload.
+* --impl reference: the CPU oracle as the reference arm (rank 0 only).
+
+Multi-GPU runs (torchrun) are independent replicas with no data-path
+collective: every rank runs the same layer on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd+bwd tokens/s on 1 GB300; % of bf16 TC / HBM roofline per kernel"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ work model
+def kernel_work(name: str, cfg, shared: bool):
+    """Algorithmic work of one launch: ("tensor", flops) or ("hbm", bytes)."""
+    T, d, E, K, I = cfg.T, cfg.d, cfg.E, cfg.K, cfg.I
+    TK = T * K
+    if shared:
+        M, Ie = T, cfg.shared_I
+    else:
+        M, Ie = TK, I
+    gemm = {
+        "gemm_gate_up": 4 * M * d * Ie, "gemm_down": 2 * M * Ie * d, "gemm_dh": 2 * M * d * Ie,
+        "gemm_dx": 4 * M * d * Ie, "gemm_wgrad_gate_up": 4 * M * d * Ie,
+        "gemm_wgrad_down": 2 * M * Ie * d,
+    }
+    if name in gemm:
+        return "tensor", gemm[name]
+    hbm = {
+        "route_topk": T * (4 * E + 8 * K),
+        "route_topk_backward": T * (12 * K + 4 * E),
+        "perm_hist": 4 * TK, "perm_scatter": 12 * TK, "ep_hist": 4 * TK, "ep_scatter": 16 * TK,
+        "dispatch": T * (2 * d * (1 + K) + 4 * K),
+        "combine": T * (2 * d * K + 8 * K + 2 * d + (2 * d if cfg.shared_I else 0)),
+        "combine_backward": T * (2 * d + 4 * d * K + 12 * K),
+        "dispatch_backward": T * (2 * d * K + 4 * K + 2 * d + (2 * d if cfg.shared_I else 0)),
+    }
+    return "hbm", hbm.get(name, 0)
+
+
+def label_records(records, steps):
+    """Splits the launch records into steps and tags the second occurrence of a
+    GEMM name within a step as the shared-expert launch."""
+    if not records or len(records) % steps:
+        return [(n, ms, False) for n, ms in records]
+    per = len(records) // steps
+    out = []
+    for s in range(steps):
+        seen = {}
+        for n, ms in records[s * per:(s + 1) * per]:
+            k = seen.get(n, 0)
+            seen[n] = k + 1
+            out.append((n, ms, n.startswith("gemm_") and k == 1))
+    return out
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file if ln.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[3:7]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_step(cfg, T_s):
+    """One oracle forward+backward on the first T_s tokens' worth of inputs."""
+    import numpy as np  # noqa: F401
+    from grouped_gemm_moe_gb300 import workloads as W
+    from oracle import moe_oracle as O
+    inp = W.make_inputs(cfg, T=T_s, with_backward=True)
+    np_inp = {k: W.to_f64(v) for k, v in inp.items()}
+    R = cfg.R if T_s % cfg.R == 0 else 1
+    t0 = time.perf_counter()
+    fwd = O.layer_forward(np_inp, cfg.K, R, cfg.renorm)
+    O.layer_backward(np_inp, fwd, np_inp["dout"], cfg.K, cfg.renorm)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, tokens):
+    R = cfg.R
+    if tokens <= 0:
+        # calibrate: aim at roughly 15 s of CPU work
+        t_small = oracle_step(cfg, R * 4)
+        per_tok = t_small / (R * 4)
+        tokens = int(min(2048, max(R * 4, 15.0 / max(per_tok, 1e-6))))
+        tokens -= tokens % R
+    dt = oracle_step(cfg, tokens)
+    return {"value": tokens / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{tokens} of {cfg.T} tokens of the same workload (full expert weights), "
+                      f"fwd+bwd, float64 NumPy, one run of {dt:.2f} s"}
+
+
+def run_reference(args, cfg, world, rank):
+    if rank != 0:
+        return
+    from grouped_gemm_moe_gb300 import workloads as W
+    budget = 120.0
+    probe = oracle_step(cfg, cfg.R * 2)
+    per_tok = probe / (cfg.R * 2)
+    n_steps = args.steps + args.warmup
+    tokens = int(max(cfg.R, min(cfg.T, budget / n_steps / max(per_tok, 1e-6))))
+    tokens -= tokens % cfg.R
+    tokens = max(tokens, cfg.R)
+    for _ in range(args.warmup):
+        oracle_step(cfg, tokens)
+    times = [oracle_step(cfg, tokens) for _ in range(args.steps)]
+    ms = statistics.mean(times) * 1e3
+    value = tokens / (ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) logits/activations, N(0,0.02) weights)",
+        "config": {"workload": f"{cfg.name}: {W.describe(cfg)}, fwd+bwd",
+                   "sample_tokens_per_step": tokens},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{tokens} of {cfg.T} tokens per step, float64 NumPy oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    from grouped_gemm_moe_gb300 import workloads as W
+    cfg = W.CONFIGS[args.config or W.BENCH_CONFIG]
+    if args.impl == "reference":
+        run_reference(args, cfg, world, rank)
+        return
+    import torch
+    import torch.distributed as dist
+    from grouped_gemm_moe_gb300 import binding as B
+    from grouped_gemm_moe_gb300 import build as build_mod
+    from grouped_gemm_moe_gb300 import layer as L
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not os.path.exists(B.LIB_PATH):
+        build_mod.build()
+    B.load()
+    if not cfg.backward:
+        raise SystemExit("the benchmark workload must include the backward pass")
+
+    inp = W.make_inputs(cfg, seed=cfg.seed + rank)
+    layer = L.layer_from_config(cfg, inp, dev)
+    logits, x, dout = (inp[k].to(dev) for k in ("logits", "x", "dout"))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    t_warm = time.time()
+    for i in range(max(args.warmup, 3)):
+        flush.zero_()
+        layer.forward(logits, x)
+        layer.backward(dout)
+    torch.cuda.synchronize()
+    # keep the GPU busy long enough for the clock sampler to see it under load
+    while time.time() - t_warm < 1.5:
+        layer.forward(logits, x)
+        layer.backward(dout)
+        torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise SystemExit("device status word reports an error")
+
+    barrier()
+    torch.cuda.synchronize()
+    B.moe_profile_start(64 * args.steps + 64)
+    evs = []
+    for i in range(args.steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        layer.forward(logits, x)
+        layer.backward(dout)
+        e.record(stream)
+        evs.append((s, e))
+    torch.cuda.synchronize()
+    barrier()
+    records = B.moe_profile_stop()
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * cfg.T / (ms / 1e3)
+
+    # per-kernel table and the dominant kernel's roofline
+    pk = peaks()
+    per = {}
+    for n, kms, sh in label_records(records, args.steps):
+        key = n + ("[shared]" if sh else "")
+        c = per.setdefault(key, {"launches": 0, "total_ms": 0.0, "shared": sh, "name": n})
+        c["launches"] += 1
+        c["total_ms"] += kms
+    tot = sum(c["total_ms"] for c in per.values()) or 1.0
+    kernels = {}
+    for k, c in per.items():
+        kind, work = kernel_work(c["name"], cfg, c["shared"])
+        avg = c["total_ms"] / c["launches"]
+        if kind == "tensor":
+            ach, unit, peak = work / (avg / 1e3) / 1e12, "TFLOP/s", pk["bf16_tflops_sustained"]
+        else:
+            ach, unit, peak = work / (avg / 1e3) / 1e9, "GB/s", pk["hbm_gbs"]
+        kernels[k] = {"launches": c["launches"], "avg_ms": round(avg, 5),
+                      "share": round(c["total_ms"] / tot, 4), "achieved": round(ach, 1),
+                      "unit": unit, "frac": round(ach / peak, 4)}
+    dom = max(per, key=lambda k: per[k]["total_ms"])
+    dkind, dwork = kernel_work(per[dom]["name"], cfg, per[dom]["shared"])
+    davg = per[dom]["total_ms"] / per[dom]["launches"]
+    if dkind == "tensor":
+        achieved = dwork / (davg / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved,
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops_sustained"],
+                "frac_of_burst_peak": achieved / pk["bf16_tflops"],
+                "peak_source": f"{pk['source']} bf16 sustained", "traffic": None,
+                "work_per_launch": f"{dwork:.4g} flop"}
+    else:
+        achieved = dwork / (davg / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                "peak_source": f"{pk['source']} HBM copy", "traffic": None,
+                "work_per_launch": f"{dwork:.4g} B"}
+    flops_step = sum(kernel_work(c["name"], cfg, c["shared"])[1] * c["launches"]
+                     for c in per.values()
+                     if kernel_work(c["name"], cfg, c["shared"])[0] == "tensor") / args.steps
+    clocks = sampler.stop() if sampler else None
+
+    # end to end through the layer API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.pin_memory()  # noqa: E731
+        lh, xh, dh = pin(inp["logits"]), pin(inp["x"]), pin(inp["dout"])
+        out_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+        dx_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+        for _ in range(2):
+            layer.step_from_host(lh, xh, dh, out_h, dx_h)
+        torch.cuda.synchronize()
+        barrier()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(args.steps):
+            h2d, d2h = layer.step_from_host(lh, xh, dh, out_h, dx_h)
+        e.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = s.elapsed_time(e) / args.steps
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * cfg.T / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, args.cpu_sample_tokens)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) logits/activations, N(0,0.02) weights)",
+            "config": {"workload": f"{cfg.name}: {W.describe(cfg)}, fwd+bwd",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed by a 256 MiB write before every timed step (outside its events)",
+                       "step_tflop": flops_step / 1e12,
+                       "layer_tflops_achieved": flops_step / (ms / 1e3) / 1e12},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": len(records), "clocks": clocks,
+            "step_ms_min_max": [min(step_ms), max(step_ms)],
+            "kernels": kernels, "device": torch.cuda.get_device_name(dev),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+// Dispatch gather, weighted combine, and their transposes.
+//
+// Sources: "Three axes of Parallelism" (nanoTitan blog), section "Expert
+// Parallel (EP)" -> "Producing assignments" (the [T*K, D] assignment buffer
+// packed expert-major) and "Dispatch, expert computation and combine" (undo
+// the packing with the saved indices, multiply each expert output by its
+// router weight and sum the K outputs); modalities PR "expert parallelism for
+// the Nemotron-3 Nano MoE layers", section "Design" (the index_select /
+// index_copy permutation pair); SpecForge PR "expert parallelism for MoE
+// drafters on the FSDP2 backend", "What this adds" (shared expert added on
+// the local tokens).
+//
+// All four kernels are HBM-bound row moves: 16-byte vector loads and stores,
+// rows of d bf16 = d/8 vectors. Dispatch and the two token-major reductions
+// map one thread to one 16-byte vector of an output row, so a warp touches 512
+// contiguous bytes; each thread of the reductions issues its K independent
+// gathered loads before it accumulates (fp32, slot order, no atomics).
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+int grid_for(long long work, int per_block) {
+  long long b = (work + per_block - 1) / per_block;
+  const long long cap = static_cast<long long>(num_sms()) * 16;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return static_cast<int>(b);
+}
+
+// xp[p] = x[perm[p] / K]
+__global__ void __launch_bounds__(kThreads)
+dispatch_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int K, int nv,
+                long long total, uint4* __restrict__ xp) {
+  const long long stride = static_cast<long long>(gridDim.x) * kThreads;
+  for (long long i0 = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i0 < total;
+       i0 += stride * kUnroll) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < total) {
+        const long long p = i / nv;
+        const int c = static_cast<int>(i - p * nv);
+        const long long t = __ldg(perm + p) / K;
+        v[u] = ldg_nc_v4(x + t * nv + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < total) stg_v4(xp + i, v[u]);
+    }
+  }
+}
+
+// out[t] = bf16( sum_j w[t,j] * rows[inv_perm[t*K+j]] + extra[t] ); w == nullptr means 1.
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads)
+gather_sum_kernel(const uint4* __restrict__ rows, const float* __restrict__ w,
+                  const int32_t* __restrict__ inv_perm, int K, int nv, long long total,
+                  const uint4* __restrict__ extra, uint4* __restrict__ out) {
+  const long long stride = static_cast<long long>(gridDim.x) * kThreads;
+  for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+       i += stride) {
+    const long long t = i / nv;
+    const int c = static_cast<int>(i - t * nv);
+    const int32_t* ip = inv_perm + t * K;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    uint4 v[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < K) v[j] = ldg_nc_v4(rows + static_cast<long long>(__ldg(ip + j)) * nv + c);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < K) {
+        const float wj = w ? __ldg(w + t * K + j) : 1.f;
+        float f[8];
+        unpack8(v[j], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(wj, f[q], acc[q]);
+      }
+    }
+    if (extra) {
+      float f[8];
+      unpack8(ldg_nc_v4(extra + i), f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+    }
+    stg_v4(out + i, pack8(acc));
+  }
+}
+
+// One warp per token: dy[p] = bf16(w[a] * dout[t]) and dw[a] = <dout[t], y[p]>.
+__global__ void __launch_bounds__(kThreads)
+combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ y,
+                        const float* __restrict__ w, const int32_t* __restrict__ inv_perm, int T,
+                        int K, int nv, uint4* __restrict__ dy, float* __restrict__ dw) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (kThreads / 32);
+  for (long long t = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+       t < T; t += warps) {
+    const uint4* drow = dout + t * nv;
+    for (int j = 0; j < K; ++j) {
+      const long long a = t * K + j;
+      const long long p = __ldg(inv_perm + a);
+      const float wa = __ldg(w + a);
+      const uint4* yrow = y + p * nv;
+      uint4* dyrow = dy + p * nv;
+      float dot = 0.f;
+#pragma unroll 4
+      for (int c = lane; c < nv; c += 32) {
+        const uint4 dv = __ldg(drow + c);
+        const uint4 yv = ldg_nc_v4(yrow + c);
+        float fd[8], fy[8], g[8];
+        unpack8(dv, fd);
+        unpack8(yv, fy);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) { dot = fmaf(fd[q], fy[q], dot); g[q] = wa * fd[q]; }
+        stg_v4(dyrow + c, pack8(g));
+      }
+      dot = warp_sum(dot);
+      if (lane == 0) dw[a] = dot;
+    }
+  }
+}
+
+int launch_gather_sum(const void* rows, const float* w, const int32_t* inv_perm, int T, int K,
+                      int d, const void* extra, void* out, cudaStream_t st) {
+  const int nv = d / 8;
+  const long long total = static_cast<long long>(T) * nv;
+  const int grid = grid_for(total, kThreads);
+  auto r = static_cast<const uint4*>(rows);
+  auto x = static_cast<const uint4*>(extra);
+  auto o = static_cast<uint4*>(out);
+  ProfScope prof(w ? "combine" : "dispatch_backward", st);
+  if (K <= 2)
+    gather_sum_kernel<2><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
+  else if (K <= 4)
+    gather_sum_kernel<4><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
+  else if (K <= 8)
+    gather_sum_kernel<8><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
+  else if (K <= 16)
+    gather_sum_kernel<16><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
+  else
+    gather_sum_kernel<32><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
+  return check_launch();
+}
+
+bool shape_ok(int T, int K, int d) { return T >= 0 && K >= 1 && K <= 32 && d > 0 && d % 8 == 0; }
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_dispatch(const moe_bf16* x, int T, int d, int K, const int32_t* perm,
+                            moe_bf16* xp, void* stream) {
+  using namespace moe;
+  if (!shape_ok(T, K, d)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !perm || !xp) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(perm) || !aligned16(xp)) return MOE_ERR_MISALIGNED;
+  const int nv = d / 8;
+  const long long total = static_cast<long long>(T) * K * nv;
+  const int grid = grid_for(total, kThreads * kUnroll);
+  ProfScope prof("dispatch", as_stream(stream));
+  dispatch_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(
+      reinterpret_cast<const uint4*>(x), perm, K, nv, total, reinterpret_cast<uint4*>(xp));
+  return check_launch();
+}
+
+extern "C" int moe_combine(const moe_bf16* y, const float* topk_w, const int32_t* inv_perm, int T,
+                           int K, int d, const moe_bf16* shared_y, moe_bf16* out, void* stream) {
+  using namespace moe;
+  if (!shape_ok(T, K, d)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!y || !topk_w || !inv_perm || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(topk_w) || !aligned16(inv_perm) || !aligned16(out) ||
+      (shared_y && !aligned16(shared_y)))
+    return MOE_ERR_MISALIGNED;
+  return launch_gather_sum(y, topk_w, inv_perm, T, K, d, shared_y, out, as_stream(stream));
+}
+
+extern "C" int moe_dispatch_backward(const moe_bf16* dxp, const int32_t* inv_perm, int T, int K,
+                                     int d, const moe_bf16* dx_shared, moe_bf16* dx,
+                                     void* stream) {
+  using namespace moe;
+  if (!shape_ok(T, K, d)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!dxp || !inv_perm || !dx) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dxp) || !aligned16(inv_perm) || !aligned16(dx) ||
+      (dx_shared && !aligned16(dx_shared)))
+    return MOE_ERR_MISALIGNED;
+  return launch_gather_sum(dxp, nullptr, inv_perm, T, K, d, dx_shared, dx, as_stream(stream));
+}
+
+extern "C" int moe_combine_backward(const moe_bf16* dout, const moe_bf16* y, const float* topk_w,
+                                    const int32_t* inv_perm, int T, int K, int d, moe_bf16* dy,
+                                    float* dtopk_w, void* stream) {
+  using namespace moe;
+  if (!shape_ok(T, K, d)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!dout || !y || !topk_w || !inv_perm || !dy || !dtopk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(y) || !aligned16(topk_w) || !aligned16(inv_perm) ||
+      !aligned16(dy) || !aligned16(dtopk_w))
+    return MOE_ERR_MISALIGNED;
+  const int per_block = kThreads / 32;
+  long long blocks = (T + per_block - 1) / per_block;
+  const long long cap = static_cast<long long>(num_sms()) * 16;
+  if (blocks > cap) blocks = cap;
+  ProfScope prof("combine_backward", as_stream(stream));
+  combine_backward_kernel<<<static_cast<int>(blocks), kThreads, 0, as_stream(stream)>>>(
+      reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(y), topk_w, inv_perm,
+      T, K, d / 8, reinterpret_cast<uint4*>(dy), dtopk_w);
+  return check_launch();
+}

@@ -1,0 +1,806 @@
+// Grouped SwiGLU expert GEMMs on the 5th-generation tensor cores (tcgen05,
+// accumulators in TMEM, operands staged by TMA), forward and backward.
+//
+// Source: "Three axes of Parallelism" (nanoTitan blog), section "Expert
+// Parallel (EP)": the stacked expert weights W_gate [E,d,I], W_val [E,d,I],
+// W_out [E,I,d] ("Mapping experts to EP ranks"); with each expert's rows
+// contiguous, expert computation is E independent MLPs ("Dispatch, expert
+// computation and combine"); expert gradients stay with their expert
+// ("EP backward pass"). SpecForge PR "expert parallelism for MoE drafters on
+// the FSDP2 backend" names a grouped_mm backend over expert-sorted rows; that
+// is prior art, this is an independent kernel.
+//
+// Kernel shape (one template, six problem kinds):
+//   * persistent: one CTA per SM, static round-robin over a tile list that
+//     every CTA derives on device from the expert offsets (no host sync);
+//   * 192 threads, warp-specialised: warp 0 issues TMA loads into a ring of
+//     shared-memory stages, warp 1 owns TMEM and issues tcgen05.mma (one
+//     thread), warps 2-5 drain the accumulator with tcgen05.ld and run the
+//     fused epilogue (SwiGLU, SwiGLU backward, bf16 or fp32 stores);
+//   * 128 x BN x 64 tiles, BN = 256 or 128, fp32 accumulators double-buffered
+//     in TMEM (2*BN columns) so the epilogue of tile i overlaps the MMAs of
+//     tile i+1;
+//   * operands use the 128-byte swizzle. K-major tiles come from row-major
+//     activations and from the weights in the backward; MN-major tiles from
+//     the weights in the forward and from both operands of the weight
+//     gradients, so no operand is ever transposed in memory;
+//   * ragged segments: forward / input-gradient tiles start at an expert's
+//     first row and mask stores past its last row; the weight gradients run a
+//     ragged K loop over the expert's rows and zero the rows of the last
+//     k-block that belong to the next expert before the MMA reads them.
+//   * every mbarrier wait is bounded (a few seconds of %globaltimer); on
+//     timeout the CTA records MOE_ERR_DEVICE_TIMEOUT in the workspace status
+//     word, drains its own TMA loads and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace gemm {
+
+enum Kind : int {
+  FWD_GATEUP = 0,  // [G|U] = X [Wg|Wu]; epilogue H = silu(G)*U (+ save GU)
+  FWD_DOWN = 1,    // Y = H Wd
+  BWD_DH = 2,      // dH = dY Wd^T; epilogue dG, dU from saved GU
+  BWD_DX = 3,      // dX = [dG|dU] [Wg|Wu]^T
+  WGRAD_GU = 4,    // [dWg|dWu] = X^T [dG|dU]   (ragged K)
+  WGRAD_D = 5      // dWd = H^T dY              (ragged K)
+};
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;
+
+struct Params {
+  const int32_t* offsets;  // [E+1] expert row offsets (device)
+  int E;
+  int M;                   // rows of the packed activations
+  int d;
+  int I;
+  int n_tiles;             // tiles along N
+  int m_tiles;             // weight gradients: tiles along M (d/128 or I/128)
+  int k_blocks;            // forward / input gradients: K / 64
+  __nv_bfloat16* out;      // h, y, dgu or dxp
+  __nv_bfloat16* out2;     // gu (forward, may be null)
+  const __nv_bfloat16* aux;  // gu (BWD_DH)
+  float* outf0;            // dWg / dWd
+  float* outf1;            // dWu
+  int ld_out;              // row length of `out` in elements
+  int* status;             // workspace status word
+};
+
+// ----------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity to complete.
+// Returns false if this CTA is aborting (another role timed out) or the wait
+// itself ran past kTimeoutNs (then it raises the abort flag and the status).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       int* status) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        report_status(status, MOE_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread i gets row (lane base + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 D, bf16 A and B, M = 128.
+template <int N, bool A_MN, bool B_MN>
+__host__ __device__ constexpr uint32_t make_idesc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) |
+         ((B_MN ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
+
+__device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const float (&v)[16]) {
+  uint4 a, b;
+  a.x = pack_bf16(v[0], v[1]);   a.y = pack_bf16(v[2], v[3]);
+  a.z = pack_bf16(v[4], v[5]);   a.w = pack_bf16(v[6], v[7]);
+  b.x = pack_bf16(v[8], v[9]);   b.y = pack_bf16(v[10], v[11]);
+  b.z = pack_bf16(v[12], v[13]); b.w = pack_bf16(v[14], v[15]);
+  uint4* p = reinterpret_cast<uint4*>(dst);
+  p[0] = a;
+  p[1] = b;
+}
+
+__device__ __forceinline__ void load16_bf16(const __nv_bfloat16* src, float (&v)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+  float f[8];
+  unpack8(p[0], f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = f[i];
+  unpack8(p[1], f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[8 + i] = f[i];
+}
+
+__device__ __forceinline__ void store16_f32(float* dst, const float (&v)[16]) {
+  float4* p = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+// ----------------------------------------------------------------- tiles
+struct Tile {
+  int e;        // expert
+  int row0;     // first packed row (forward / input gradients) or first k row (weight grads)
+  int rows;     // valid rows (forward / input gradients) or K rows (weight grads)
+  int m0;       // weight gradients: first output row
+  int n0;       // first output column (in the kind's N space)
+  int nkb;      // k-blocks
+};
+
+template <int KIND, int BN>
+__device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int* s_off,
+                                            const int* s_mt) {
+  Tile tl;
+  if constexpr (KIND == WGRAD_GU || KIND == WGRAD_D) {
+    const int per_e = p.m_tiles * p.n_tiles;
+    tl.e = t / per_e;
+    const int rem = t - tl.e * per_e;
+    const int mt = rem / p.n_tiles;
+    const int nt = rem - mt * p.n_tiles;
+    tl.m0 = mt * BM;
+    tl.n0 = nt * BN;
+    tl.row0 = s_off[tl.e];
+    tl.rows = s_off[tl.e + 1] - tl.row0;
+    tl.nkb = (tl.rows + BK - 1) / BK;
+  } else {
+    const int mg = t / p.n_tiles;
+    const int nt = t - mg * p.n_tiles;
+    int lo = 0, hi = p.E - 1;   // largest e with s_mt[e] <= mg
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_mt[mid] <= mg) lo = mid; else hi = mid - 1;
+    }
+    tl.e = lo;
+    tl.row0 = s_off[lo] + (mg - s_mt[lo]) * BM;
+    tl.rows = min(BM, s_off[lo + 1] - tl.row0);
+    tl.m0 = 0;
+    tl.n0 = nt * (KIND == FWD_GATEUP ? BN / 2 : BN);
+    tl.nkb = p.k_blocks;
+  }
+  return tl;
+}
+
+// ----------------------------------------------------------------- kernel
+template <int KIND, int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const Params p) {
+  constexpr bool kWgrad = (KIND == WGRAD_GU || KIND == WGRAD_D);
+  constexpr bool A_MN = kWgrad;
+  constexpr bool B_MN = (KIND == FWD_GATEUP || KIND == FWD_DOWN || kWgrad);
+  constexpr uint32_t A_BYTES = BM * BK * 2;
+  constexpr uint32_t B_BYTES = BN * BK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr uint32_t IDESC = make_idesc<BN, A_MN, B_MN>();
+  constexpr uint32_t MN_ATOM = 64 * 128;   // one [64 rows x 128 B] TMA box
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_mt = s_off + (p.E + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 4); }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB0)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB1)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
+  __syncthreads();
+  if constexpr (!kWgrad) {
+    // exclusive prefix of per-expert m-tile counts (warp 0)
+    if (warp == 0) {
+      int carry = 0;
+      for (int base = 0; base <= p.E; base += 32) {
+        const int i = base + lane;
+        const int v = (i < p.E) ? (s_off[i + 1] - s_off[i] + BM - 1) / BM : 0;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (i <= p.E) s_mt[i] = carry + x - v;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = kWgrad ? p.E * p.m_tiles * p.n_tiles : s_mt[p.E] * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<KIND, BN>(t, p, s_off, s_mt);
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t fb = full_bar(stage);
+          mbar_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          if constexpr (KIND == FWD_GATEUP) {
+            tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
+            const int yb = tl.e * p.d + kb * BK;
+#pragma unroll
+            for (int i = 0; i < BN / 128; ++i) {
+              tma_load_2d(sb + i * MN_ATOM, &tmB0, fb, tl.n0 + 64 * i, yb);
+              tma_load_2d(sb + (BN / 128 + i) * MN_ATOM, &tmB1, fb, tl.n0 + 64 * i, yb);
+            }
+          } else if constexpr (KIND == FWD_DOWN) {
+            tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
+            const int yb = tl.e * p.I + kb * BK;
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(sb + i * MN_ATOM, &tmB0, fb, tl.n0 + 64 * i, yb);
+          } else if constexpr (KIND == BWD_DH) {
+            tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
+            tma_load_2d(sb, &tmB0, fb, kb * BK, tl.e * p.I + tl.n0);
+          } else if constexpr (KIND == BWD_DX) {
+            tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
+            const int kx = kb * BK;
+            if (kx < p.I)
+              tma_load_2d(sb, &tmB0, fb, kx, tl.e * p.d + tl.n0);
+            else
+              tma_load_2d(sb, &tmB1, fb, kx - p.I, tl.e * p.d + tl.n0);
+          } else {  // weight gradients: both operands MN-major, K = token rows
+            const int ky = tl.row0 + kb * BK;
+            tma_load_2d(sa, &tmA, fb, tl.m0, ky);
+            tma_load_2d(sa + MN_ATOM, &tmA, fb, tl.m0 + 64, ky);
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(sb + i * MN_ATOM, &tmB0, fb, tl.n0 + 64 * i, ky);
+          }
+          issued[stage] += 1;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // make sure no TMA write into this CTA's shared memory is still in flight
+      for (int s = 0; s < STAGES; ++s) {
+        if (!issued[s]) continue;
+        const uint32_t par = (issued[s] - 1u) & 1u;
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(full_bar(s), par) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode_tile<KIND, BN>(t, p, s_off, s_mt);
+      if (tl.nkb == 0) continue;
+      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = 0; kb < tl.nkb; ++kb) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_base + stage * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+        if constexpr (kWgrad) {
+          const int kvalid = tl.rows - kb * BK;
+          if (kvalid < BK) {
+            // rows [kvalid, 64) of this k-block belong to the next expert: zero them in A
+            uint8_t* a_gen = smem + stage * STAGE_BYTES;
+            const int first = kvalid * 128;
+            for (int off = first + lane * 16; off < static_cast<int>(MN_ATOM); off += 32 * 16) {
+              *reinterpret_cast<uint4*>(a_gen + off) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(a_gen + MN_ATOM + off) = make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            uint64_t ad, bd;
+            if constexpr (A_MN) ad = smem_desc(sa + kk * 2048, MN_ATOM, 1024);
+            else ad = smem_desc(sa + kk * 32, 16, 1024);
+            if constexpr (B_MN) bd = smem_desc(sb + kk * 2048, MN_ATOM, 1024);
+            else bd = smem_desc(sb + kk * 32, 16, 1024);
+            tc_mma(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(tfull_bar(acc));
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    // all MMAs issued by this CTA complete before TMEM is released
+    if (lane == 0) {
+      tc_commit(drain_bar);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try(drain_bar, 0) && globaltimer() - t0 < kTimeoutNs) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                  // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;             // accumulator row of this thread
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode_tile<KIND, BN>(t, p, s_off, s_mt);
+      if constexpr (kWgrad) {
+        if (tl.nkb == 0) {     // expert without rows: its weight gradient is zero
+          float z[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) z[i] = 0.f;
+          const int m = tl.m0 + r;
+          for (int c = 0; c < BN; c += 16) {
+            const int n = tl.n0 + c;
+            if constexpr (KIND == WGRAD_GU) {
+              float* dst = (n < p.I) ? p.outf0 + (static_cast<size_t>(tl.e) * p.d + m) * p.I + n
+                                     : p.outf1 + (static_cast<size_t>(tl.e) * p.d + m) * p.I + (n - p.I);
+              store16_f32(dst, z);
+            } else {
+              store16_f32(p.outf0 + (static_cast<size_t>(tl.e) * p.I + m) * p.d + n, z);
+            }
+          }
+          continue;
+        }
+      }
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
+      if constexpr (KIND == FWD_GATEUP) {
+        constexpr int HALF = BN / 2;
+        const bool valid = r < tl.rows;
+        const size_t grow = static_cast<size_t>(tl.row0 + r);
+        for (int c = 0; c < HALF; c += 16) {
+          float g[16], u[16], h[16];
+          tmem_ld16(tacc + c, g);
+          tmem_ld16(tacc + HALF + c, u);
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) h[i] = silu_f(g[i]) * u[i];
+            store16_bf16(p.out + grow * p.I + tl.n0 + c, h);
+            if (p.out2) {
+              store16_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c, g);
+              store16_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c, u);
+            }
+          }
+        }
+      } else if constexpr (KIND == FWD_DOWN || KIND == BWD_DX) {
+        const bool valid = r < tl.rows;
+        const size_t grow = static_cast<size_t>(tl.row0 + r);
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(tacc + c, v);
+          tmem_wait_ld();
+          if (valid) store16_bf16(p.out + grow * p.ld_out + tl.n0 + c, v);
+        }
+      } else if constexpr (KIND == BWD_DH) {
+        const bool valid = r < tl.rows;
+        const size_t grow = static_cast<size_t>(tl.row0 + r);
+        for (int c = 0; c < BN; c += 16) {
+          float dh[16];
+          tmem_ld16(tacc + c, dh);
+          tmem_wait_ld();
+          if (valid) {
+            float g[16], u[16], dg[16], du[16];
+            const __nv_bfloat16* gurow = p.aux + grow * (2 * p.I);
+            load16_bf16(gurow + tl.n0 + c, g);
+            load16_bf16(gurow + p.I + tl.n0 + c, u);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float s = 1.f / (1.f + expf(-g[i]));
+              dg[i] = dh[i] * u[i] * s * (1.f + g[i] * (1.f - s));
+              du[i] = dh[i] * g[i] * s;
+            }
+            __nv_bfloat16* orow = p.out + grow * (2 * p.I);
+            store16_bf16(orow + tl.n0 + c, dg);
+            store16_bf16(orow + p.I + tl.n0 + c, du);
+          }
+        }
+      } else {  // weight gradients, fp32 out
+        const int m = tl.m0 + r;
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(tacc + c, v);
+          tmem_wait_ld();
+          const int n = tl.n0 + c;
+          if constexpr (KIND == WGRAD_GU) {
+            float* dst = (n < p.I) ? p.outf0 + (static_cast<size_t>(tl.e) * p.d + m) * p.I + n
+                                   : p.outf1 + (static_cast<size_t>(tl.e) * p.d + m) * p.I + (n - p.I);
+            store16_f32(dst, v);
+          } else {
+            store16_f32(p.outf0 + (static_cast<size_t>(tl.e) * p.I + m) * p.d + n, v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ----------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] array, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND, int BN, int STAGES>
+size_t smem_bytes(int E) {
+  return 1024 + STAGES * (BM * BK * 2 + BN * BK * 2) + 8 * (2 * STAGES + 5) + 16 +
+         sizeof(int) * 2 * (E + 1) + 16;
+}
+
+template <int KIND, int BN, int STAGES>
+int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
+           long long tiles_upper, cudaStream_t st) {
+  auto kern = grouped_gemm_kernel<KIND, BN, STAGES>;
+  const size_t sm = smem_bytes<KIND, BN, STAGES>(p.E);
+  static thread_local int configured = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<KIND, BN, STAGES>(1024)));
+    if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
+    configured = dev;
+  }
+  long long grid = num_sms();
+  if (tiles_upper < grid) grid = tiles_upper;
+  if (grid < 1) return MOE_OK;
+  static const char* kNames[] = {"gemm_gate_up", "gemm_down", "gemm_dh", "gemm_dx",
+                                 "gemm_wgrad_gate_up", "gemm_wgrad_down"};
+  ProfScope prof(kNames[KIND], st);
+  kern<<<static_cast<int>(grid), kThreads, sm, st>>>(a, b0, b1, p);
+  return check_launch();
+}
+
+constexpr int kStages256 = 4;
+constexpr int kStages128 = 6;
+
+template <int KIND>
+int launch_bn(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+              const Params& p, long long tiles_upper, cudaStream_t st) {
+  if (bn == 256) return launch<KIND, 256, kStages256>(a, b0, b1, p, tiles_upper, st);
+  return launch<KIND, 128, kStages128>(a, b0, b1, p, tiles_upper, st);
+}
+
+}  // namespace gemm
+
+size_t ffn_backward_scratch(long long M, int I) {
+  return static_cast<size_t>(M) * 2 * I * sizeof(uint16_t);
+}
+
+}  // namespace moe
+
+namespace {
+
+bool ffn_shape_ok(int E, int M, int d, int I) {
+  return E >= 1 && E <= 1024 && M >= 0 && d > 0 && I > 0 && d % 64 == 0 && I % 128 == 0;
+}
+
+}  // namespace
+
+extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E, int M, int d,
+                               int I, const moe_bf16* w_gate, const moe_bf16* w_up,
+                               const moe_bf16* w_down, moe_bf16* y, moe_bf16* h, moe_bf16* gu,
+                               void* ws, size_t ws_bytes, void* stream) {
+  using namespace moe;
+  using namespace moe::gemm;
+  if (!ffn_shape_ok(E, M, d, I)) {
+    if (E >= 1 && M >= 0 && d > 0 && I > 0 && d % 8 == 0 && I % 8 == 0) return MOE_ERR_UNSUPPORTED;
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (M == 0) return MOE_OK;
+  if (!xp || !offsets || !w_gate || !w_up || !w_down || !y || !h) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xp) || !aligned16(offsets) || !aligned16(w_gate) || !aligned16(w_up) ||
+      !aligned16(w_down) || !aligned16(y) || !aligned16(h) || (gu && !aligned16(gu)))
+    return MOE_ERR_MISALIGNED;
+  if (!ws || ws_bytes < kWorkspaceHeader || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  if (cc_major() < 10) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  Params p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.M = M;
+  p.d = d;
+  p.I = I;
+  p.status = static_cast<int*>(ws);
+  const long long mt_upper = (M + BM - 1) / BM + E;
+  CUtensorMap ta, tb0, tb1;
+  // gate/up projection with the SwiGLU epilogue
+  if (!make_map(&ta, xp, d, M, 64, BM) || !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, 64) ||
+      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, 64))
+    return MOE_ERR_CUDA;
+  p.n_tiles = I / 128;
+  p.k_blocks = d / BK;
+  p.out = reinterpret_cast<__nv_bfloat16*>(h);
+  p.out2 = reinterpret_cast<__nv_bfloat16*>(gu);
+  p.ld_out = I;
+  int rc = launch_bn<FWD_GATEUP>(256, ta, tb0, tb1, p, mt_upper * p.n_tiles, st);
+  if (rc) return rc;
+  // down projection
+  const int bn = (d % 256 == 0) ? 256 : 128;
+  if (!make_map(&ta, h, I, M, 64, BM) || !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, 64))
+    return MOE_ERR_CUDA;
+  p.n_tiles = d / bn;
+  p.k_blocks = I / BK;
+  p.out = reinterpret_cast<__nv_bfloat16*>(y);
+  p.out2 = nullptr;
+  p.ld_out = d;
+  return launch_bn<FWD_DOWN>(bn, ta, tb0, tb0, p, mt_upper * p.n_tiles, st);
+}
+
+extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
+                                        const moe_bf16* h, const int32_t* offsets, int E, int M,
+                                        int d, int I, const moe_bf16* w_gate, const moe_bf16* w_up,
+                                        const moe_bf16* w_down, moe_bf16* dxp, float* dw_gate,
+                                        float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  using namespace moe;
+  using namespace moe::gemm;
+  if (!ffn_shape_ok(E, M, d, I) || d % 128 != 0) {
+    if (E >= 1 && M >= 0 && d > 0 && I > 0 && d % 8 == 0 && I % 8 == 0) return MOE_ERR_UNSUPPORTED;
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!offsets || !w_gate || !w_up || !w_down || !dw_gate || !dw_up || !dw_down)
+    return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!dy || !xp || !gu || !h || !dxp)) return MOE_ERR_INVALID_ARG;
+  if ((M > 0 && (!aligned16(dy) || !aligned16(xp) || !aligned16(gu) || !aligned16(h) ||
+                 !aligned16(dxp))) ||
+      !aligned16(offsets) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(dw_gate) || !aligned16(dw_up) || !aligned16(dw_down))
+    return MOE_ERR_MISALIGNED;
+  if (!ws || !aligned16(ws) || ws_bytes < kWorkspaceHeader + ffn_backward_scratch(M, I))
+    return MOE_ERR_WORKSPACE;
+  if (cc_major() < 10) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  const size_t wbytes = static_cast<size_t>(E) * d * I * sizeof(float);
+  if (M == 0) {
+    cudaMemsetAsync(dw_gate, 0, wbytes, st);
+    cudaMemsetAsync(dw_up, 0, wbytes, st);
+    cudaMemsetAsync(dw_down, 0, wbytes, st);
+    return check_launch();
+  }
+  auto dgu = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + kWorkspaceHeader);
+  Params p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.M = M;
+  p.d = d;
+  p.I = I;
+  p.status = static_cast<int*>(ws);
+  const long long mt_upper = (M + BM - 1) / BM + E;
+  CUtensorMap ta, tb0, tb1;
+  // dH = dY Wd^T with the SwiGLU backward epilogue -> [dG | dU]
+  const int bn_h = (I % 256 == 0) ? 256 : 128;
+  if (!make_map(&ta, dy, d, M, 64, BM) ||
+      !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h))
+    return MOE_ERR_CUDA;
+  p.n_tiles = I / bn_h;
+  p.k_blocks = d / BK;
+  p.out = dgu;
+  p.aux = reinterpret_cast<const __nv_bfloat16*>(gu);
+  p.ld_out = 2 * I;
+  int rc = launch_bn<BWD_DH>(bn_h, ta, tb0, tb0, p, mt_upper * p.n_tiles, st);
+  if (rc) return rc;
+  // dX = dG Wg^T + dU Wu^T
+  const int bn_x = (d % 256 == 0) ? 256 : 128;
+  if (!make_map(&ta, dgu, 2 * static_cast<uint64_t>(I), M, 64, BM) ||
+      !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, bn_x) ||
+      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, bn_x))
+    return MOE_ERR_CUDA;
+  p.n_tiles = d / bn_x;
+  p.k_blocks = 2 * I / BK;
+  p.out = reinterpret_cast<__nv_bfloat16*>(dxp);
+  p.aux = nullptr;
+  p.ld_out = d;
+  rc = launch_bn<BWD_DX>(bn_x, ta, tb0, tb1, p, mt_upper * p.n_tiles, st);
+  if (rc) return rc;
+  // [dWg | dWu] = X^T [dG | dU]
+  if (!make_map(&ta, xp, d, M, 64, 64) || !make_map(&tb0, dgu, 2 * static_cast<uint64_t>(I), M, 64, 64))
+    return MOE_ERR_CUDA;
+  p.m_tiles = d / BM;
+  p.n_tiles = 2 * I / 256;
+  p.outf0 = dw_gate;
+  p.outf1 = dw_up;
+  p.out = nullptr;
+  rc = launch_bn<WGRAD_GU>(256, ta, tb0, tb0, p, static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
+  if (rc) return rc;
+  // dWd = H^T dY
+  const int bn_d = (d % 256 == 0) ? 256 : 128;
+  if (!make_map(&ta, h, I, M, 64, 64) || !make_map(&tb0, dy, d, M, 64, 64)) return MOE_ERR_CUDA;
+  p.m_tiles = I / BM;
+  p.n_tiles = d / bn_d;
+  p.outf0 = dw_down;
+  p.outf1 = nullptr;
+  return launch_bn<WGRAD_D>(bn_d, ta, tb0, tb0, p, static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
+}

@@ -1,0 +1,175 @@
+"""One MoE layer's forward and backward on one GPU, as a fixed sequence of
+library calls on the current CUDA stream with every buffer preallocated.
+
+Forward:  moe_route_topk -> moe_build_permutation -> moe_ep_layout (one
+          device-to-host copy of the splits) -> moe_dispatch ->
+          moe_grouped_ffn (routed experts; shared experts as E=1 on x) ->
+          moe_combine.
+Backward: moe_combine_backward -> moe_grouped_ffn_backward (routed; shared)
+          -> moe_dispatch_backward -> moe_route_topk_backward.
+
+This module only allocates tensors and orders the calls; each step is a
+kernel of libmoe_gb300.so.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional
+
+import torch
+
+from . import binding as B
+
+
+class MoELayer:
+    def __init__(self, T: int, d: int, E: int, K: int, I: int, R: int,
+                 weights: Dict[str, torch.Tensor], renorm: int = 1,
+                 device: Optional[torch.device] = None):
+        self.T, self.d, self.E, self.K, self.I, self.R = T, d, E, K, I, R
+        self.renorm = renorm
+        dev = torch.device(device) if device is not None else weights["w_gate"].device
+        self.device = dev
+        self.w = weights
+        self.shared = "ws_gate" in weights
+        TK = T * K
+        bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+        e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        # forward buffers
+        self.topk_idx, self.topk_w = e(T, K, dt=i32), e(T, K, dt=f32)
+        self.counts, self.offsets = e(E, dt=i32), e(E + 1, dt=i32)
+        self.perm, self.inv_perm = e(TK, dt=i32), e(TK, dt=i32)
+        n_split = R * E + R * R
+        self.ep_splits = e(n_split, dt=i32)
+        self.send_index, self.a2a_index, self.regroup_index = (e(TK, dt=i32) for _ in range(3))
+        self.host_splits = torch.empty(n_split, dtype=i32, pin_memory=True)
+        self.xp = e(TK, d, dt=bf)
+        self.y, self.h, self.gu = e(TK, d, dt=bf), e(TK, I, dt=bf), e(TK, 2 * I, dt=bf)
+        self.out = e(T, d, dt=bf)
+        self.ws_perm = B.new_workspace(B.workspace_size(B.MOE_OP_BUILD_PERMUTATION, T, E, K), dev)
+        self.ws_ep = B.new_workspace(B.workspace_size(B.MOE_OP_EP_LAYOUT, T, E, K, R), dev)
+        self.ws_ffn = B.new_workspace(B.workspace_size(B.MOE_OP_GROUPED_FFN, T, E, K, 1, d, I), dev)
+        # backward buffers
+        self.dy, self.dtopk_w = e(TK, d, dt=bf), e(T, K, dt=f32)
+        self.dxp = e(TK, d, dt=bf)
+        self.dw_gate, self.dw_up = e(E, d, I, dt=f32), e(E, d, I, dt=f32)
+        self.dw_down = e(E, I, d, dt=f32)
+        self.dx, self.dlogits = e(T, d, dt=bf), e(T, E, dt=f32)
+        self.ws_bwd = B.new_workspace(
+            B.workspace_size(B.MOE_OP_GROUPED_FFN_BACKWARD, T, E, K, 1, d, I), dev)
+        if self.shared:
+            Is = weights["ws_gate"].shape[1]
+            self.Is = Is
+            self.ws_g = weights["ws_gate"].unsqueeze(0)
+            self.ws_u = weights["ws_up"].unsqueeze(0)
+            self.ws_d = weights["ws_down"].unsqueeze(0)
+            self.s_offsets = torch.tensor([0, T], dtype=i32, device=dev)
+            self.ys, self.hs, self.gus = e(T, d, dt=bf), e(T, Is, dt=bf), e(T, 2 * Is, dt=bf)
+            self.dxs = e(T, d, dt=bf)
+            self.dws_gate, self.dws_up = e(1, d, Is, dt=f32), e(1, d, Is, dt=f32)
+            self.dws_down = e(1, Is, d, dt=f32)
+            self.ws_sfwd = B.new_workspace(B.workspace_size(B.MOE_OP_GROUPED_FFN, T, 1, 1, 1, d, Is), dev)
+            self.ws_sbwd = B.new_workspace(
+                B.workspace_size(B.MOE_OP_GROUPED_FFN_BACKWARD, T, 1, 1, 1, d, Is), dev)
+        self.logits = None
+        self.x = None
+        self.timeline: Optional[List] = None   # when a list, (name, start_event, end_event) per call
+
+    # -------------------------------------------------------------- timing hooks
+    def _mark(self, name):
+        if self.timeline is None:
+            return None
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(torch.cuda.current_stream(self.device))
+        return (name, ev)
+
+    def _close(self, tok):
+        if tok is None:
+            return
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(torch.cuda.current_stream(self.device))
+        self.timeline.append((tok[0], tok[1], ev))
+
+    def _run(self, name, fn, *a, **k):
+        tok = self._mark(name)
+        r = fn(*a, **k)
+        self._close(tok)
+        return r
+
+    # -------------------------------------------------------------- passes
+    def forward(self, logits: torch.Tensor, x: torch.Tensor, copy_splits: bool = True):
+        self.logits, self.x = logits, x
+        w = self.w
+        K, E, R = self.K, self.E, self.R
+        self._run("route_topk", B.moe_route_topk, logits, K, self.renorm,
+                  out=(self.topk_idx, self.topk_w))
+        self._run("build_permutation", B.moe_build_permutation, self.topk_idx, E, ws=self.ws_perm,
+                  out=(self.counts, self.offsets, self.perm, self.inv_perm))
+        self._run("ep_layout", B.moe_ep_layout, self.topk_idx, E, R,
+                  host_splits=self.host_splits if copy_splits else False, ws=self.ws_ep,
+                  out=(self.ep_splits, self.send_index, self.a2a_index, self.regroup_index))
+        self._run("dispatch", B.moe_dispatch, x, self.perm, K, out=self.xp)
+        self._run("grouped_ffn", B.moe_grouped_ffn, self.xp, self.offsets, w["w_gate"], w["w_up"],
+                  w["w_down"], ws=self.ws_ffn, out=(self.y, self.h, self.gu))
+        shared_y = None
+        if self.shared:
+            self._run("shared_ffn", B.moe_grouped_ffn, x, self.s_offsets, self.ws_g, self.ws_u,
+                      self.ws_d, ws=self.ws_sfwd, out=(self.ys, self.hs, self.gus))
+            shared_y = self.ys
+        self._run("combine", B.moe_combine, self.y, self.topk_w, self.inv_perm, shared_y,
+                  out=self.out)
+        return self.out
+
+    def backward(self, dout: torch.Tensor):
+        w = self.w
+        self._run("combine_backward", B.moe_combine_backward, dout, self.y, self.topk_w,
+                  self.inv_perm, out=(self.dy, self.dtopk_w))
+        self._run("grouped_ffn_backward", B.moe_grouped_ffn_backward, self.dy, self.xp, self.gu,
+                  self.h, self.offsets, w["w_gate"], w["w_up"], w["w_down"], ws=self.ws_bwd,
+                  out=(self.dxp, self.dw_gate, self.dw_up, self.dw_down))
+        dxs = None
+        if self.shared:
+            self._run("shared_ffn_backward", B.moe_grouped_ffn_backward, dout, self.x, self.gus,
+                      self.hs, self.s_offsets, self.ws_g, self.ws_u, self.ws_d, ws=self.ws_sbwd,
+                      out=(self.dxs, self.dws_gate, self.dws_up, self.dws_down))
+            dxs = self.dxs
+        self._run("dispatch_backward", B.moe_dispatch_backward, self.dxp, self.inv_perm, self.T,
+                  self.K, dxs, out=self.dx)
+        self._run("route_topk_backward", B.moe_route_topk_backward,
+                  None if self.renorm else self.logits, self.topk_idx, self.topk_w, self.dtopk_w,
+                  self.E, self.renorm, out=self.dlogits)
+        return self.dx
+
+    def step_from_host(self, logits_h: torch.Tensor, x_h: torch.Tensor, dout_h: torch.Tensor,
+                       out_h: torch.Tensor, dx_h: torch.Tensor):
+        """One forward + backward whose inputs start in (pinned) host memory and
+        whose outputs end there: copies in, runs the layer, copies out, all
+        enqueued on the current stream. Returns the bytes copied each way."""
+        if not hasattr(self, "_in_logits"):
+            self._in_logits = torch.empty(self.T, self.E, dtype=torch.float32, device=self.device)
+            self._in_x = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=self.device)
+            self._in_dout = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=self.device)
+        self._in_logits.copy_(logits_h, non_blocking=True)
+        self._in_x.copy_(x_h, non_blocking=True)
+        self._in_dout.copy_(dout_h, non_blocking=True)
+        out = self.forward(self._in_logits, self._in_x)
+        dx = self.backward(self._in_dout)
+        out_h.copy_(out, non_blocking=True)
+        dx_h.copy_(dx, non_blocking=True)
+        h2d = logits_h.numel() * 4 + x_h.numel() * 2 + dout_h.numel() * 2
+        d2h = out_h.numel() * 2 + dx_h.numel() * 2 + self.host_splits.numel() * 4
+        return h2d, d2h
+
+    def device_status(self) -> int:
+        """First nonzero device status among the GEMM workspaces (synchronises)."""
+        wss = [self.ws_ffn, self.ws_bwd] + ([self.ws_sfwd, self.ws_sbwd] if self.shared else [])
+        for ws in wss:
+            s = B.moe_read_device_status(ws)
+            if s:
+                return s
+        return 0
+
+
+def layer_from_config(cfg, inputs: Dict[str, torch.Tensor], device) -> MoELayer:
+    """Copies a workload's weights to ``device`` and builds the layer."""
+    keys = ["w_gate", "w_up", "w_down"] + (["ws_gate", "ws_up", "ws_down"] if cfg.shared_I else [])
+    weights = {k: inputs[k].to(device).contiguous() for k in keys}
+    return MoELayer(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.R, weights, cfg.renorm, device)

@@ -1,0 +1,252 @@
+/*
+ * moe_gb300.h -- C ABI of the single-GPU MoE-layer hot path for GB300 (sm_103a).
+ *
+ * One mixture-of-experts layer on one GPU: router top-k, per-expert histogram
+ * and offsets, stable expert-major permutation, the layout of an all-to-all
+ * over R simulated expert-parallel ranks, dispatch gather, grouped SwiGLU
+ * expert GEMMs (tcgen05 tensor cores), weighted combine, and the backward of
+ * each step.
+ *
+ * Sources (cited by page title and section):
+ *   [TAS] "Three axes of Parallelism" (nanoTitan blog), section "Expert
+ *         Parallel (EP)": "Mapping experts to EP ranks", "Producing
+ *         assignments", "Dispatch, expert computation and combine",
+ *         "EP backward pass".
+ *   [MOD] modalities PR "feat(parallelism): expert parallelism for the
+ *         Nemotron-3 Nano MoE layers", section "Design".
+ *   [SF]  SpecForge PR "(fsdp2 dev.) feat(moe): expert parallelism for MoE
+ *         drafters on the FSDP2 backend", section "What this adds".
+ *
+ * Conventions for every entry point
+ *   - Pointers named for tensors are DEVICE pointers unless the name says
+ *     host. The caller allocates and owns all memory; the library allocates
+ *     nothing and keeps no state between calls (apart from a cached driver
+ *     entry point and per-device attributes).
+ *   - Tensors are dense, row-major, with 16-byte aligned base addresses.
+ *     bf16 data are IEEE bfloat16 bit patterns stored as uint16_t.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Every call only enqueues work on that stream and returns; no
+ *     call synchronises with the device.
+ *   - Notation: T tokens, d hidden size, E routed experts, K experts per token,
+ *     I expert intermediate size, R simulated ranks, TK = T*K assignments,
+ *     flat assignment index a = t*K + j ([TAS] "Producing assignments":
+ *     token 0's K slots first), p = position in expert-major order.
+ *   - Return value: a moe_status code. Argument errors are detected on the
+ *     host before anything is enqueued. MOE_ERR_CUDA reports a launch error
+ *     (the cudaError_t is kept in moe_last_cuda_error()). Errors that only a
+ *     running kernel can see (a wait that timed out) are written to the
+ *     status word at the start of the workspace; read it with
+ *     moe_read_device_status.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,      /* null pointer, bad dimension or relation between them */
+  MOE_ERR_MISALIGNED = 2,       /* a pointer is not 16-byte aligned */
+  MOE_ERR_WORKSPACE = 3,        /* workspace missing or smaller than moe_workspace_size */
+  MOE_ERR_UNSUPPORTED = 4,      /* shape outside what the kernels implement, or no sm_100+ GPU */
+  MOE_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 6,   /* a bounded device-side wait ran out (read from the workspace) */
+  MOE_ERR_DEVICE_CHECK = 7      /* a device-side consistency check failed (read from the workspace) */
+};
+
+/* Workspace operation ids for moe_workspace_size. */
+enum moe_op {
+  MOE_OP_BUILD_PERMUTATION = 1,
+  MOE_OP_EP_LAYOUT = 2,
+  MOE_OP_GROUPED_FFN = 3,
+  MOE_OP_GROUPED_FFN_BACKWARD = 4
+};
+
+/* Bytes of device workspace the operation needs for these sizes (0 on bad
+ * arguments). The first 256 bytes of every workspace are a header whose
+ * first int32 is the device status word. Zero the header once before first
+ * use (for example by allocating the workspace zero-filled); the library only
+ * ever writes a nonzero code into it and moe_read_device_status clears it.
+ * A workspace may be reused by consecutive calls on one stream; calls that
+ * run concurrently need separate workspaces. */
+size_t moe_workspace_size(int op, int T, int E, int K, int R, int d, int I);
+
+/* A1. Router top-k ([TAS] "Producing assignments": the router scores every
+ * token against all E experts; top-K selection gives expert_IDs and
+ * router_weights, both [T,K]).
+ *   logits   [T,E] fp32 in.
+ *   topk_idx [T,K] int32 out: slot j holds the token's j-th best expert by
+ *            logit, equal logits ordered by ascending expert id (float
+ *            comparison, so -0.0 ties +0.0).
+ *   topk_w   [T,K] fp32 out: softmax over all E logits at the selected ids;
+ *            if renorm != 0 divided by their sum over the K selected
+ *            (equivalently a softmax over the K selected logits).
+ * Limits: 1 <= K <= min(E, 32), E <= 1024, T >= 0. Logits must be finite. */
+int moe_route_topk(const float* logits, int T, int E, int K, int renorm,
+                   int32_t* topk_idx, float* topk_w, void* stream);
+
+/* B4. Backward of moe_route_topk: dlogits [T,E] fp32 out (every element written).
+ *   renorm != 0: dlogits[t,e_j] = w_j (dw_j - sum_m w_m dw_m), 0 for experts not
+ *                selected; logits may be NULL.
+ *   renorm == 0: dlogits[t,i] = p_i (g_i - sum_j w_j dw_j), p = softmax(logits[t]),
+ *                g_i = dw_j where i = e_j else 0; logits [T,E] required.
+ *   topk_idx, topk_w, dtopk_w: [T,K] as produced by / the gradient of moe_route_topk. */
+int moe_route_topk_backward(const float* logits, const int32_t* topk_idx, const float* topk_w,
+                            const float* dtopk_w, int T, int E, int K, int renorm,
+                            float* dlogits, void* stream);
+
+/* A2 + A3. Per-expert histogram, offsets and stable expert-major permutation
+ * ([TAS] "Producing assignments": count assignments per expert, offsets from
+ * the cumulative counts, pack expert-major; [MOD] "Design" item 1: built
+ * entirely on device, no host round trip).
+ *   topk_idx [TK] int32 in, values in [0,E).
+ *   counts   [E] int32 out: assignments per expert.
+ *   offsets  [E+1] int32 out: offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e].
+ *   perm     [TK] int32 out: perm[p] = a, sorted by expert id with ties in
+ *            ascending a (stable), so expert e owns [offsets[e], offsets[e+1]).
+ *   inv_perm [TK] int32 out: inv_perm[a] = p.
+ *   ws, ws_bytes: workspace of moe_workspace_size(MOE_OP_BUILD_PERMUTATION, T,E,K,1,0,0).
+ * Limits: E <= 1024, T*K < 2^31. Ids outside [0,E) are undefined behaviour. */
+int moe_build_permutation(const int32_t* topk_idx, int T, int E, int K,
+                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* A4. Layout of one dispatch all-to-all over R simulated expert-parallel ranks
+ * ([TAS] "Mapping experts to EP ranks": rank i owns experts
+ * [i*E/R, (i+1)*E/R); "Dispatch, expert computation and combine": per-rank
+ * expert counts reshaped into a send matrix, a source-major receive buffer,
+ * then a regroup so each local expert's rows are contiguous; [MOD] "Design"
+ * items 1-2: indices built on device, exactly one device-to-host copy of the
+ * splits). Simulated rank s owns tokens [s*T/R, (s+1)*T/R).
+ *   ep_splits [R*E + R*R] int32 out: first R*E entries C[s,e] = assignments of
+ *             rank s routed to expert e; then R*R entries S[s,dst] = assignments
+ *             rank s sends to rank dst.
+ *   send_index    [TK] int32 out: send position q -> a. Rank s's send block
+ *                 starts at s*TK/R and is packed by (expert, a).
+ *   a2a_index     [TK] int32 out: receive position r -> q. Receive buffers are
+ *                 concatenated over destinations; each is source-major and each
+ *                 source's rows keep its packed (expert, a) order.
+ *   regroup_index [TK] int32 out: expert-major position p -> r. Within a
+ *                 destination, rows are ordered (local expert, source, a); this
+ *                 is the same order as moe_build_permutation's perm, so
+ *                 send_index[a2a_index[regroup_index[p]]] == perm[p].
+ *   host_splits   HOST pointer, page-locked, [R*E + R*R] int32, or NULL. When
+ *                 non-NULL exactly one cudaMemcpyAsync device-to-host of
+ *                 ep_splits is enqueued; it is complete once the stream is.
+ * Limits: R divides E and T, E <= 1024, R <= 64. */
+int moe_ep_layout(const int32_t* topk_idx, int T, int E, int K, int R,
+                  int32_t* ep_splits, int32_t* send_index, int32_t* a2a_index,
+                  int32_t* regroup_index, int32_t* host_splits,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* A5. Dispatch gather ([TAS] "Producing assignments": the assignment buffer
+ * in expert-major order; [MOD] "Design": the index_select half of the
+ * permutation pair): xp[p] = x[perm[p] / K], an exact copy.
+ *   x [T,d] bf16 in, perm [TK] int32 in, xp [TK,d] bf16 out. d % 8 == 0. */
+int moe_dispatch(const moe_bf16* x, int T, int d, int K, const int32_t* perm,
+                 moe_bf16* xp, void* stream);
+
+/* A6. Grouped SwiGLU experts ([TAS] "Mapping experts to EP ranks": stacked
+ * W_gate [E,d,I], W_val [E,d,I], W_out [E,I,d]; "Dispatch, expert
+ * computation and combine": each expert is an independent MLP over its
+ * contiguous rows). For expert e on rows [offsets[e], offsets[e+1]):
+ *   G = X Wg[e], U = X Wu[e] (fp32 accumulation), H = bf16(silu(G) * U),
+ *   Y = bf16(H Wd[e]); optionally GU = bf16([G | U]) is saved for backward.
+ *   xp      [M,d] bf16 in (M rows in total, M = offsets[E]).
+ *   offsets [E+1] int32 in (device), non-decreasing, offsets[0] = 0, offsets[E] = M.
+ *   w_gate, w_up [E,d,I] bf16; w_down [E,I,d] bf16.
+ *   y  [M,d] bf16 out.   h [M,I] bf16 out (needed by the down projection).
+ *   gu [M,2I] bf16 out, or NULL to skip saving it.
+ *   ws: moe_workspace_size(MOE_OP_GROUPED_FFN, ...), status word only.
+ * Limits: d % 64 == 0, I % 128 == 0, E <= 1024. Also used with E = 1 and
+ * offsets {0, T} for always-on shared experts ([SF] "What this adds"). */
+int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E, int M, int d, int I,
+                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                    moe_bf16* y, moe_bf16* h, moe_bf16* gu,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* B2. Backward of moe_grouped_ffn ([TAS] "EP backward pass": expert gradients
+ * stay with the expert's owner; here they are the exact derivative of this
+ * layer, with no 1/R scaling). Per expert, with G, U from the saved gu:
+ *   dH = dY Wd^T; s = sigmoid(G); dG = bf16(dH U s (1 + G (1 - s)));
+ *   dU = bf16(dH G s); dX = bf16(dG Wg^T + dU Wu^T);
+ *   dWd = H^T dY, dWg = X^T dG, dWu = X^T dU (fp32, written for every expert,
+ *   zero for experts with no rows).
+ *   dy [M,d], xp [M,d], gu [M,2I], h [M,I] bf16 in; offsets and weights as in
+ *   moe_grouped_ffn. dxp [M,d] bf16 out; dw_gate, dw_up [E,d,I] fp32 out;
+ *   dw_down [E,I,d] fp32 out.
+ *   ws: moe_workspace_size(MOE_OP_GROUPED_FFN_BACKWARD, T,E,K,R,d,I) with
+ *   T*K = M; holds [dG | dU] as bf16 [M,2I]. */
+int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
+                             const moe_bf16* h, const int32_t* offsets, int E, int M, int d,
+                             int I, const moe_bf16* w_gate, const moe_bf16* w_up,
+                             const moe_bf16* w_down, moe_bf16* dxp, float* dw_gate,
+                             float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/* A7. Combine ([TAS] "Dispatch, expert computation and combine", last
+ * paragraph: undo the packing with the saved indices, weight each expert
+ * output by its router weight, sum the K outputs; [SF] "What this adds": the
+ * shared experts' output is added on the local tokens):
+ *   out[t] = bf16( sum_{j<K} topk_w[t,j] * y[inv_perm[t*K+j]] + shared_y[t] ),
+ *   fp32 accumulation in slot order, no atomics.
+ *   y [TK,d] bf16, topk_w [T,K] fp32, inv_perm [TK] int32, shared_y [T,d] bf16
+ *   or NULL; out [T,d] bf16. d % 8 == 0. */
+int moe_combine(const moe_bf16* y, const float* topk_w, const int32_t* inv_perm, int T, int K,
+                int d, const moe_bf16* shared_y, moe_bf16* out, void* stream);
+
+/* B1. Backward of moe_combine: for a = t*K + j and p = inv_perm[a],
+ *   dy[p] = bf16(topk_w[a] * dout[t]) (rows in expert-major order),
+ *   dtopk_w[a] = sum_c dout[t,c] * y[p,c] (fp32).
+ *   dout [T,d] bf16, y [TK,d] bf16, topk_w [T,K] fp32, inv_perm [TK] int32 in;
+ *   dy [TK,d] bf16 out, dtopk_w [T,K] fp32 out. */
+int moe_combine_backward(const moe_bf16* dout, const moe_bf16* y, const float* topk_w,
+                         const int32_t* inv_perm, int T, int K, int d, moe_bf16* dy,
+                         float* dtopk_w, void* stream);
+
+/* B3. Backward of moe_dispatch ([MOD] "Design": the index_copy transpose):
+ *   dx[t] = bf16( sum_{j<K} dxp[inv_perm[t*K+j]] + dx_shared[t] ), fp32 sums.
+ *   dxp [TK,d] bf16, inv_perm [TK] int32, dx_shared [T,d] bf16 or NULL;
+ *   dx [T,d] bf16 out. */
+int moe_dispatch_backward(const moe_bf16* dxp, const int32_t* inv_perm, int T, int K, int d,
+                          const moe_bf16* dx_shared, moe_bf16* dx, void* stream);
+
+/* Per-launch timing (diagnostics). While recording is on, every kernel this
+ * library launches is bracketed by two cudaEventRecord calls on the stream it
+ * is launched on, so the caller can read each launch's device duration.
+ *   moe_profile_start(capacity): creates (or reuses) 2*capacity events on the
+ *     current device and starts recording; launches beyond capacity are not
+ *     recorded. Not thread-safe: record from one host thread.
+ *   moe_profile_stop(): stops recording; returns the number of records.
+ *   moe_profile_record(i, name, ms): synchronises record i's end event and
+ *     returns the launch's kernel name (static storage) and duration in ms. */
+int moe_profile_start(int capacity);
+int moe_profile_stop(void);
+int moe_profile_record(int i, const char** name, float* ms);
+
+/* Reads the workspace's device status word after synchronising `stream`,
+ * stores it in *host_status (a moe_status value, 0 if no kernel reported an
+ * error) and clears it. The only call in this library that synchronises. */
+int moe_read_device_status(void* ws, void* stream, int* host_status);
+
+/* Short English description of a moe_status code (static storage). */
+const char* moe_status_string(int status);
+
+/* cudaError_t of the most recent MOE_ERR_CUDA on this host thread (0 if none). */
+int moe_last_cuda_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

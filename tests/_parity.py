@@ -1,0 +1,63 @@
+"""Shared helpers of the GPU parity tests: building the library, moving seeded
+inputs to the device, and the tolerance checks the tests use.
+
+Tolerances (written here once, used by every GPU test):
+* integer / index outputs and the dispatch copy: bit-exact;
+* fp32 router weights: max |gpu - ref| <= 1e-5 * |ref| (relative, element-wise);
+* bf16 outputs of the expert GEMMs and of combine, and the backward's bf16 and
+  fp32 gradients: max |gpu - ref| <= 2e-2 * RMS(ref) per tensor;
+* fp32 dtopk_w and dlogits fed identical inputs: max |err| <= 1e-3 * RMS(ref).
+"""
+import numpy as np
+import torch
+
+from grouped_gemm_moe_gb300 import build as build_mod
+
+REL_W = 1e-5
+RMS_TOL = 2e-2
+RMS_TOL_SMALL = 1e-3
+
+_built = False
+
+
+def ensure_built():
+    global _built
+    if not _built:
+        build_mod.build()
+        _built = True
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def i64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").to(torch.int64).numpy()
+
+
+def to_dev(a, dtype) -> torch.Tensor:
+    if isinstance(a, np.ndarray):
+        a = torch.from_numpy(np.ascontiguousarray(a))
+    return a.to(dtype).to(dev()).contiguous()
+
+
+def assert_rms_close(got, ref, tol=RMS_TOL, name=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    rms = np.sqrt(np.mean(ref ** 2))
+    err = np.abs(got - ref).max() if ref.size else 0.0
+    assert np.isfinite(got).all(), name
+    assert err <= tol * rms + 1e-30, f"{name}: max|err|={err:.3e} > {tol}*RMS({rms:.3e})"
+    return err / rms if rms else 0.0
+
+
+def assert_rel_close(got, ref, tol=REL_W, name=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    assert (err <= tol * np.abs(ref) + 1e-30).all(), f"{name}: worst rel err {(err / np.abs(ref)).max():.3e}"

@@ -1,0 +1,202 @@
+"""GPU parity of the tcgen05 grouped SwiGLU GEMMs (forward and backward)
+against the CPU oracle: every element on small ragged problems, sampled rows
+and sampled weight-gradient columns at the workloads' full sizes. Tolerance:
+max |err| <= 2e-2 * RMS(reference) per tensor."""
+import numpy as np
+import pytest
+import torch
+
+from grouped_gemm_moe_gb300 import binding as B
+from grouped_gemm_moe_gb300 import workloads as W
+from oracle import moe_oracle as O
+
+from _parity import assert_rms_close, ensure_built, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def _bf16(shape, gen, scale=1.0):
+    return (torch.randn(*shape, generator=gen) * scale).to(torch.bfloat16)
+
+
+def _problem(counts, d, I, seed):
+    g = torch.Generator().manual_seed(seed)
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M = int(off[-1])
+    xp = _bf16((M, d), g)
+    wg = _bf16((E, d, I), g, 0.02)
+    wu = _bf16((E, d, I), g, 0.02)
+    wd = _bf16((E, I, d), g, 0.02)
+    return off, xp, wg, wu, wd
+
+
+SMALL = [
+    # (counts per expert, d, I)
+    ([40, 0, 300, 1, 127, 128, 129, 64], 128, 256),
+    ([513, 255, 0, 0, 77], 256, 384),
+    ([1000], 512, 128),
+    ([63, 65, 200, 1, 0, 319], 384, 512),
+    ([0, 0, 0, 5], 256, 256),
+]
+
+
+@pytest.mark.parametrize("counts,d,I", SMALL)
+def test_grouped_ffn_forward_small(counts, d, I):
+    off, xp, wg, wu, wd = _problem(counts, d, I, sum(counts) + d)
+    y, h, gu = B.moe_grouped_ffn(to_dev(xp, torch.bfloat16), to_dev(off, torch.int32),
+                                 to_dev(wg, torch.bfloat16), to_dev(wu, torch.bfloat16),
+                                 to_dev(wd, torch.bfloat16))
+    ry, rgu, rh = O.grouped_ffn(xp.double().numpy(), off, wg.double().numpy(),
+                                wu.double().numpy(), wd.double().numpy())
+    assert_rms_close(f64(h), rh, name="h")
+    assert_rms_close(f64(gu), rgu, name="gu")
+    assert_rms_close(f64(y), ry, name="y")
+
+
+@pytest.mark.parametrize("counts,d,I", [c for c in SMALL if c[1] % 128 == 0])
+def test_grouped_ffn_backward_small(counts, d, I):
+    off, xp, wg, wu, wd = _problem(counts, d, I, 3 * sum(counts) + I)
+    g = torch.Generator().manual_seed(11)
+    M = int(off[-1])
+    dy = _bf16((M, d), g, 0.1)
+    gu = _bf16((M, 2 * I), g, 1.0)
+    h = _bf16((M, I), g, 0.5)
+    dxp, dwg, dwu, dwd = B.moe_grouped_ffn_backward(
+        to_dev(dy, torch.bfloat16), to_dev(xp, torch.bfloat16), to_dev(gu, torch.bfloat16),
+        to_dev(h, torch.bfloat16), to_dev(off, torch.int32), to_dev(wg, torch.bfloat16),
+        to_dev(wu, torch.bfloat16), to_dev(wd, torch.bfloat16))
+    r = O.grouped_ffn_backward(dy.double().numpy(), xp.double().numpy(), gu.double().numpy(),
+                               h.double().numpy(), off, wg.double().numpy(), wu.double().numpy(),
+                               wd.double().numpy())
+    assert_rms_close(f64(dxp), r[0], name="dxp")
+    assert_rms_close(f64(dwg), r[1], name="dw_gate")
+    assert_rms_close(f64(dwu), r[2], name="dw_up")
+    assert_rms_close(f64(dwd), r[3], name="dw_down")
+    for e, c in enumerate(counts):
+        if c == 0:
+            assert (f64(dwg[e]) == 0).all() and (f64(dwd[e]) == 0).all()
+
+
+def test_shared_expert_as_single_group():
+    """E = 1 with offsets {0, T} is the dense always-on expert."""
+    T, d, Is = 700, 256, 2 * 384
+    g = torch.Generator().manual_seed(5)
+    x = _bf16((T, d), g)
+    wg, wu = _bf16((1, d, Is), g, 0.02), _bf16((1, d, Is), g, 0.02)
+    wd = _bf16((1, Is, d), g, 0.02)
+    off = np.array([0, T], np.int32)
+    y, h, gu = B.moe_grouped_ffn(to_dev(x, torch.bfloat16), to_dev(off, torch.int32),
+                                 to_dev(wg, torch.bfloat16), to_dev(wu, torch.bfloat16),
+                                 to_dev(wd, torch.bfloat16), save_gu=False)
+    assert gu is None
+    ry, _, rh = O.swiglu_expert(x.double().numpy(), wg[0].double().numpy(), wu[0].double().numpy(),
+                                wd[0].double().numpy())
+    assert_rms_close(f64(y), ry, name="y")
+    assert_rms_close(f64(h), rh, name="h")
+
+
+# ------------------------------------------------------------ full workloads
+def _full(name):
+    cfg = W.CONFIGS[name]
+    inp = W.make_inputs(cfg, with_backward=False)
+    idx, _ = O.route_topk(inp["logits"].numpy(), cfg.K, 1)
+    counts, off = O.expert_counts_offsets(idx, cfg.E)
+    perm, _ = O.stable_permutation(idx, cfg.E)
+    return cfg, inp, counts, off.astype(np.int32), perm
+
+
+def _sample_rows(off, counts, n_per=3, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = []
+    nz = np.nonzero(counts)[0]
+    pick = set([int(nz[0]), int(nz[-1]), int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])])
+    pick |= set(rng.choice(nz, size=min(4, len(nz)), replace=False).tolist())
+    for e in sorted(pick):
+        lo, hi = int(off[e]), int(off[e + 1])
+        cand = {lo, hi - 1, min(lo + 127, hi - 1), min(lo + 128, hi - 1)}
+        cand |= set(rng.integers(lo, hi, size=n_per).tolist())
+        rows += [(e, p) for p in sorted(cand)]
+    return rows
+
+
+@pytest.mark.parametrize("name", ["qwen3", "dsv2lite", "skew", "drafter"])
+def test_grouped_ffn_forward_full_sampled(name):
+    cfg, inp, counts, off, perm = _full(name)
+    K = cfg.K
+    dxd = to_dev(inp["x"], torch.bfloat16)
+    xp = B.moe_dispatch(dxd, to_dev(perm, torch.int32), K)
+    wg, wu, wd = (to_dev(inp[k], torch.bfloat16) for k in ("w_gate", "w_up", "w_down"))
+    y, h, gu = B.moe_grouped_ffn(xp, to_dev(off, torch.int32), wg, wu, wd)
+    torch.cuda.synchronize()
+    rows = _sample_rows(off, counts)
+    ps = torch.tensor([p for _, p in rows])
+    yg, hg, gug = f64(y[ps.to(y.device)]), f64(h[ps.to(h.device)]), f64(gu[ps.to(gu.device)])
+    ry, rh, rgu = [], [], []
+    x64 = inp["x"]
+    for (e, p) in rows:
+        X = x64[int(perm[p]) // K].double().numpy()[None]
+        a, b, c = O.swiglu_expert(X, inp["w_gate"][e].double().numpy(),
+                                  inp["w_up"][e].double().numpy(), inp["w_down"][e].double().numpy())
+        ry.append(a[0]); rgu.append(b[0]); rh.append(c[0])
+    assert_rms_close(yg, np.array(ry), name="y")
+    assert_rms_close(hg, np.array(rh), name="h")
+    assert_rms_close(gug, np.array(rgu), name="gu")
+
+
+@pytest.mark.parametrize("name", ["qwen3", "dsv2lite", "skew", "drafter"])
+def test_grouped_ffn_backward_full_sampled(name):
+    cfg, inp, counts, off, perm = _full(name)
+    K, d, I, E = cfg.K, cfg.d, cfg.I, cfg.E
+    M = cfg.TK
+    g = torch.Generator().manual_seed(21)
+    dy = _bf16((M, d), g, 0.1)
+    gu = _bf16((M, 2 * I), g, 1.0)
+    h = _bf16((M, I), g, 0.5)
+    xd = to_dev(inp["x"], torch.bfloat16)
+    xp = B.moe_dispatch(xd, to_dev(perm, torch.int32), K)
+    wg, wu, wd = (to_dev(inp[k], torch.bfloat16) for k in ("w_gate", "w_up", "w_down"))
+    dxp, dwg, dwu, dwd = B.moe_grouped_ffn_backward(
+        to_dev(dy, torch.bfloat16), xp, to_dev(gu, torch.bfloat16), to_dev(h, torch.bfloat16),
+        to_dev(off, torch.int32), wg, wu, wd)
+    torch.cuda.synchronize()
+    x = inp["x"]
+    # sampled rows of dxp
+    rows = _sample_rows(off, counts, n_per=2, seed=1)
+    ps = torch.tensor([p for _, p in rows])
+    got = f64(dxp[ps.to(dxp.device)])
+    ref = []
+    for (e, p) in rows:
+        X = x[int(perm[p]) // K].double().numpy()[None]
+        r = O.swiglu_expert_backward(dy[p:p + 1].double().numpy(), X, gu[p:p + 1].double().numpy(),
+                                     h[p:p + 1].double().numpy(), inp["w_gate"][e].double().numpy(),
+                                     inp["w_up"][e].double().numpy(), inp["w_down"][e].double().numpy())
+        ref.append(r[0][0])
+    assert_rms_close(got, np.array(ref), name="dxp rows")
+    # sampled columns of the weight gradients, restricted-column sub-problems of the oracle
+    rng = np.random.default_rng(2)
+    nz = np.nonzero(counts)[0]
+    experts = sorted(set([int(nz[0]), int(nz[-1]), int(nz[np.argmax(counts[nz])])]))
+    cols = np.sort(rng.choice(I, size=4, replace=False))
+    for e in experts:
+        lo, hi = int(off[e]), int(off[e + 1])
+        X = x[torch.from_numpy(perm[lo:hi] // K)].double().numpy()
+        GU = gu[lo:hi].double().numpy()
+        sub_gu = np.concatenate([GU[:, cols], GU[:, I + cols]], axis=1)
+        r = O.swiglu_expert_backward(dy[lo:hi].double().numpy(), X, sub_gu,
+                                     h[lo:hi, cols].double().numpy(),
+                                     inp["w_gate"][e][:, cols].double().numpy(),
+                                     inp["w_up"][e][:, cols].double().numpy(),
+                                     inp["w_down"][e][cols, :].double().numpy())
+        ci = torch.from_numpy(cols).to(dwg.device)
+        assert_rms_close(f64(dwg[e][:, ci]), r[1], name=f"dw_gate[{e}]")
+        assert_rms_close(f64(dwu[e][:, ci]), r[2], name=f"dw_up[{e}]")
+        assert_rms_close(f64(dwd[e][ci, :]), r[3], name=f"dw_down[{e}]")
+    empty = np.nonzero(counts == 0)[0]
+    for e in empty[:4]:
+        assert float(dwg[int(e)].abs().max()) == 0.0 and float(dwd[int(e)].abs().max()) == 0.0

@@ -62,6 +62,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's figure (replicas run the same work; the job is done
+    when the last one is)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(ms_per_step: float, tokens_per_rank: int, world: int) -> float:
+    """Whole-job tokens/s: every rank processes its own batch in ms_per_step."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -302,12 +319,8 @@ def main():
     barrier()
     records = B.moe_profile_stop()
     step_ms = [s.elapsed_time(e) for s, e in evs]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * cfg.T / (ms / 1e3)
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
+    value = aggregate_value(ms, cfg.T, world)
 
     # per-kernel table and the dominant kernel's roofline
     pk = peaks()
@@ -369,12 +382,8 @@ def main():
         e.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = s.elapsed_time(e) / args.steps
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * cfg.T / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        ems = max_over_ranks(s.elapsed_time(e) / args.steps, world, dev)
+        e2e = {"value": aggregate_value(ems, cfg.T, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems}
 
     cpu = None

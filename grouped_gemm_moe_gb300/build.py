@@ -1,9 +1,10 @@
 """Builds libmoe_gb300.so in-tree with nvcc for sm_103a.
 
 Each CUDA source compiles to an object in parallel, then one shared library
-is linked next to this file. The CUDA runtime is linked statically; the
-tensor-map encoder is fetched from the driver at run time, so nothing links
-against libcuda.
+is linked next to this file. The CUDA runtime is the shared libcudart (the
+one PyTorch has already loaded when the binding is used; otherwise found via
+the rpath); the tensor-map encoder is fetched from the driver at run time, so
+nothing links against libcuda.
 """
 from __future__ import annotations
 
@@ -65,7 +66,8 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
         list(ex.map(run, jobs))
     objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
     if force or jobs or not os.path.exists(LIB):
-        run([cc, *ARCH, "-shared", "-o", LIB, *objs])
+        run([cc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
+             "-o", LIB, *objs])
     return LIB
 
 

@@ -55,6 +55,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// bf16 of the exact product a*b, rounded once (to nearest, ties to even).
+// p = fl32(a*b) can only round differently from the exact product when p lies
+// exactly on a midpoint between two bf16 values; the FMA residual a*b - p
+// (exact) then says on which side the exact product lies, and p is nudged one
+// fp32 ulp that way before the bf16 rounding.
+__device__ __forceinline__ float mul_bf16_exact(float a, float b) {
+  const float p = a * b;
+  const float r = fmaf(a, b, -p);
+  uint32_t u = __float_as_uint(p);
+  if ((u & 0xffffu) == 0x8000u && r != 0.f) u += ((r > 0.f) == (p > 0.f)) ? 1u : 0xffffffffu;
+  return __uint_as_float(u);
+}
+
 __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
   f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
   f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);

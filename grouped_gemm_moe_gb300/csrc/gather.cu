@@ -95,6 +95,8 @@ gather_sum_kernel(const uint4* __restrict__ rows, const float* __restrict__ w,
 }
 
 // One warp per token: dy[p] = bf16(w[a] * dout[t]) and dw[a] = <dout[t], y[p]>.
+// dy is the exact product rounded once, so it is bit-identical to any
+// correctly rounded evaluation.
 __global__ void __launch_bounds__(kThreads)
 combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ y,
                         const float* __restrict__ w, const int32_t* __restrict__ inv_perm, int T,
@@ -119,7 +121,7 @@ combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict_
         unpack8(dv, fd);
         unpack8(yv, fy);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) { dot = fmaf(fd[q], fy[q], dot); g[q] = wa * fd[q]; }
+        for (int q = 0; q < 8; ++q) { dot = fmaf(fd[q], fy[q], dot); g[q] = mul_bf16_exact(wa, fd[q]); }
         stg_v4(dyrow + c, pack8(g));
       }
       dot = warp_sum(dot);

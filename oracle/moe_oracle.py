@@ -271,22 +271,29 @@ def _silu(z):
     return z / (1.0 + np.exp(-z))
 
 
-def swiglu_expert(X, Wg, Wu, Wd, exact: bool = False):
+def swiglu_expert(X, Wg, Wu, Wd, exact: bool = False, pre: bool = False):
     """One expert MLP on rows X [M,d]: G = X Wg, U = X Wu (exact sums),
-    saved GU = bf16([G | U]), H = bf16(silu(G) * U), Y = bf16(H Wd)."""
+    saved GU = bf16([G | U]), H = bf16(silu(G) * U), Y = bf16(H Wd).
+
+    ``pre=True`` returns each output's value just before its own bf16
+    rounding (Y still comes from the rounded H, as the method stores H)."""
     rnd = _rounder(exact)
     X = np.asarray(X, dtype=np.float64)
     G = X @ np.asarray(Wg, dtype=np.float64)
     U = X @ np.asarray(Wu, dtype=np.float64)
-    GU = rnd(np.concatenate([G, U], axis=1))
-    H = rnd(_silu(G) * U)
-    Y = rnd(H @ np.asarray(Wd, dtype=np.float64))
-    return Y, GU, H
+    GU = np.concatenate([G, U], axis=1)
+    Hx = _silu(G) * U
+    H = rnd(Hx)
+    Y = H @ np.asarray(Wd, dtype=np.float64)
+    if pre:
+        return Y, GU, Hx
+    return rnd(Y), rnd(GU), H
 
 
-def grouped_ffn(xp, offsets, Wg, Wu, Wd, exact: bool = False):
+def grouped_ffn(xp, offsets, Wg, Wu, Wd, exact: bool = False, pre: bool = False):
     """Expert e runs on packed rows [offsets[e], offsets[e+1]); empty experts
-    produce no rows. Returns y [TK,d], gu [TK,2I], h [TK,I]."""
+    produce no rows. Returns y [TK,d], gu [TK,2I], h [TK,I] (before their own
+    bf16 rounding when ``pre``)."""
     xp = np.asarray(xp, dtype=np.float64)
     E = len(offsets) - 1
     I = np.asarray(Wg).shape[-1]
@@ -299,16 +306,17 @@ def grouped_ffn(xp, offsets, Wg, Wu, Wd, exact: bool = False):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi == lo:
             continue
-        y[lo:hi], gu[lo:hi], h[lo:hi] = swiglu_expert(xp[lo:hi], Wg[e], Wu[e], Wd[e], exact)
+        y[lo:hi], gu[lo:hi], h[lo:hi] = swiglu_expert(xp[lo:hi], Wg[e], Wu[e], Wd[e], exact, pre)
     return y, gu, h
 
 
-def swiglu_expert_backward(dY, X, GU, H, Wg, Wu, Wd, exact: bool = False):
+def swiglu_expert_backward(dY, X, GU, H, Wg, Wu, Wd, exact: bool = False, pre: bool = False):
     """Backward of one expert MLP, G and U taken from the saved GU.
 
     dH = dY Wd^T; with s = sigmoid(G): dG = bf16(dH * U * s * (1 + G (1 - s))),
     dU = bf16(dH * G * s); dX = bf16(dG Wg^T + dU Wu^T);
-    dWd = H^T dY, dWg = X^T dG, dWu = X^T dU (exact sums).
+    dWd = H^T dY, dWg = X^T dG, dWu = X^T dU (exact sums). ``pre=True``
+    returns dX before its bf16 rounding (dG, dU stay rounded, as stored).
     """
     rnd = _rounder(exact)
     dY = np.asarray(dY, dtype=np.float64)
@@ -324,11 +332,14 @@ def swiglu_expert_backward(dY, X, GU, H, Wg, Wu, Wd, exact: bool = False):
     s = 1.0 / (1.0 + np.exp(-G))
     dG = rnd(dH * U * s * (1.0 + G * (1.0 - s)))
     dU = rnd(dH * G * s)
-    dX = rnd(dG @ Wg.T + dU @ Wu.T)
+    dX = dG @ Wg.T + dU @ Wu.T
+    if not pre:
+        dX = rnd(dX)
     return dX, X.T @ dG, X.T @ dU, H.T @ dY
 
 
-def grouped_ffn_backward(dy, xp, gu, h, offsets, Wg, Wu, Wd, exact: bool = False):
+def grouped_ffn_backward(dy, xp, gu, h, offsets, Wg, Wu, Wd, exact: bool = False,
+                         pre: bool = False):
     """Per-expert backward over the packed segments. Experts with no rows get
     zero weight gradients. Returns dxp [TK,d], dWg, dWu [E,d,I], dWd [E,I,d]."""
     E = len(offsets) - 1
@@ -344,7 +355,7 @@ def grouped_ffn_backward(dy, xp, gu, h, offsets, Wg, Wu, Wd, exact: bool = False
         if hi == lo:
             continue
         dxp[lo:hi], dWg[e], dWu[e], dWd[e] = swiglu_expert_backward(
-            dy[lo:hi], xp[lo:hi], gu[lo:hi], h[lo:hi], Wg[e], Wu[e], Wd[e], exact)
+            dy[lo:hi], xp[lo:hi], gu[lo:hi], h[lo:hi], Wg[e], Wu[e], Wd[e], exact, pre)
     return dxp, dWg, dWu, dWd
 
 
@@ -353,7 +364,7 @@ def grouped_ffn_backward(dy, xp, gu, h, offsets, Wg, Wu, Wd, exact: bool = False
 # ([TAS] "Dispatch, expert computation and combine", last paragraph;
 #  [MOD] index_select / index_copy pair; [SF] shared expert on local tokens)
 # --------------------------------------------------------------------------- #
-def combine(y, w, inv_perm, K: int, shared_y=None, exact: bool = False):
+def combine(y, w, inv_perm, K: int, shared_y=None, exact: bool = False, pre: bool = False):
     """out[t] = bf16( sum_j w[t,j] * y[inv_perm[t*K+j]] (+ shared_y[t]) ):
     undo the packing, weight each expert output by its router weight and sum
     the K outputs of each token; the shared experts' output is added unweighted."""
@@ -365,7 +376,7 @@ def combine(y, w, inv_perm, K: int, shared_y=None, exact: bool = False):
     acc = np.einsum("tk,tkd->td", w, rows)
     if shared_y is not None:
         acc = acc + np.asarray(shared_y, dtype=np.float64)
-    return rnd(acc)
+    return acc if pre else rnd(acc)
 
 
 def combine_backward(dout, y, w, inv_perm, K: int, exact: bool = False):
@@ -382,23 +393,27 @@ def combine_backward(dout, y, w, inv_perm, K: int, exact: bool = False):
     return dy, dw
 
 
-def dispatch_backward(dxp, inv_perm, K: int, T: int, dx_shared=None, exact: bool = False):
+def dispatch_backward(dxp, inv_perm, K: int, T: int, dx_shared=None, exact: bool = False,
+                      pre: bool = False):
     """dx[t] = bf16( sum_j dxp[inv_perm[t*K+j]] (+ dx_shared[t]) )."""
     rnd = _rounder(exact)
     dxp = np.asarray(dxp, dtype=np.float64)
     acc = dxp[np.asarray(inv_perm).reshape(T, K)].sum(axis=1)
     if dx_shared is not None:
         acc = acc + np.asarray(dx_shared, dtype=np.float64)
-    return rnd(acc)
+    return acc if pre else rnd(acc)
 
 
 # --------------------------------------------------------------------------- #
 # Whole layer
 # --------------------------------------------------------------------------- #
-def layer_forward(inp, K: int, R: int, renorm: int = 1, exact: bool = False):
+def layer_forward(inp, K: int, R: int, renorm: int = 1, exact: bool = False,
+                  pre: bool = False):
     """One MoE layer's forward on the inputs of ``workloads.make_inputs``
     converted to float64 numpy arrays (keys logits, x, w_gate, w_up, w_down,
-    optional ws_gate/ws_up/ws_down). Returns a dict of every intermediate."""
+    optional ws_gate/ws_up/ws_down). Returns a dict of every intermediate;
+    with ``pre`` it also holds y_pre, gu_pre, h_pre, out_pre: those outputs
+    before their own bf16 rounding."""
     logits = inp["logits"]
     T, E = logits.shape
     idx, w = route_topk(logits, K, renorm)
@@ -413,14 +428,21 @@ def layer_forward(inp, K: int, R: int, renorm: int = 1, exact: bool = False):
     out = combine(y, w, inv_perm, K, ys, exact)
     res = dict(topk_idx=idx, topk_w=w, counts=counts, offsets=offsets, perm=perm,
                inv_perm=inv_perm, xp=xp, y=y, gu=gu, h=h, out=out)
+    if pre:
+        res["y_pre"], res["gu_pre"], res["h_pre"] = grouped_ffn(
+            xp, offsets, inp["w_gate"], inp["w_up"], inp["w_down"], exact, pre=True)
+        res["out_pre"] = combine(y, w, inv_perm, K, ys, exact, pre=True)
     res.update(ep)
     if ys is not None:
         res.update(ys=ys, gus=gus, hs=hs)
     return res
 
 
-def layer_backward(inp, fwd, dout, K: int, renorm: int = 1, exact: bool = False):
-    """Backward of ``layer_forward`` for upstream gradient dout [T,d]."""
+def layer_backward(inp, fwd, dout, K: int, renorm: int = 1, exact: bool = False,
+                   pre: bool = False):
+    """Backward of ``layer_forward`` for upstream gradient dout [T,d]; with
+    ``pre`` the result also holds dxp_pre and dx_pre (before their bf16
+    rounding)."""
     T, E = inp["logits"].shape
     dy, dw = combine_backward(dout, fwd["y"], fwd["topk_w"], fwd["inv_perm"], K, exact)
     dxp, dWg, dWu, dWd = grouped_ffn_backward(dy, fwd["xp"], fwd["gu"], fwd["h"], fwd["offsets"],
@@ -436,4 +458,9 @@ def layer_backward(inp, fwd, dout, K: int, renorm: int = 1, exact: bool = False)
     dlogits = route_topk_backward(inp["logits"], fwd["topk_idx"], fwd["topk_w"], dw, renorm)
     res.update(dy=dy, dtopk_w=dw, dxp=dxp, dw_gate=dWg, dw_up=dWu, dw_down=dWd, dx=dx,
                dlogits=dlogits)
+    if pre:
+        res["dxp_pre"] = grouped_ffn_backward(dy, fwd["xp"], fwd["gu"], fwd["h"], fwd["offsets"],
+                                              inp["w_gate"], inp["w_up"], inp["w_down"], exact,
+                                              pre=True)[0]
+        res["dx_pre"] = dispatch_backward(dxp, fwd["inv_perm"], K, T, dxs, exact, pre=True)
     return res

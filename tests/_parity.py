@@ -4,8 +4,17 @@ inputs to the device, and the tolerance checks the tests use.
 Tolerances (written here once, used by every GPU test):
 * integer / index outputs and the dispatch copy: bit-exact;
 * fp32 router weights: max |gpu - ref| <= 1e-5 * |ref| (relative, element-wise);
-* bf16 outputs of the expert GEMMs and of combine, and the backward's bf16 and
-  fp32 gradients: max |gpu - ref| <= 2e-2 * RMS(ref) per tensor;
+* bf16 results of a sum (y, out, dxp, dx) and fp32 weight gradients:
+  max |gpu - ref| <= 2e-2 * RMS(ref) per tensor, where for a bf16 tensor ref is
+  the oracle's value just before that tensor's own bf16 rounding (its inputs
+  rounded as stored). Against an independently rounded reference a single
+  1-ulp rounding flip at an element of |x| > 2.6 RMS already costs 2% of RMS,
+  so the final rounding is charged to the GPU side only;
+* element-wise bf16 intermediates (h, gu): |gpu - ref| <= 2^-8 |ref| +
+  1e-3 RMS(ref) against the pre-rounding ref: round-to-nearest moves a value
+  by at most half an ulp, 2^-8 of its magnitude, and the slack covers the
+  fp32-vs-fp64 accumulation difference before the rounding;
+* dy = bf16(w * dout) is rounded once from the exact product: bit-exact;
 * fp32 dtopk_w and dlogits fed identical inputs: max |err| <= 1e-3 * RMS(ref).
 """
 import numpy as np
@@ -54,6 +63,17 @@ def assert_rms_close(got, ref, tol=RMS_TOL, name=""):
     assert np.isfinite(got).all(), name
     assert err <= tol * rms + 1e-30, f"{name}: max|err|={err:.3e} > {tol}*RMS({rms:.3e})"
     return err / rms if rms else 0.0
+
+
+def assert_bf16_close(got, ref_pre, name=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref_pre, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    rms = np.sqrt(np.mean(ref ** 2)) if ref.size else 0.0
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), (f"{name}: {int(bad.sum())} elements outside half an ulp; worst "
+                           f"|err|={np.abs(got - ref)[bad].max():.3e}")
 
 
 def assert_rel_close(got, ref, tol=REL_W, name=""):

@@ -8,7 +8,8 @@ from grouped_gemm_moe_gb300 import layer as L
 from grouped_gemm_moe_gb300 import workloads as W
 from oracle import moe_oracle as O
 
-from _parity import assert_rel_close, assert_rms_close, dev, ensure_built, f64, i64
+from _parity import (assert_bf16_close, assert_rel_close, assert_rms_close, dev, ensure_built,
+                     f64, i64)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +40,7 @@ def test_layer_forward_backward(cfg):
     dx = layer.backward(dout)
     torch.cuda.synchronize()
     assert layer.device_status() == 0
-    ref = O.layer_forward(np_inp, cfg.K, cfg.R, cfg.renorm)
+    ref = O.layer_forward(np_inp, cfg.K, cfg.R, cfg.renorm, pre=True)
     assert np.array_equal(i64(layer.topk_idx), ref["topk_idx"])
     assert_rel_close(f64(layer.topk_w), ref["topk_w"], name="topk_w")
     assert np.array_equal(i64(layer.counts), ref["counts"])
@@ -54,11 +55,13 @@ def test_layer_forward_backward(cfg):
     for k in ("send_index", "a2a_index", "regroup_index"):
         assert np.array_equal(i64(getattr(layer, k)), ref[k]), k
     assert np.array_equal(f64(layer.xp), ref["xp"])
-    assert_rms_close(f64(layer.h), ref["h"], name="h")
-    assert_rms_close(f64(layer.y), ref["y"], name="y")
-    assert_rms_close(f64(out), ref["out"], name="out")
-    rb = O.layer_backward(np_inp, ref, np_inp["dout"], cfg.K, cfg.renorm)
-    assert_rms_close(f64(dx), rb["dx"], name="dx")
+    assert_bf16_close(f64(layer.h), ref["h_pre"], name="h")
+    assert_bf16_close(f64(layer.gu), ref["gu_pre"], name="gu")
+    assert_rms_close(f64(layer.y), ref["y_pre"], name="y")
+    assert_rms_close(f64(out), ref["out_pre"], name="out")
+    rb = O.layer_backward(np_inp, ref, np_inp["dout"], cfg.K, cfg.renorm, pre=True)
+    assert_rms_close(f64(dx), rb["dx_pre"], name="dx")
+    assert_rms_close(f64(layer.dxp), rb["dxp_pre"], name="dxp")
     assert_rms_close(f64(layer.dlogits), rb["dlogits"], name="dlogits")
     assert_rms_close(f64(layer.dw_gate), rb["dw_gate"], name="dw_gate")
     assert_rms_close(f64(layer.dw_up), rb["dw_up"], name="dw_up")
@@ -76,9 +79,10 @@ def test_exactly_one_device_to_host_copy_per_forward():
     layer.forward(logits, x)          # warm-up (library load, attribute setup)
     torch.cuda.synchronize()
     from torch.profiler import ProfilerActivity, profile
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+    with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
         layer.forward(logits, x)
         torch.cuda.synchronize()
     names = [e.name for e in prof.events()]
-    d2h = [n for n in names if "DtoH" in n or "Device -> Host" in n or "DeviceToHost" in n]
+    d2h = [n for n in names if "Memcpy" in n and ("DtoH" in n or "Device -> " in n)]
     assert len(d2h) == 1, names
+    assert sum(n.startswith("cudaMemcpy") for n in names) == 1, names

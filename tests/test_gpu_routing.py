@@ -40,7 +40,7 @@ def test_route_topk_workloads(name):
 
 
 @pytest.mark.parametrize("T,E,K,renorm", [(1, 8, 2, 1), (37, 100, 7, 1), (300, 1000, 32, 1),
-                                          (64, 33, 33, 0), (513, 64, 6, 0), (1000, 7, 1, 1),
+                                          (64, 33, 32, 0), (513, 64, 6, 0), (1000, 7, 1, 1),
                                           (129, 256, 8, 0), (77, 512, 16, 1)])
 def test_route_topk_shapes(T, E, K, renorm):
     g = torch.Generator().manual_seed(T * E + K)

@@ -250,3 +250,22 @@ def test_workload_shapes_and_skew():
     mean = cfg.T * cfg.K / cfg.E
     assert counts.max() > 10 * mean
     assert (counts == 0).sum() >= 5
+
+
+def test_pre_rounding_outputs_round_to_the_stored_values():
+    """``pre=True`` gives each stored bf16 output just before its rounding:
+    rounding it reproduces the stored value, and it is the exact function of
+    the (rounded) stored inputs."""
+    cfg = W.small_config(T=64, d=64, E=8, K=2, I=64, R=2, shared_I=64)
+    inp = _np_inputs(cfg)
+    f = O.layer_forward(inp, cfg.K, cfg.R, 1, pre=True)
+    for k in ("y", "gu", "h", "out"):
+        assert np.array_equal(O.round_bf16(f[k + "_pre"]), f[k]), k
+    b = O.layer_backward(inp, f, inp["dout"], cfg.K, 1, pre=True)
+    for k in ("dxp", "dx"):
+        assert np.array_equal(O.round_bf16(b[k + "_pre"]), b[k]), k
+    # y_pre = H_stored @ Wd exactly, segment by segment
+    off = f["offsets"]
+    for e in range(cfg.E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        assert np.allclose(f["y_pre"][lo:hi], f["h"][lo:hi] @ inp["w_down"][e], rtol=1e-13, atol=0)

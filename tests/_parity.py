@@ -4,12 +4,15 @@ inputs to the device, and the tolerance checks the tests use.
 Tolerances (written here once, used by every GPU test):
 * integer / index outputs and the dispatch copy: bit-exact;
 * fp32 router weights: max |gpu - ref| <= 1e-5 * |ref| (relative, element-wise);
-* bf16 results of a sum (y, out, dxp, dx) and fp32 weight gradients:
-  max |gpu - ref| <= 2e-2 * RMS(ref) per tensor, where for a bf16 tensor ref is
-  the oracle's value just before that tensor's own bf16 rounding (its inputs
-  rounded as stored). Against an independently rounded reference a single
-  1-ulp rounding flip at an element of |x| > 2.6 RMS already costs 2% of RMS,
-  so the final rounding is charged to the GPU side only;
+* fp32 weight gradients: max |gpu - ref| <= 2e-2 * RMS(ref) per tensor;
+* bf16 results of a sum (y, out, dxp, dx): the same 2e-2 * RMS(ref) bound on the
+  error beyond the output's own rounding, max(|gpu - ref| - 2^-8 |ref|, 0),
+  where ref is the oracle's value just before that tensor's bf16 rounding (its
+  inputs rounded as stored). bf16 keeps 8 significant bits, so rounding alone
+  moves an element by up to 2^-8 of its magnitude: 2% of RMS already at 5.1 RMS,
+  which a Gaussian tensor of a few million elements exceeds. Against an
+  independently rounded reference a single 1-ulp flip at |x| > 2.6 RMS costs
+  the same;
 * element-wise bf16 intermediates (h, gu): |gpu - ref| <= 2^-8 |ref| +
   1e-3 RMS(ref) against the pre-rounding ref: round-to-nearest moves a value
   by at most half an ulp, 2^-8 of its magnitude, and the slack covers the
@@ -63,6 +66,21 @@ def assert_rms_close(got, ref, tol=RMS_TOL, name=""):
     assert np.isfinite(got).all(), name
     assert err <= tol * rms + 1e-30, f"{name}: max|err|={err:.3e} > {tol}*RMS({rms:.3e})"
     return err / rms if rms else 0.0
+
+
+def assert_out_close(got, ref_pre, tol=RMS_TOL, name=""):
+    """bf16 result of a sum against the oracle's pre-rounding value."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref_pre, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.isfinite(got).all(), name
+    if not ref.size:
+        return 0.0
+    rms = np.sqrt(np.mean(ref ** 2))
+    excess = np.maximum(np.abs(got - ref) - 2.0 ** -8 * np.abs(ref), 0.0).max()
+    assert excess <= tol * rms + 1e-30, (f"{name}: error beyond the bf16 rounding "
+                                         f"{excess:.3e} > {tol}*RMS({rms:.3e})")
+    return excess / rms if rms else 0.0
 
 
 def assert_bf16_close(got, ref_pre, name=""):

@@ -8,7 +8,7 @@ from grouped_gemm_moe_gb300 import binding as B
 from grouped_gemm_moe_gb300 import workloads as W
 from oracle import moe_oracle as O
 
-from _parity import assert_rms_close, ensure_built, f64, i64, to_dev
+from _parity import assert_out_close, assert_rms_close, ensure_built, f64, i64, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,7 @@ def test_combine(T, d, E, K, shared):
                         to_dev(inv, torch.int32), None if ys is None else to_dev(ys, torch.bfloat16))
     ref = O.combine(y.double().numpy(), w.astype(np.float64), inv, K,
                     None if ys is None else ys.double().numpy(), pre=True)
-    assert_rms_close(f64(out), ref, name="out")
+    assert_out_close(f64(out), ref, name="out")
 
 
 def test_identity_round_trip_is_exact():
@@ -94,4 +94,4 @@ def test_dispatch_backward(T, d, E, K, shared):
                                  None if dxs is None else to_dev(dxs, torch.bfloat16))
     ref = O.dispatch_backward(dxp.double().numpy(), inv, K, T,
                               None if dxs is None else dxs.double().numpy(), pre=True)
-    assert_rms_close(f64(dx), ref, name="dx")
+    assert_out_close(f64(dx), ref, name="dx")

@@ -8,8 +8,8 @@ from grouped_gemm_moe_gb300 import layer as L
 from grouped_gemm_moe_gb300 import workloads as W
 from oracle import moe_oracle as O
 
-from _parity import (assert_bf16_close, assert_rel_close, assert_rms_close, dev, ensure_built,
-                     f64, i64)
+from _parity import (assert_bf16_close, assert_out_close, assert_rel_close, assert_rms_close, dev,
+                     ensure_built, f64, i64)
 
 pytestmark = pytest.mark.gpu
 
@@ -57,11 +57,11 @@ def test_layer_forward_backward(cfg):
     assert np.array_equal(f64(layer.xp), ref["xp"])
     assert_bf16_close(f64(layer.h), ref["h_pre"], name="h")
     assert_bf16_close(f64(layer.gu), ref["gu_pre"], name="gu")
-    assert_rms_close(f64(layer.y), ref["y_pre"], name="y")
-    assert_rms_close(f64(out), ref["out_pre"], name="out")
+    assert_out_close(f64(layer.y), ref["y_pre"], name="y")
+    assert_out_close(f64(out), ref["out_pre"], name="out")
     rb = O.layer_backward(np_inp, ref, np_inp["dout"], cfg.K, cfg.renorm, pre=True)
-    assert_rms_close(f64(dx), rb["dx_pre"], name="dx")
-    assert_rms_close(f64(layer.dxp), rb["dxp_pre"], name="dxp")
+    assert_out_close(f64(dx), rb["dx_pre"], name="dx")
+    assert_out_close(f64(layer.dxp), rb["dxp_pre"], name="dxp")
     assert_rms_close(f64(layer.dlogits), rb["dlogits"], name="dlogits")
     assert_rms_close(f64(layer.dw_gate), rb["dw_gate"], name="dw_gate")
     assert_rms_close(f64(layer.dw_up), rb["dw_up"], name="dw_up")
@@ -79,10 +79,12 @@ def test_exactly_one_device_to_host_copy_per_forward():
     layer.forward(logits, x)          # warm-up (library load, attribute setup)
     torch.cuda.synchronize()
     from torch.profiler import ProfilerActivity, profile
+    from torch.profiler import record_function
     with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
-        layer.forward(logits, x)
-        torch.cuda.synchronize()
+        with record_function("moe_layer_forward"):
+            layer.forward(logits, x)
+            torch.cuda.synchronize()
     names = [e.name for e in prof.events()]
     d2h = [n for n in names if "Memcpy" in n and ("DtoH" in n or "Device -> " in n)]
-    assert len(d2h) == 1, names
+    assert len(d2h) == 1, prof.key_averages().table(row_limit=40)
     assert sum(n.startswith("cudaMemcpy") for n in names) == 1, names

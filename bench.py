@@ -52,7 +52,48 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
+    ap.add_argument("--profile-case", choices=["gemm", "layer"], default=None,
+                    help="run a small fixed case twice for an ncu capture and exit")
     return ap.parse_args()
+
+
+def profile_case(which: str):
+    """Small cases for ncu captures (inputs above the 129 MB L2, a few GB on the device).
+
+    gemm:  the grouped-GEMM entry points, forward and backward, on E=64 experts x 512 rows
+           (d=2048, I=768; the qwen3 workload's rows per expert), run twice.
+    layer: one qwen3-shaped layer at T=2048 tokens (forward + backward), run twice.
+    """
+    import torch
+    from grouped_gemm_moe_gb300 import binding as B
+    from grouped_gemm_moe_gb300 import build as build_mod
+    from grouped_gemm_moe_gb300 import layer as L
+    from grouped_gemm_moe_gb300 import workloads as W
+    if not os.path.exists(B.LIB_PATH):
+        build_mod.build()
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev).manual_seed(0)
+    if which == "gemm":
+        E, d, I, rows = 64, 2048, 768, 512
+        M = E * rows
+        bf = torch.bfloat16
+        rnd = lambda *s, sc=1.0: (torch.randn(*s, device=dev, generator=g) * sc).to(bf)  # noqa: E731
+        off = torch.arange(0, M + 1, rows, dtype=torch.int32, device=dev)
+        xp, dy, gu, h = rnd(M, d), rnd(M, d, sc=0.1), rnd(M, 2 * I), rnd(M, I, sc=0.5)
+        wg, wu, wd = rnd(E, d, I, sc=0.02), rnd(E, d, I, sc=0.02), rnd(E, I, d, sc=0.02)
+        for _ in range(2):
+            B.moe_grouped_ffn_backward(dy, xp, gu, h, off, wg, wu, wd)
+            B.moe_grouped_ffn(xp, off, wg, wu, wd)
+    else:
+        cfg = W.MoEConfig("qwen3-2k", T=2048, d=2048, E=128, K=8, I=768, R=8)
+        inp = W.make_inputs(cfg)
+        layer = L.layer_from_config(cfg, inp, dev)
+        logits, x, dout = (inp[k].to(dev) for k in ("logits", "x", "dout"))
+        for _ in range(2):
+            layer.forward(logits, x)
+            layer.backward(dout)
+    torch.cuda.synchronize()
+    print(f"profile case {which} ok, peak {torch.cuda.max_memory_allocated() / 2**30:.2f} GiB")
 
 
 def dist_env():
@@ -251,6 +292,9 @@ def run_reference(args, cfg, world, rank):
 # ------------------------------------------------------------------ GPU arm
 def main():
     args = parse()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
     world, rank, local = dist_env()
     from grouped_gemm_moe_gb300 import workloads as W
     cfg = W.CONFIGS[args.config or W.BENCH_CONFIG]

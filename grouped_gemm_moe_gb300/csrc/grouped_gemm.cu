@@ -172,6 +172,46 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 32 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bulk tensor store shared -> global (2-D tile), tracked by this thread's bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory accesses with later async-proxy ones.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -269,10 +309,20 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int* s
 }
 
 // ----------------------------------------------------------------- kernel
+// Epilogue shared memory per kind: weight gradients stage one [32 rows x 32 fp32]
+// block per epilogue warp for a bulk tensor store; gemm_dh prefetches, per
+// epilogue warp, the saved G and U of 32 rows x 128 columns (four [32 x 64]
+// bf16 boxes) for the tile it is about to drain.
+template <int KIND>
+__host__ __device__ constexpr uint32_t epi_bytes() {
+  return (KIND == WGRAD_GU || KIND == WGRAD_D) ? 4u * 4096u : (KIND == BWD_DH ? 4u * 16384u : 0u);
+}
+
 template <int KIND, int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const Params p) {
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
+                    const __grid_constant__ CUtensorMap tmC1, const Params p) {
   constexpr bool kWgrad = (KIND == WGRAD_GU || KIND == WGRAD_D);
   constexpr bool A_MN = kWgrad;
   constexpr bool B_MN = (KIND == FWD_GATEUP || KIND == FWD_DOWN || kWgrad);
@@ -286,9 +336,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint8_t* epi = smem + STAGES * STAGE_BYTES;            // epilogue region (epi_bytes)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + epi_bytes<KIND>());
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, aux[4]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_mt = s_off + (p.E + 1);
@@ -302,16 +353,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
+  auto aux_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + 5 + w); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 4); }
     mbar_init(drain_bar, 1);
+    for (int w = 0; w < 4; ++w) mbar_init(aux_bar(w), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB0)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB1)) : "memory");
+    if constexpr (epi_bytes<KIND>() != 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC1)) : "memory");
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -472,98 +529,151 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quarter of this warp
+    const int ew = warp - 2;                 // epilogue warp index (its shared-memory slot)
     const int r = q * 32 + lane;             // accumulator row of this thread
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t aux_phase = 0;
+    bool aux_pending = false;                // a G/U prefetch was requested and not yet waited for
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile<KIND, BN>(t, p, s_off, s_mt);
       if constexpr (kWgrad) {
-        if (tl.nkb == 0) {     // expert without rows: its weight gradient is zero
-          float z[16];
+        // fp32 weight gradient of rows [m0 + 32q, +32) x [n0, n0 + BN): staged per 32 columns
+        // in a 128-byte-swizzled [32 x 32] block and written by a bulk tensor store.
+        uint8_t* stg = epi + ew * 4096;
+        const uint32_t stg_addr = smem_u32(stg);
+        const bool empty = (tl.nkb == 0);    // expert without rows: its gradient is zero
+        if (!empty) {
+          if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+          tc_fence_after();
+        }
+        const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
+        const int mrow = tl.m0 + q * 32;
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          if (!empty) {
+            tmem_ld32(tacc + c, v);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) z[i] = 0.f;
-          const int m = tl.m0 + r;
-          for (int c = 0; c < BN; c += 16) {
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+          if (lane == 0) bulk_wait_read_all();     // the previous store has read the block
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4* dst = reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4));
+            *dst = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
             const int n = tl.n0 + c;
             if constexpr (KIND == WGRAD_GU) {
-              float* dst = (n < p.I) ? p.outf0 + (static_cast<size_t>(tl.e) * p.d + m) * p.I + n
-                                     : p.outf1 + (static_cast<size_t>(tl.e) * p.d + m) * p.I + (n - p.I);
-              store16_f32(dst, z);
+              if (n < p.I) tma_store_2d(&tmC0, stg_addr, n, tl.e * p.d + mrow);
+              else tma_store_2d(&tmC1, stg_addr, n - p.I, tl.e * p.d + mrow);
             } else {
-              store16_f32(p.outf0 + (static_cast<size_t>(tl.e) * p.I + m) * p.d + n, z);
+              tma_store_2d(&tmC0, stg_addr, n, tl.e * p.I + mrow);
             }
-          }
-          continue;
-        }
-      }
-      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
-      if constexpr (KIND == FWD_GATEUP) {
-        constexpr int HALF = BN / 2;
-        const bool valid = r < tl.rows;
-        const size_t grow = static_cast<size_t>(tl.row0 + r);
-        for (int c = 0; c < HALF; c += 16) {
-          float g[16], u[16], h[16];
-          tmem_ld16(tacc + c, g);
-          tmem_ld16(tacc + HALF + c, u);
-          tmem_wait_ld();
-          if (valid) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) h[i] = silu_f(g[i]) * u[i];
-            store16_bf16(p.out + grow * p.I + tl.n0 + c, h);
-            if (p.out2) {
-              store16_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c, g);
-              store16_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c, u);
-            }
+            bulk_commit();
           }
         }
-      } else if constexpr (KIND == FWD_DOWN || KIND == BWD_DX) {
-        const bool valid = r < tl.rows;
-        const size_t grow = static_cast<size_t>(tl.row0 + r);
-        for (int c = 0; c < BN; c += 16) {
-          float v[16];
-          tmem_ld16(tacc + c, v);
-          tmem_wait_ld();
-          if (valid) store16_bf16(p.out + grow * p.ld_out + tl.n0 + c, v);
-        }
+        if (empty) continue;
       } else if constexpr (KIND == BWD_DH) {
+        // Saved G and U for this warp's 32 rows arrive by TMA in 128-column passes;
+        // the first pass is requested before the accumulator is ready.
+        uint8_t* aux = epi + ew * 16384;     // boxes: G[c0, +64), G[c0+64, +64), U.., U..
+        const uint32_t aux_addr = smem_u32(aux);
+        const uint32_t ab = aux_bar(ew);
+        const int grow0 = tl.row0 + q * 32;
+        auto request = [&](int c0) {
+          if (lane == 0) {
+            mbar_expect_tx(ab, 16384);
+            tma_load_2d(aux_addr, &tmC0, ab, tl.n0 + c0, grow0);
+            tma_load_2d(aux_addr + 4096, &tmC0, ab, tl.n0 + c0 + 64, grow0);
+            tma_load_2d(aux_addr + 8192, &tmC0, ab, p.I + tl.n0 + c0, grow0);
+            tma_load_2d(aux_addr + 12288, &tmC0, ab, p.I + tl.n0 + c0 + 64, grow0);
+          }
+          aux_pending = true;
+        };
+        request(0);
+        if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
         const bool valid = r < tl.rows;
         const size_t grow = static_cast<size_t>(tl.row0 + r);
-        for (int c = 0; c < BN; c += 16) {
-          float dh[16];
-          tmem_ld16(tacc + c, dh);
-          tmem_wait_ld();
-          if (valid) {
-            float g[16], u[16], dg[16], du[16];
-            const __nv_bfloat16* gurow = p.aux + grow * (2 * p.I);
-            load16_bf16(gurow + tl.n0 + c, g);
-            load16_bf16(gurow + p.I + tl.n0 + c, u);
+        bool ok = true;
+        for (int c0 = 0; c0 < BN; c0 += 128) {
+          if (c0) request(c0);
+          if (!mbar_wait(ab, aux_phase, abort_flag, p.status)) { ok = false; break; }
+          aux_phase ^= 1u;
+          aux_pending = false;
+          for (int c = 0; c < 128; c += 16) {
+            float dh[16];
+            tmem_ld16(tacc + c0 + c, dh);
+            tmem_wait_ld();
+            // this row's 16 columns: two 16-byte chunks of a 128-byte-swizzled box row
+            const int box = c >> 6;
+            const int j0 = (c & 63) >> 3;
+            float g[16], u[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float s = 1.f / (1.f + expf(-g[i]));
-              dg[i] = dh[i] * u[i] * s * (1.f + g[i] * (1.f - s));
-              du[i] = dh[i] * g[i] * s;
+            for (int hh = 0; hh < 2; ++hh) {
+              const int off = lane * 128 + (((j0 + hh) ^ (lane & 7)) << 4);
+              float f[8];
+              unpack8(*reinterpret_cast<const uint4*>(aux + box * 4096 + off), f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) g[8 * hh + i] = f[i];
+              unpack8(*reinterpret_cast<const uint4*>(aux + 8192 + box * 4096 + off), f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) u[8 * hh + i] = f[i];
             }
-            __nv_bfloat16* orow = p.out + grow * (2 * p.I);
-            store16_bf16(orow + tl.n0 + c, dg);
-            store16_bf16(orow + p.I + tl.n0 + c, du);
+            if (valid) {
+              float dg[16], du[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float s = 1.f / (1.f + expf(-g[i]));
+                dg[i] = dh[i] * u[i] * s * (1.f + g[i] * (1.f - s));
+                du[i] = dh[i] * g[i] * s;
+              }
+              __nv_bfloat16* orow = p.out + grow * (2 * p.I);
+              store16_bf16(orow + tl.n0 + c0 + c, dg);
+              store16_bf16(orow + p.I + tl.n0 + c0 + c, du);
+            }
           }
+          fence_proxy_async();    // reads of this pass's boxes before the next TMA write
+          __syncwarp();
         }
-      } else {  // weight gradients, fp32 out
-        const int m = tl.m0 + r;
-        for (int c = 0; c < BN; c += 16) {
-          float v[16];
-          tmem_ld16(tacc + c, v);
-          tmem_wait_ld();
-          const int n = tl.n0 + c;
-          if constexpr (KIND == WGRAD_GU) {
-            float* dst = (n < p.I) ? p.outf0 + (static_cast<size_t>(tl.e) * p.d + m) * p.I + n
-                                   : p.outf1 + (static_cast<size_t>(tl.e) * p.d + m) * p.I + (n - p.I);
-            store16_f32(dst, v);
-          } else {
-            store16_f32(p.outf0 + (static_cast<size_t>(tl.e) * p.I + m) * p.d + n, v);
+        if (!ok) break;
+      } else {
+        if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
+        const bool valid = r < tl.rows;
+        const size_t grow = static_cast<size_t>(tl.row0 + r);
+        if constexpr (KIND == FWD_GATEUP) {
+          constexpr int HALF = BN / 2;
+          for (int c = 0; c < HALF; c += 16) {
+            float g[16], u[16], h[16];
+            tmem_ld16(tacc + c, g);
+            tmem_ld16(tacc + HALF + c, u);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) h[i] = silu_f(g[i]) * u[i];
+              store16_bf16(p.out + grow * p.I + tl.n0 + c, h);
+              if (p.out2) {
+                store16_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c, g);
+                store16_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c, u);
+              }
+            }
+          }
+        } else {  // FWD_DOWN, BWD_DX: bf16 store
+          for (int c = 0; c < BN; c += 16) {
+            float v[16];
+            tmem_ld16(tacc + c, v);
+            tmem_wait_ld();
+            if (valid) store16_bf16(p.out + grow * p.ld_out + tl.n0 + c, v);
           }
         }
       }
@@ -572,6 +682,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       if (lane == 0) mbar_arrive(tempty_bar(acc));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+    }
+    if constexpr (kWgrad) {
+      if (lane == 0) bulk_wait_all();        // stores done before the CTA's shared memory goes
+      __syncwarp();
+    }
+    if constexpr (KIND == BWD_DH) {
+      // a prefetch still in flight because the loop stopped early: let it land (bounded)
+      if (lane == 0 && aux_pending) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(aux_bar(ew), aux_phase) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+      __syncwarp();
     }
   }
 
@@ -599,29 +722,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer, inner] array, 128-byte swizzle.
+// 2-D tensor map over a row-major [outer, inner] array of bf16 (or fp32), 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer) {
+              uint32_t box_outer, bool fp32 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * (fp32 ? 4 : 2)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int KIND, int BN, int STAGES>
 size_t smem_bytes(int E) {
-  return 1024 + STAGES * (BM * BK * 2 + BN * BK * 2) + 8 * (2 * STAGES + 5) + 16 +
-         sizeof(int) * 2 * (E + 1) + 16;
+  return 1024 + STAGES * (BM * BK * 2 + BN * BK * 2) + epi_bytes<KIND>() + 8 * (2 * STAGES + 9) +
+         16 + sizeof(int) * 2 * (E + 1) + 16;
 }
 
 template <int KIND, int BN, int STAGES>
-int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
-           long long tiles_upper, cudaStream_t st) {
+int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+           const CUtensorMap& c0, const CUtensorMap& c1, const Params& p, long long tiles_upper,
+           cudaStream_t st) {
   auto kern = grouped_gemm_kernel<KIND, BN, STAGES>;
   const size_t sm = smem_bytes<KIND, BN, STAGES>(p.E);
   static thread_local int configured = -1;
@@ -639,19 +764,28 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, c
   static const char* kNames[] = {"gemm_gate_up", "gemm_down", "gemm_dh", "gemm_dx",
                                  "gemm_wgrad_gate_up", "gemm_wgrad_down"};
   ProfScope prof(kNames[KIND], st);
-  kern<<<static_cast<int>(grid), kThreads, sm, st>>>(a, b0, b1, p);
+  kern<<<static_cast<int>(grid), kThreads, sm, st>>>(a, b0, b1, c0, c1, p);
   return check_launch();
 }
 
-constexpr int kStages256 = 4;
-constexpr int kStages128 = 6;
+// Pipeline depth: as many operand stages as fit next to the kind's epilogue buffers
+// (227 KB of shared memory per CTA, expert tables for up to 1024 experts included).
+template <int KIND, int BN>
+constexpr int stages_for() {
+  return (KIND == BWD_DH) ? (BN == 256 ? 3 : 4) : (BN == 256 ? 4 : 6);
+}
 
 template <int KIND>
 int launch_bn(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-              const Params& p, long long tiles_upper, cudaStream_t st) {
-  if (bn == 256) return launch<KIND, 256, kStages256>(a, b0, b1, p, tiles_upper, st);
-  return launch<KIND, 128, kStages128>(a, b0, b1, p, tiles_upper, st);
+              const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
+              long long tiles_upper, cudaStream_t st) {
+  if (bn == 256)
+    return launch<KIND, 256, stages_for<KIND, 256>()>(a, b0, b1, c0, c1, p, tiles_upper, st);
+  return launch<KIND, 128, stages_for<KIND, 128>()>(a, b0, b1, c0, c1, p, tiles_upper, st);
 }
+
+static_assert(1024 + 3 * (16384 + 32768) + 65536 + 8 * 15 + 32 + 8 * 1025 <= 232448, "dh smem");
+static_assert(1024 + 4 * (16384 + 32768) + 16384 + 8 * 17 + 32 + 8 * 1025 <= 232448, "wgrad smem");
 
 }  // namespace gemm
 
@@ -705,7 +839,7 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
   p.out = reinterpret_cast<__nv_bfloat16*>(h);
   p.out2 = reinterpret_cast<__nv_bfloat16*>(gu);
   p.ld_out = I;
-  int rc = launch_bn<FWD_GATEUP>(256, ta, tb0, tb1, p, mt_upper * p.n_tiles, st);
+  int rc = launch_bn<FWD_GATEUP>(256, ta, tb0, tb1, ta, ta, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // down projection
   const int bn = (d % 256 == 0) ? 256 : 128;
@@ -716,7 +850,7 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
   p.out = reinterpret_cast<__nv_bfloat16*>(y);
   p.out2 = nullptr;
   p.ld_out = d;
-  return launch_bn<FWD_DOWN>(bn, ta, tb0, tb0, p, mt_upper * p.n_tiles, st);
+  return launch_bn<FWD_DOWN>(bn, ta, tb0, tb0, ta, ta, p, mt_upper * p.n_tiles, st);
 }
 
 extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
@@ -759,18 +893,19 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   p.I = I;
   p.status = static_cast<int*>(ws);
   const long long mt_upper = (M + BM - 1) / BM + E;
-  CUtensorMap ta, tb0, tb1;
+  CUtensorMap ta, tb0, tb1, tc0, tc1;
   // dH = dY Wd^T with the SwiGLU backward epilogue -> [dG | dU]
   const int bn_h = (I % 256 == 0) ? 256 : 128;
   if (!make_map(&ta, dy, d, M, 64, BM) ||
-      !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h))
+      !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h) ||
+      !make_map(&tc0, gu, 2 * static_cast<uint64_t>(I), M, 64, 32))
     return MOE_ERR_CUDA;
   p.n_tiles = I / bn_h;
   p.k_blocks = d / BK;
   p.out = dgu;
   p.aux = reinterpret_cast<const __nv_bfloat16*>(gu);
   p.ld_out = 2 * I;
-  int rc = launch_bn<BWD_DH>(bn_h, ta, tb0, tb0, p, mt_upper * p.n_tiles, st);
+  int rc = launch_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc0, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // dX = dG Wg^T + dU Wu^T
   const int bn_x = (d % 256 == 0) ? 256 : 128;
@@ -783,24 +918,30 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   p.out = reinterpret_cast<__nv_bfloat16*>(dxp);
   p.aux = nullptr;
   p.ld_out = d;
-  rc = launch_bn<BWD_DX>(bn_x, ta, tb0, tb1, p, mt_upper * p.n_tiles, st);
+  rc = launch_bn<BWD_DX>(bn_x, ta, tb0, tb1, ta, ta, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // [dWg | dWu] = X^T [dG | dU]
-  if (!make_map(&ta, xp, d, M, 64, 64) || !make_map(&tb0, dgu, 2 * static_cast<uint64_t>(I), M, 64, 64))
+  if (!make_map(&ta, xp, d, M, 64, 64) || !make_map(&tb0, dgu, 2 * static_cast<uint64_t>(I), M, 64, 64) ||
+      !make_map(&tc0, dw_gate, I, static_cast<uint64_t>(E) * d, 32, 32, true) ||
+      !make_map(&tc1, dw_up, I, static_cast<uint64_t>(E) * d, 32, 32, true))
     return MOE_ERR_CUDA;
   p.m_tiles = d / BM;
   p.n_tiles = 2 * I / 256;
   p.outf0 = dw_gate;
   p.outf1 = dw_up;
   p.out = nullptr;
-  rc = launch_bn<WGRAD_GU>(256, ta, tb0, tb0, p, static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
+  rc = launch_bn<WGRAD_GU>(256, ta, tb0, tb0, tc0, tc1, p,
+                           static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
   if (rc) return rc;
   // dWd = H^T dY
   const int bn_d = (d % 256 == 0) ? 256 : 128;
-  if (!make_map(&ta, h, I, M, 64, 64) || !make_map(&tb0, dy, d, M, 64, 64)) return MOE_ERR_CUDA;
+  if (!make_map(&ta, h, I, M, 64, 64) || !make_map(&tb0, dy, d, M, 64, 64) ||
+      !make_map(&tc0, dw_down, d, static_cast<uint64_t>(E) * I, 32, 32, true))
+    return MOE_ERR_CUDA;
   p.m_tiles = I / BM;
   p.n_tiles = d / bn_d;
   p.outf0 = dw_down;
   p.outf1 = nullptr;
-  return launch_bn<WGRAD_D>(bn_d, ta, tb0, tb0, p, static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
+  return launch_bn<WGRAD_D>(bn_d, ta, tb0, tb0, tc0, tc0, p,
+                            static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
 }

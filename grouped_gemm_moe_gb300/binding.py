@@ -45,6 +45,7 @@ SIGNATURES = {
     "moe_route_topk": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_route_topk_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_build_permutation": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_build_permutation_static": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_ep_layout": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_ffn": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -181,6 +182,24 @@ def moe_build_permutation(topk_idx: torch.Tensor, E: int, ws: Optional[torch.Ten
     _check("moe_build_permutation", load().moe_build_permutation(
         _ptr(topk_idx), T, E, K, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(ws),
         ws.numel(), _stream(dev)))
+    return counts, offsets, perm, inv
+
+
+def moe_build_permutation_static(topk_idx: torch.Tensor, E: int, out=None):
+    """moe_build_permutation without a workspace: the library's fixed device
+    scratch holds the chunk histogram (for callers that cannot allocate)."""
+    _need(topk_idx, torch.int32, 2, "topk_idx")
+    T, K = topk_idx.shape
+    dev = topk_idx.device
+    if out is None:
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(T * K, dtype=torch.int32, device=dev)
+        inv = torch.empty(T * K, dtype=torch.int32, device=dev)
+    else:
+        counts, offsets, perm, inv = out
+    _check("moe_build_permutation_static", load().moe_build_permutation_static(
+        _ptr(topk_idx), T, E, K, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _stream(dev)))
     return counts, offsets, perm, inv
 
 

@@ -325,3 +325,87 @@ extern "C" int moe_ep_layout(const int32_t* topk_idx, int T, int E, int K, int R
   }
   return check_launch();
 }
+
+// ---------------------------------------------------------------------------
+// moe_build_permutation_static: the same two kernels with the chunk histogram
+// in a fixed device array instead of a caller workspace, for callers that
+// cannot allocate. Host code must not pass g_static_hist itself to a kernel
+// (in host code the name is a host-side stand-in, not a device address); it
+// passes the address cudaGetSymbolAddress returns for the current device.
+namespace moe {
+
+static __device__ __align__(256) int32_t g_static_hist[MOE_STATIC_HIST_INTS];
+
+namespace {
+
+constexpr int kMaxStaticDevices = 64;
+int32_t* g_static_hist_dev[kMaxStaticDevices] = {nullptr};
+bool g_static_smem_set[kMaxStaticDevices] = {false};
+
+// Device address of g_static_hist on the current device (looked up once per device).
+int static_hist_on_current_device(int32_t** out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
+  if (dev < 0 || dev >= kMaxStaticDevices) return MOE_ERR_UNSUPPORTED;
+  if (!g_static_hist_dev[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_hist);
+    if (e != cudaSuccess || !ptr) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
+    g_static_hist_dev[dev] = static_cast<int32_t*>(ptr);
+  }
+  *out = g_static_hist_dev[dev];
+  *dev_out = dev;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_build_permutation_static(const int32_t* topk_idx, int T, int E, int K,
+                                            int32_t* counts, int32_t* offsets, int32_t* perm,
+                                            int32_t* inv_perm, void* stream) {
+  using namespace moe;
+  if (T < 0 || E < 1 || E > 1024 || K < 1 || K > E) return MOE_ERR_INVALID_ARG;
+  const long long TK = static_cast<long long>(T) * K;
+  if (TK >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (TK == 0) {
+    cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st);
+    cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), st);
+    return check_launch();
+  }
+  if (!topk_idx || !perm || !inv_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(topk_idx) || !aligned16(counts) || !aligned16(offsets) || !aligned16(perm) ||
+      !aligned16(inv_perm))
+    return MOE_ERR_MISALIGNED;
+  ChunkGeom g;
+  g.seg_len = TK;
+  g.cps = static_cast<int>((TK + kChunk - 1) / kChunk);
+  const int NC = g.cps;
+  if (static_cast<long long>(NC) * E > MOE_STATIC_HIST_INTS) return MOE_ERR_WORKSPACE;
+  int32_t* hist = nullptr;
+  int dev = 0;
+  int rc = static_hist_on_current_device(&hist, &dev);
+  if (rc) return rc;
+  if (!g_static_smem_set[dev]) {
+    cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    cudaFuncSetAttribute(scatter_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         160 * 1024);
+    g_static_smem_set[dev] = true;
+  }
+  const size_t sh_hist = static_cast<size_t>(kWarps) * E * sizeof(int);
+  const size_t sh_scatter = sh_hist + static_cast<size_t>(6 * E + 3) * sizeof(int);
+  PermOut po{counts, offsets, perm, inv_perm};
+  EpOut eo{};
+  {
+    ProfScope prof("perm_hist", st);
+    hist_kernel<<<NC, kThreads, sh_hist, st>>>(topk_idx, E, g, hist);
+  }
+  rc = check_launch();
+  if (rc) return rc;
+  ProfScope prof("perm_scatter", st);
+  scatter_kernel<false><<<NC, kThreads, sh_scatter, st>>>(topk_idx, E, g, NC, hist, po, eo);
+  return check_launch();
+}

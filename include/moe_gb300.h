@@ -118,6 +118,33 @@ int moe_build_permutation(const int32_t* topk_idx, int T, int E, int K,
                           int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of moe_build_permutation. The pages have no
+ * counterpart: it exists for callers that cannot allocate device memory on
+ * the call path. Examples are a host runtime that owns every device buffer
+ * and hands the library only its inputs and outputs, and hot loops that must
+ * not call cudaMalloc (it synchronises the device) yet have no workspace of
+ * their own to pass.
+ *   Same arguments, outputs and results as moe_build_permutation, minus the
+ *   workspace. The per-chunk expert histogram lives instead in one file-scope
+ *   device array of MOE_STATIC_HIST_INTS int32 (1 MiB) that every GPU loading
+ *   the library holds until the process exits.
+ *   Limit: ceil(T*K / 4096) * E <= MOE_STATIC_HIST_INTS (for example E = 128
+ *   up to T*K = 8,388,608); larger problems return MOE_ERR_WORKSPACE before
+ *   anything is enqueued. Other limits as moe_build_permutation.
+ *   The first call on a device looks up that device's address of the array
+ *   (cudaGetSymbolAddress, with the device current) and caches it; make that
+ *   first call before any stream capture on that device.
+ *   All calls share the array and it keeps the last call's contents; every
+ *   entry a call reads is written earlier in the same call, so nothing needs
+ *   clearing. Calls that overlap on the GPU (other streams, other host
+ *   threads) race on the array: serialise them.
+ *   The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *   routine. */
+#define MOE_STATIC_HIST_INTS (1 << 18)
+int moe_build_permutation_static(const int32_t* topk_idx, int T, int E, int K,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm,
+                                 int32_t* inv_perm, void* stream);
+
 /* A4. Layout of one dispatch all-to-all over R simulated expert-parallel ranks
  * ([TAS] "Mapping experts to EP ranks": rank i owns experts
  * [i*E/R, (i+1)*E/R); "Dispatch, expert computation and combine": per-rank

@@ -21,7 +21,6 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
 
 int grid_for(long long work, int per_block) {
   long long b = (work + per_block - 1) / per_block;
@@ -31,28 +30,33 @@ int grid_for(long long work, int per_block) {
   return static_cast<int>(b);
 }
 
-// xp[p] = x[perm[p] / K]
+// xp[p] = x[perm[p] / K]. One warp per packed row (rows strided over the
+// grid's warps); a lane issues all of its 16-byte loads of a 4 KB slice of the
+// row before its stores, so each warp keeps a whole row in flight.
+constexpr int kRowVecs = 8;   // 16-byte vectors per lane per pass (4 KB per warp)
+
 __global__ void __launch_bounds__(kThreads)
 dispatch_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int K, int nv,
-                long long total, uint4* __restrict__ xp) {
-  const long long stride = static_cast<long long>(gridDim.x) * kThreads;
-  for (long long i0 = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i0 < total;
-       i0 += stride * kUnroll) {
-    uint4 v[kUnroll];
+                long long rows, uint4* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (kThreads / 32);
+  for (long long p = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+       p < rows; p += nwarps) {
+    const long long t = __ldg(perm + p) / K;
+    const uint4* src = x + t * nv;
+    uint4* dst = xp + p * nv;
+    for (int c0 = 0; c0 < nv; c0 += 32 * kRowVecs) {
+      uint4 v[kRowVecs];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const long long i = i0 + u * stride;
-      if (i < total) {
-        const long long p = i / nv;
-        const int c = static_cast<int>(i - p * nv);
-        const long long t = __ldg(perm + p) / K;
-        v[u] = ldg_nc_v4(x + t * nv + c);
+      for (int u = 0; u < kRowVecs; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < nv) v[u] = ldg_nc_v4(src + c);
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const long long i = i0 + u * stride;
-      if (i < total) stg_v4(xp + i, v[u]);
+      for (int u = 0; u < kRowVecs; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < nv) stg_v4(dst + c, v[u]);
+      }
     }
   }
 }
@@ -94,9 +98,12 @@ gather_sum_kernel(const uint4* __restrict__ rows, const float* __restrict__ w,
   }
 }
 
-// One warp per token: dy[p] = bf16(w[a] * dout[t]) and dw[a] = <dout[t], y[p]>.
-// dy is the exact product rounded once, so it is bit-identical to any
-// correctly rounded evaluation.
+// One warp per token: dy[p] = bf16(w[a] * dout[t]) and dw[a] = <dout[t], y[p]>
+// for its K assignments a = t*K + j, p = inv_perm[a]. Each lane walks its
+// 16-byte columns once, with the K gathered loads of a column in flight
+// together and one dot-product accumulator per slot. dy is the exact product
+// rounded once, so it is bit-identical to any correctly rounded evaluation.
+template <int KMAX>
 __global__ void __launch_bounds__(kThreads)
 combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ y,
                         const float* __restrict__ w, const int32_t* __restrict__ inv_perm, int T,
@@ -106,26 +113,44 @@ combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict_
   for (long long t = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
        t < T; t += warps) {
     const uint4* drow = dout + t * nv;
-    for (int j = 0; j < K; ++j) {
-      const long long a = t * K + j;
-      const long long p = __ldg(inv_perm + a);
-      const float wa = __ldg(w + a);
-      const uint4* yrow = y + p * nv;
-      uint4* dyrow = dy + p * nv;
-      float dot = 0.f;
-#pragma unroll 4
-      for (int c = lane; c < nv; c += 32) {
-        const uint4 dv = __ldg(drow + c);
-        const uint4 yv = ldg_nc_v4(yrow + c);
-        float fd[8], fy[8], g[8];
-        unpack8(dv, fd);
-        unpack8(yv, fy);
+    long long prow[KMAX];
+    float wa[KMAX], dot[KMAX];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) { dot = fmaf(fd[q], fy[q], dot); g[q] = mul_bf16_exact(wa, fd[q]); }
-        stg_v4(dyrow + c, pack8(g));
+    for (int j = 0; j < KMAX; ++j) {
+      dot[j] = 0.f;
+      if (j < K) {
+        prow[j] = static_cast<long long>(__ldg(inv_perm + t * K + j)) * nv;
+        wa[j] = __ldg(w + t * K + j);
       }
-      dot = warp_sum(dot);
-      if (lane == 0) dw[a] = dot;
+    }
+    for (int c = lane; c < nv; c += 32) {
+      const uint4 dv = ldg_nc_v4(drow + c);
+      uint4 yv[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < K) yv[j] = ldg_nc_v4(y + prow[j] + c);
+      float fd[8];
+      unpack8(dv, fd);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < K) {
+          float fy[8], g[8];
+          unpack8(yv[j], fy);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            dot[j] = fmaf(fd[q], fy[q], dot[j]);
+            g[q] = mul_bf16_exact(wa[j], fd[q]);
+          }
+          stg_v4(dy + prow[j] + c, pack8(g));
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < K) {
+        const float s = warp_sum(dot[j]);
+        if (lane == 0) dw[t * K + j] = s;
+      }
     }
   }
 }
@@ -165,11 +190,11 @@ extern "C" int moe_dispatch(const moe_bf16* x, int T, int d, int K, const int32_
   if (!x || !perm || !xp) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(perm) || !aligned16(xp)) return MOE_ERR_MISALIGNED;
   const int nv = d / 8;
-  const long long total = static_cast<long long>(T) * K * nv;
-  const int grid = grid_for(total, kThreads * kUnroll);
+  const long long rows = static_cast<long long>(T) * K;
+  const int grid = grid_for(rows, kThreads / 32);
   ProfScope prof("dispatch", as_stream(stream));
   dispatch_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(
-      reinterpret_cast<const uint4*>(x), perm, K, nv, total, reinterpret_cast<uint4*>(xp));
+      reinterpret_cast<const uint4*>(x), perm, K, nv, rows, reinterpret_cast<uint4*>(xp));
   return check_launch();
 }
 
@@ -213,8 +238,15 @@ extern "C" int moe_combine_backward(const moe_bf16* dout, const moe_bf16* y, con
   const long long cap = static_cast<long long>(num_sms()) * 16;
   if (blocks > cap) blocks = cap;
   ProfScope prof("combine_backward", as_stream(stream));
-  combine_backward_kernel<<<static_cast<int>(blocks), kThreads, 0, as_stream(stream)>>>(
-      reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(y), topk_w, inv_perm,
-      T, K, d / 8, reinterpret_cast<uint4*>(dy), dtopk_w);
+  auto go = [&](auto kern) {
+    kern<<<static_cast<int>(blocks), kThreads, 0, as_stream(stream)>>>(
+        reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(y), topk_w, inv_perm,
+        T, K, d / 8, reinterpret_cast<uint4*>(dy), dtopk_w);
+  };
+  if (K <= 2) go(combine_backward_kernel<2>);
+  else if (K <= 4) go(combine_backward_kernel<4>);
+  else if (K <= 8) go(combine_backward_kernel<8>);
+  else if (K <= 16) go(combine_backward_kernel<16>);
+  else go(combine_backward_kernel<32>);
   return check_launch();
 }

@@ -135,6 +135,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Pulls a tile into L2 only (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -309,6 +317,79 @@ __device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int* s
 }
 
 // ----------------------------------------------------------------- kernel
+// The TMA boxes of one k-block of a tile: loaded into a pipeline stage
+// (PREFETCH = false) or only pulled into L2 (PREFETCH = true; measured slower
+// on the qwen3 workload when issued 8 k-blocks ahead, so the kernels do not use it).
+template <int KIND, int BN, bool PREFETCH>
+__device__ __forceinline__ void issue_kblock(const Tile& tl, int kb, const Params& p,
+                                             const CUtensorMap* tmA, const CUtensorMap* tmB0,
+                                             const CUtensorMap* tmB1, uint32_t sa, uint32_t sb,
+                                             uint32_t fb) {
+  constexpr uint32_t MN_ATOM = 64 * 128;
+  auto box = [&](const CUtensorMap* m, uint32_t dst, int x, int y) {
+    if constexpr (PREFETCH) tma_prefetch_2d(m, x, y);
+    else tma_load_2d(dst, m, fb, x, y);
+  };
+  if constexpr (KIND == FWD_GATEUP) {
+    box(tmA, sa, kb * BK, tl.row0);
+    const int yb = tl.e * p.d + kb * BK;
+#pragma unroll
+    for (int i = 0; i < BN / 128; ++i) {
+      box(tmB0, sb + i * MN_ATOM, tl.n0 + 64 * i, yb);
+      box(tmB1, sb + (BN / 128 + i) * MN_ATOM, tl.n0 + 64 * i, yb);
+    }
+  } else if constexpr (KIND == FWD_DOWN) {
+    box(tmA, sa, kb * BK, tl.row0);
+    const int yb = tl.e * p.I + kb * BK;
+#pragma unroll
+    for (int i = 0; i < BN / 64; ++i) box(tmB0, sb + i * MN_ATOM, tl.n0 + 64 * i, yb);
+  } else if constexpr (KIND == BWD_DH) {
+    box(tmA, sa, kb * BK, tl.row0);
+    box(tmB0, sb, kb * BK, tl.e * p.I + tl.n0);
+  } else if constexpr (KIND == BWD_DX) {
+    box(tmA, sa, kb * BK, tl.row0);
+    const int kx = kb * BK;
+    if (kx < p.I) box(tmB0, sb, kx, tl.e * p.d + tl.n0);
+    else box(tmB1, sb, kx - p.I, tl.e * p.d + tl.n0);
+  } else {  // weight gradients: both operands MN-major, K = token rows
+    const int ky = tl.row0 + kb * BK;
+    box(tmA, sa, tl.m0, ky);
+    box(tmA, sa + MN_ATOM, tl.m0 + 64, ky);
+#pragma unroll
+    for (int i = 0; i < BN / 64; ++i) box(tmB0, sb + i * MN_ATOM, tl.n0 + 64 * i, ky);
+  }
+}
+
+// Walks this CTA's (tile, k-block) sequence in the order the MMA consumes it,
+// skipping tiles without k-blocks.
+template <int KIND, int BN>
+struct KStream {
+  int t, kb, total;
+  bool valid;
+  Tile tl;
+  __device__ __forceinline__ void settle(const Params& p, const int* s_off, const int* s_mt) {
+    while (t < total) {
+      tl = decode_tile<KIND, BN>(t, p, s_off, s_mt);
+      if (tl.nkb > 0) break;
+      t += gridDim.x;
+    }
+    valid = t < total;
+  }
+  __device__ __forceinline__ void start(int t0, int tot, const Params& p, const int* s_off,
+                                        const int* s_mt) {
+    t = t0;
+    kb = 0;
+    total = tot;
+    settle(p, s_off, s_mt);
+  }
+  __device__ __forceinline__ void next(const Params& p, const int* s_off, const int* s_mt) {
+    if (++kb < tl.nkb) return;
+    kb = 0;
+    t += gridDim.x;
+    settle(p, s_off, s_mt);
+  }
+};
+
 // Epilogue shared memory per kind: weight gradients stage one [32 rows x 32 fp32]
 // block per epilogue warp for a bulk tensor store; gemm_dh prefetches, per
 // epilogue warp, the saved G and U of 32 rows x 128 columns (four [32 x 64]
@@ -411,50 +492,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t issued[STAGES];
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) issued[s] = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<KIND, BN>(t, p, s_off, s_mt);
-        for (int kb = 0; kb < tl.nkb; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          const uint32_t fb = full_bar(stage);
-          mbar_expect_tx(fb, STAGE_BYTES);
-          const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          if constexpr (KIND == FWD_GATEUP) {
-            tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
-            const int yb = tl.e * p.d + kb * BK;
-#pragma unroll
-            for (int i = 0; i < BN / 128; ++i) {
-              tma_load_2d(sb + i * MN_ATOM, &tmB0, fb, tl.n0 + 64 * i, yb);
-              tma_load_2d(sb + (BN / 128 + i) * MN_ATOM, &tmB1, fb, tl.n0 + 64 * i, yb);
-            }
-          } else if constexpr (KIND == FWD_DOWN) {
-            tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
-            const int yb = tl.e * p.I + kb * BK;
-#pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-              tma_load_2d(sb + i * MN_ATOM, &tmB0, fb, tl.n0 + 64 * i, yb);
-          } else if constexpr (KIND == BWD_DH) {
-            tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
-            tma_load_2d(sb, &tmB0, fb, kb * BK, tl.e * p.I + tl.n0);
-          } else if constexpr (KIND == BWD_DX) {
-            tma_load_2d(sa, &tmA, fb, kb * BK, tl.row0);
-            const int kx = kb * BK;
-            if (kx < p.I)
-              tma_load_2d(sb, &tmB0, fb, kx, tl.e * p.d + tl.n0);
-            else
-              tma_load_2d(sb, &tmB1, fb, kx - p.I, tl.e * p.d + tl.n0);
-          } else {  // weight gradients: both operands MN-major, K = token rows
-            const int ky = tl.row0 + kb * BK;
-            tma_load_2d(sa, &tmA, fb, tl.m0, ky);
-            tma_load_2d(sa + MN_ATOM, &tmA, fb, tl.m0 + 64, ky);
-#pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-              tma_load_2d(sb + i * MN_ATOM, &tmB0, fb, tl.n0 + 64 * i, ky);
-          }
-          issued[stage] += 1;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
+      KStream<KIND, BN> ld;
+      ld.start(blockIdx.x, total, p, s_off, s_mt);
+      while (ld.valid) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) break;
+        const uint32_t fb = full_bar(stage);
+        mbar_expect_tx(fb, STAGE_BYTES);
+        const uint32_t sa = smem_base + stage * STAGE_BYTES;
+        issue_kblock<KIND, BN, false>(ld.tl, ld.kb, p, &tmA, &tmB0, &tmB1, sa, sa + A_BYTES, fb);
+        issued[stage] += 1;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        ld.next(p, s_off, s_mt);
       }
       // make sure no TMA write into this CTA's shared memory is still in flight
       for (int s = 0; s < STAGES; ++s) {

@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
-    ap.add_argument("--profile-case", choices=["gemm", "layer"], default=None,
+    ap.add_argument("--profile-case", choices=["gemm", "gemm_l2", "layer"], default=None,
                     help="run a small fixed case twice for an ncu capture and exit")
     return ap.parse_args()
 
@@ -60,9 +60,14 @@ def parse():
 def profile_case(which: str):
     """Small cases for ncu captures (inputs above the 129 MB L2, a few GB on the device).
 
-    gemm:  the grouped-GEMM entry points, forward and backward, on E=64 experts x 512 rows
-           (d=2048, I=768; the qwen3 workload's rows per expert), run twice.
-    layer: one qwen3-shaped layer at T=2048 tokens (forward + backward), run twice.
+    gemm:    the grouped-GEMM entry points, forward and backward, on E=64 experts x 512 rows
+             (d=2048, I=768; the qwen3 workload's rows per expert), run twice.
+    gemm_l2: the same entry points on one expert of 16384 rows (d=2048, I=768): weights
+             and activations mostly resident in L2, which isolates the kernels' own
+             pipeline from DRAM streaming.
+    layer:   one qwen3-shaped layer at T=2048 tokens (forward + backward), run twice.
+    Prints each kernel's launch time (CUDA events on the launching stream) and rate for
+    the last run.
     """
     import torch
     from grouped_gemm_moe_gb300 import binding as B
@@ -73,15 +78,22 @@ def profile_case(which: str):
         build_mod.build()
     dev = torch.device("cuda:0")
     g = torch.Generator(device=dev).manual_seed(0)
-    if which == "gemm":
-        E, d, I, rows = 64, 2048, 768, 512
+    flops = {}
+    if which in ("gemm", "gemm_l2"):
+        E, d, I, rows = (64, 2048, 768, 512) if which == "gemm" else (1, 2048, 768, 16384)
         M = E * rows
+        flops = {"gemm_gate_up": 4 * M * d * I, "gemm_down": 2 * M * d * I, "gemm_dh": 2 * M * d * I,
+                 "gemm_dx": 4 * M * d * I, "gemm_wgrad_gate_up": 4 * M * d * I,
+                 "gemm_wgrad_down": 2 * M * d * I}
         bf = torch.bfloat16
         rnd = lambda *s, sc=1.0: (torch.randn(*s, device=dev, generator=g) * sc).to(bf)  # noqa: E731
         off = torch.arange(0, M + 1, rows, dtype=torch.int32, device=dev)
         xp, dy, gu, h = rnd(M, d), rnd(M, d, sc=0.1), rnd(M, 2 * I), rnd(M, I, sc=0.5)
         wg, wu, wd = rnd(E, d, I, sc=0.02), rnd(E, d, I, sc=0.02), rnd(E, I, d, sc=0.02)
-        for _ in range(2):
+        for it in range(2):
+            if it == 1:
+                torch.cuda.synchronize()
+                B.moe_profile_start(64)
             B.moe_grouped_ffn_backward(dy, xp, gu, h, off, wg, wu, wd)
             B.moe_grouped_ffn(xp, off, wg, wu, wd)
     else:
@@ -93,6 +105,9 @@ def profile_case(which: str):
             layer.forward(logits, x)
             layer.backward(dout)
     torch.cuda.synchronize()
+    if flops:
+        for name, ms in B.moe_profile_stop():
+            print(f"  {name:22s} {ms * 1e3:9.1f} us  {flops.get(name, 0) / (ms * 1e-3) / 1e12:8.1f} TFLOP/s")
     print(f"profile case {which} ok, peak {torch.cuda.max_memory_allocated() / 2**30:.2f} GiB")
 
 

@@ -109,9 +109,8 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase of `bar` with the given parity to complete.
 // Returns false if this CTA is aborting (another role timed out) or the wait
 // itself ran past kTimeoutNs (then it raises the abort flag and the status).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       int* status) {
-  if (mbar_try(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                            volatile int* abort_flag, int* status) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try(bar, parity)) return true;
@@ -124,6 +123,13 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       }
     }
   }
+}
+
+// Fast path inline (the phase is usually complete already), slow path out of line.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, status);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -224,6 +230,70 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---- CTA-pair (cluster of two, tcgen05 cta_group::2) helpers
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t n_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+// D[tmem of both CTAs] (+)= A[smem of both] * B[smem of both]^T, M = 256.
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier at this offset in both CTAs when this thread's MMAs complete.
+__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
+  const uint16_t mask = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle, descriptor version 1.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -235,12 +305,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return d;
 }
 
-// Instruction descriptor for kind::f16: fp32 D, bf16 A and B, M = 128.
-template <int N, bool A_MN, bool B_MN>
+// Instruction descriptor for kind::f16: fp32 D, bf16 A and B, M rows (128, or 256 for a pair).
+template <int N, bool A_MN, bool B_MN, int M = BM>
 __host__ __device__ constexpr uint32_t make_idesc() {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) |
          ((B_MN ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(BM >> 4) << 24);
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
@@ -528,7 +598,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       for (int kb = 0; kb < tl.nkb; ++kb) {
         if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
         const uint32_t sa = smem_base + stage * STAGE_BYTES;
         const uint32_t sb = sa + A_BYTES;
         if constexpr (kWgrad) {
@@ -756,6 +825,382 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   }
 }
 
+// ----------------------------------------------------------------- CTA-pair kernel
+// Forward and input-gradient kinds on a cluster of two CTAs that share one
+// tcgen05 MMA of M = 256 (cta_group::2): each CTA holds 128 rows of A and half
+// of B's N in its own shared memory, the leader (cluster rank 0) issues the
+// MMA, and each CTA's TMEM receives its own 128 rows of the 256 x BN
+// accumulator. Per CTA a k-block stage is 32 KB for 276 ns of MMA work (half
+// the bytes of a single-CTA 128 x 256 tile), so six stages hide 1.4 us of
+// load latency.
+//
+// Tiles pair two 128-row m-tiles of the same expert (the second may be past
+// the expert's end and then stores nothing), times BN-wide n-tiles.
+struct PTile {
+  int e;
+  int row0;   // this CTA's first packed row
+  int rows;   // this CTA's valid rows (<= 0: none)
+  int n0;
+};
+
+template <int KIND, int BN>
+__device__ __forceinline__ PTile decode_pair(int t, int rank, const Params& p, const int* s_off,
+                                             const int* s_mp) {
+  PTile tl;
+  const int mg = t / p.n_tiles;
+  const int nt = t - mg * p.n_tiles;
+  int lo = 0, hi = p.E - 1;   // largest e with s_mp[e] <= mg
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_mp[mid] <= mg) lo = mid; else hi = mid - 1;
+  }
+  tl.e = lo;
+  tl.row0 = s_off[lo] + (2 * (mg - s_mp[lo]) + rank) * BM;
+  tl.rows = min(BM, s_off[lo + 1] - tl.row0);
+  tl.n0 = nt * (KIND == FWD_GATEUP ? BN / 2 : BN);
+  return tl;
+}
+
+// This CTA's boxes of one k-block: its 128 A rows and its half of B (gate or up
+// for the gate/up GEMM), counted on the leader's full barrier.
+template <int KIND, int BN>
+__device__ __forceinline__ void issue_pair(const PTile& tl, int kb, uint32_t rank, const Params& p,
+                                           const CUtensorMap* tmA, const CUtensorMap* tmB0,
+                                           const CUtensorMap* tmB1, uint32_t sa, uint32_t sb,
+                                           uint32_t fb) {
+  constexpr uint32_t MN_ATOM = 64 * 128;
+  constexpr int HB = BN / 2;
+  tma_load_2d_pair(sa, tmA, fb, kb * BK, tl.row0);
+  if constexpr (KIND == FWD_GATEUP) {
+    const CUtensorMap* m = rank ? tmB1 : tmB0;
+#pragma unroll
+    for (int i = 0; i < HB / 64; ++i)
+      tma_load_2d_pair(sb + i * MN_ATOM, m, fb, tl.n0 + 64 * i, tl.e * p.d + kb * BK);
+  } else if constexpr (KIND == FWD_DOWN) {
+#pragma unroll
+    for (int i = 0; i < HB / 64; ++i)
+      tma_load_2d_pair(sb + i * MN_ATOM, tmB0, fb, tl.n0 + static_cast<int>(rank) * HB + 64 * i,
+                       tl.e * p.I + kb * BK);
+  } else if constexpr (KIND == BWD_DH) {
+    tma_load_2d_pair(sb, tmB0, fb, kb * BK, tl.e * p.I + tl.n0 + static_cast<int>(rank) * HB);
+  } else {  // BWD_DX
+    const int kx = kb * BK;
+    const int y = tl.e * p.d + tl.n0 + static_cast<int>(rank) * HB;
+    if (kx < p.I) tma_load_2d_pair(sb, tmB0, fb, kx, y);
+    else tma_load_2d_pair(sb, tmB1, fb, kx - p.I, y);
+  }
+}
+
+template <int KIND, int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB0,
+                         const __grid_constant__ CUtensorMap tmB1,
+                         const __grid_constant__ CUtensorMap tmC0,
+                         const __grid_constant__ CUtensorMap tmC1, const Params p) {
+  static_assert(KIND == FWD_GATEUP || KIND == FWD_DOWN || KIND == BWD_DH || KIND == BWD_DX,
+                "pair kernel: forward and input-gradient kinds");
+  constexpr bool B_MN = (KIND == FWD_GATEUP || KIND == FWD_DOWN);
+  constexpr uint32_t A_BYTES = BM * BK * 2;
+  constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr uint32_t IDESC = make_idesc<BN, false, B_MN, 2 * BM>();
+  constexpr uint32_t MN_ATOM = 64 * 128;
+  (void)tmC1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* epi = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + epi_bytes<KIND>());
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, aux[4]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_mp = s_off + (p.E + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = (rank == 0);
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
+  auto aux_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + 5 + w); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    // the leader's accumulator-empty barriers collect the four epilogue warps of both CTAs
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 8); }
+    mbar_init(drain_bar, 1);
+    for (int w = 0; w < 4; ++w) mbar_init(aux_bar(w), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB0)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB1)) : "memory");
+    if constexpr (KIND == BWD_DH)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
+  }
+  if (warp == 1) {   // one warp in each CTA of the pair allocates collectively
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
+  __syncthreads();
+  if (warp == 0) {   // exclusive prefix of per-expert m-tile pairs
+    int carry = 0;
+    for (int base = 0; base <= p.E; base += 32) {
+      const int i = base + lane;
+      const int v = (i < p.E) ? ((s_off[i + 1] - s_off[i] + BM - 1) / BM + 1) / 2 : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (i <= p.E) s_mp[i] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers exist before any remote arrive or TMA
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // both CTAs must hold the same TMEM columns for the pair's MMAs; otherwise do nothing
+  uint32_t peer_base;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];"
+               : "=r"(peer_base)
+               : "r"(map_to_rank(smem_u32(tmem_slot), rank ^ 1u))
+               : "memory");
+  const bool tmem_ok = (peer_base == tmem_base);
+  if (!tmem_ok && threadIdx.x == 0) report_status(p.status, MOE_ERR_DEVICE_CHECK);
+  const int total = tmem_ok ? s_mp[p.E] * p.n_tiles : 0;
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(n_clusters_x());
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl) {
+        const PTile tl = decode_pair<KIND, BN>(t, static_cast<int>(rank), p, s_off, s_mp);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t fb_local = full_bar(stage);
+          if (leader) mbar_expect_tx(fb_local, 2 * STAGE_BYTES);   // both CTAs' boxes
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          issue_pair<KIND, BN>(tl, kb, rank, p, &tmA, &tmB0, &tmB1, sa, sa + A_BYTES,
+                               map_to_rank(fb_local, 0));
+          issued[stage] += 1;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (leader) {
+        // the leader's full barriers count both CTAs' loads: wait for the last phases
+        for (int s = 0; s < STAGES; ++s) {
+          if (!issued[s]) continue;
+          const uint32_t par = (issued[s] - 1u) & 1u;
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try(full_bar(s), par) && globaltimer() - t0 < kTimeoutNs) {
+          }
+        }
+      } else if (!ok) {
+        // loads of this CTA may still be landing after a timeout: give them a moment
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 1000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          if (lane == 0) {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+              uint64_t bd;
+              if constexpr (B_MN) bd = smem_desc(sb + kk * 2048, MN_ATOM, 1024);
+              else bd = smem_desc(sb + kk * 32, 16, 1024);
+              tc_mma_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit_pair_both(empty_bar(stage));
+          }
+          __syncwarp();
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit_pair_both(tfull_bar(acc));
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (lane == 0) {
+        tc_commit_pair_local(drain_bar);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(drain_bar, 0) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t aux_phase = 0;
+    bool aux_pending = false;
+    for (int t = cid; t < total; t += ncl) {
+      const PTile tl = decode_pair<KIND, BN>(t, static_cast<int>(rank), p, s_off, s_mp);
+      const bool valid = r < tl.rows;
+      const size_t grow = static_cast<size_t>(tl.row0 + r);
+      if constexpr (KIND == BWD_DH) {
+        uint8_t* aux = epi + ew * 16384;
+        const uint32_t aux_addr = smem_u32(aux);
+        const uint32_t ab = aux_bar(ew);
+        const int grow0 = tl.row0 + q * 32;
+        auto request = [&](int c0) {
+          if (lane == 0) {
+            mbar_expect_tx(ab, 16384);
+            tma_load_2d(aux_addr, &tmC0, ab, tl.n0 + c0, grow0);
+            tma_load_2d(aux_addr + 4096, &tmC0, ab, tl.n0 + c0 + 64, grow0);
+            tma_load_2d(aux_addr + 8192, &tmC0, ab, p.I + tl.n0 + c0, grow0);
+            tma_load_2d(aux_addr + 12288, &tmC0, ab, p.I + tl.n0 + c0 + 64, grow0);
+          }
+          aux_pending = true;
+        };
+        request(0);
+        if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int c0 = 0; c0 < BN; c0 += 128) {
+          if (c0) request(c0);
+          if (!mbar_wait(ab, aux_phase, abort_flag, p.status)) { ok = false; break; }
+          aux_phase ^= 1u;
+          aux_pending = false;
+          for (int c = 0; c < 128; c += 16) {
+            float dh[16];
+            tmem_ld16(tacc + c0 + c, dh);
+            tmem_wait_ld();
+            const int box = c >> 6;
+            const int j0 = (c & 63) >> 3;
+            float g[16], u[16];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int off = lane * 128 + (((j0 + hh) ^ (lane & 7)) << 4);
+              float f[8];
+              unpack8(*reinterpret_cast<const uint4*>(aux + box * 4096 + off), f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) g[8 * hh + i] = f[i];
+              unpack8(*reinterpret_cast<const uint4*>(aux + 8192 + box * 4096 + off), f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) u[8 * hh + i] = f[i];
+            }
+            if (valid) {
+              float dg[16], du[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float sg = 1.f / (1.f + expf(-g[i]));
+                dg[i] = dh[i] * u[i] * sg * (1.f + g[i] * (1.f - sg));
+                du[i] = dh[i] * g[i] * sg;
+              }
+              __nv_bfloat16* orow = p.out + grow * (2 * p.I);
+              store16_bf16(orow + tl.n0 + c0 + c, dg);
+              store16_bf16(orow + p.I + tl.n0 + c0 + c, du);
+            }
+          }
+          fence_proxy_async();
+          __syncwarp();
+        }
+        if (!ok) break;
+      } else {
+        if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
+        if constexpr (KIND == FWD_GATEUP) {
+          constexpr int HALF = BN / 2;
+          for (int c = 0; c < HALF; c += 16) {
+            float g[16], u[16], h[16];
+            tmem_ld16(tacc + c, g);
+            tmem_ld16(tacc + HALF + c, u);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) h[i] = silu_f(g[i]) * u[i];
+              store16_bf16(p.out + grow * p.I + tl.n0 + c, h);
+              if (p.out2) {
+                store16_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c, g);
+                store16_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c, u);
+              }
+            }
+          }
+        } else {
+          for (int c = 0; c < BN; c += 16) {
+            float v[16];
+            tmem_ld16(tacc + c, v);
+            tmem_wait_ld();
+            if (valid) store16_bf16(p.out + grow * p.ld_out + tl.n0 + c, v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if constexpr (KIND == BWD_DH) {
+      if (lane == 0 && aux_pending) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(aux_bar(ew), aux_phase) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // the leader's MMAs into both TMEMs and all remote arrivals are done
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
 // ----------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -816,6 +1261,89 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
   return check_launch();
 }
 
+#ifndef MOE_PAIR_BN_MAX
+#define MOE_PAIR_BN_MAX 256
+#endif
+
+template <int KIND, int BN, int STAGES>
+size_t pair_smem_bytes(int E) {
+  return 1024 + STAGES * (BM * BK * 2 + (BN / 2) * BK * 2) + epi_bytes<KIND>() +
+         8 * (2 * STAGES + 9) + 16 + sizeof(int) * 2 * (E + 1) + 16;
+}
+
+// Launches the CTA-pair kernel on as many clusters of two as can be resident.
+template <int KIND, int BN, int STAGES>
+int launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
+                long long tiles_upper, cudaStream_t st) {
+  auto kern = grouped_gemm_pair_kernel<KIND, BN, STAGES>;
+  const size_t sm = pair_smem_bytes<KIND, BN, STAGES>(p.E);
+  const size_t sm_max = pair_smem_bytes<KIND, BN, STAGES>(1024);
+  static thread_local int configured = -1;
+  static thread_local int max_clusters = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (configured != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sm_max));
+    if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(2 * num_sms(), 1, 1);
+    q.dynamicSmemBytes = sm_max;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+    if (e != cudaSuccess || n < 1) {
+      set_last_cuda_error(e == cudaSuccess ? cudaErrorInvalidConfiguration : e);
+      return MOE_ERR_CUDA;
+    }
+    max_clusters = n;
+    configured = dev;
+  }
+  long long ncl = max_clusters;
+  if (tiles_upper < ncl) ncl = tiles_upper;
+  if (ncl < 1) return MOE_OK;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * ncl), 1, 1);
+  static const char* kNames[] = {"gemm_gate_up", "gemm_down", "gemm_dh", "gemm_dx", "", ""};
+  ProfScope prof(kNames[KIND], st);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b0, b1, c0, c1, p);
+  if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
+  return check_launch();
+}
+
+// Pair pipeline depth: 32 KB stages (64 KB of [G|U] prefetch buffers for dh).
+template <int KIND, int BN>
+constexpr int pair_stages() {
+  return KIND == BWD_DH ? (BN == 256 ? 4 : 5) : (BN == 256 ? 6 : 8);
+}
+
+template <int KIND>
+int launch_pair_bn(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                   const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
+                   long long tiles_upper, cudaStream_t st) {
+#if MOE_PAIR_BN_MAX >= 256
+  if (bn == 256)
+    return launch_pair<KIND, 256, pair_stages<KIND, 256>()>(a, b0, b1, c0, c1, p, tiles_upper, st);
+#endif
+  return launch_pair<KIND, 128, pair_stages<KIND, 128>()>(a, b0, b1, c0, c1, p, tiles_upper, st);
+}
+
+// The N width a pair tile uses for an output of n columns (n % 128 == 0).
+inline int pair_bn(int n) { return (n % 256 == 0 && MOE_PAIR_BN_MAX >= 256) ? 256 : 128; }
+
+static_assert(1024 + 6 * (16384 + 16384) + 8 * 21 + 32 + 8 * 1025 <= 232448, "pair smem");
+static_assert(1024 + 4 * (16384 + 16384) + 65536 + 8 * 17 + 32 + 8 * 1025 <= 232448, "pair dh smem");
+
 // Pipeline depth: as many operand stages as fit next to the kind's epilogue buffers
 // (227 KB of shared memory per CTA, expert tables for up to 1024 experts included).
 template <int KIND, int BN>
@@ -846,7 +1374,7 @@ size_t ffn_backward_scratch(long long M, int I) {
 namespace {
 
 bool ffn_shape_ok(int E, int M, int d, int I) {
-  return E >= 1 && E <= 1024 && M >= 0 && d > 0 && I > 0 && d % 64 == 0 && I % 128 == 0;
+  return E >= 1 && E <= 1024 && M >= 0 && d > 0 && I > 0 && d % 128 == 0 && I % 128 == 0;
 }
 
 }  // namespace
@@ -882,15 +1410,16 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
   if (!make_map(&ta, xp, d, M, 64, BM) || !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, 64) ||
       !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, 64))
     return MOE_ERR_CUDA;
-  p.n_tiles = I / 128;
+  const int bn_gu = (MOE_PAIR_BN_MAX >= 256) ? 256 : 128;   // half gate, half up columns
+  p.n_tiles = I / (bn_gu / 2);
   p.k_blocks = d / BK;
   p.out = reinterpret_cast<__nv_bfloat16*>(h);
   p.out2 = reinterpret_cast<__nv_bfloat16*>(gu);
   p.ld_out = I;
-  int rc = launch_bn<FWD_GATEUP>(256, ta, tb0, tb1, ta, ta, p, mt_upper * p.n_tiles, st);
+  int rc = launch_pair_bn<FWD_GATEUP>(bn_gu, ta, tb0, tb1, ta, ta, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // down projection
-  const int bn = (d % 256 == 0) ? 256 : 128;
+  const int bn = pair_bn(d);
   if (!make_map(&ta, h, I, M, 64, BM) || !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, 64))
     return MOE_ERR_CUDA;
   p.n_tiles = d / bn;
@@ -898,7 +1427,7 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
   p.out = reinterpret_cast<__nv_bfloat16*>(y);
   p.out2 = nullptr;
   p.ld_out = d;
-  return launch_bn<FWD_DOWN>(bn, ta, tb0, tb0, ta, ta, p, mt_upper * p.n_tiles, st);
+  return launch_pair_bn<FWD_DOWN>(bn, ta, tb0, tb0, ta, ta, p, mt_upper * p.n_tiles, st);
 }
 
 extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
@@ -943,9 +1472,9 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   const long long mt_upper = (M + BM - 1) / BM + E;
   CUtensorMap ta, tb0, tb1, tc0, tc1;
   // dH = dY Wd^T with the SwiGLU backward epilogue -> [dG | dU]
-  const int bn_h = (I % 256 == 0) ? 256 : 128;
+  const int bn_h = pair_bn(I);
   if (!make_map(&ta, dy, d, M, 64, BM) ||
-      !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h) ||
+      !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h / 2) ||
       !make_map(&tc0, gu, 2 * static_cast<uint64_t>(I), M, 64, 32))
     return MOE_ERR_CUDA;
   p.n_tiles = I / bn_h;
@@ -953,20 +1482,20 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   p.out = dgu;
   p.aux = reinterpret_cast<const __nv_bfloat16*>(gu);
   p.ld_out = 2 * I;
-  int rc = launch_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc0, p, mt_upper * p.n_tiles, st);
+  int rc = launch_pair_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc0, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // dX = dG Wg^T + dU Wu^T
-  const int bn_x = (d % 256 == 0) ? 256 : 128;
+  const int bn_x = pair_bn(d);
   if (!make_map(&ta, dgu, 2 * static_cast<uint64_t>(I), M, 64, BM) ||
-      !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, bn_x) ||
-      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, bn_x))
+      !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2) ||
+      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2))
     return MOE_ERR_CUDA;
   p.n_tiles = d / bn_x;
   p.k_blocks = 2 * I / BK;
   p.out = reinterpret_cast<__nv_bfloat16*>(dxp);
   p.aux = nullptr;
   p.ld_out = d;
-  rc = launch_bn<BWD_DX>(bn_x, ta, tb0, tb1, ta, ta, p, mt_upper * p.n_tiles, st);
+  rc = launch_pair_bn<BWD_DX>(bn_x, ta, tb0, tb1, ta, ta, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // [dWg | dWu] = X^T [dG | dU]
   if (!make_map(&ta, xp, d, M, 64, 64) || !make_map(&tb0, dgu, 2 * static_cast<uint64_t>(I), M, 64, 64) ||

@@ -12,11 +12,11 @@
 //
 // Design: a two-kernel stable counting sort, deterministic and free of
 // atomics on positions.
-//  1. hist:    the assignments are cut into chunks of 4096 that never straddle
-//              a sender block. Each warp counts its 256 assignments per expert
+//  1. hist:    the assignments are cut into chunks of 1024 that never straddle
+//              a sender block. Each warp counts its 128 assignments per expert
 //              with __match_any_sync (one leader per equal-id group adds the
 //              group's popcount to a warp-private counter), then the CTA sums
-//              the 16 warps into hist[chunk][e].
+//              the 8 warps into hist[chunk][e].
 //  2. scatter: every CTA reads the whole (small) hist table and derives, per
 //              expert, the counts/offsets and the prefix of earlier chunks;
 //              it redoes the warp counts, scans them across warps, and walks
@@ -28,11 +28,11 @@
 namespace moe {
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSteps = 8;
-constexpr int kPerWarp = kSteps * 32;          // 256 assignments per warp
-constexpr int kChunk = kWarps * kPerWarp;      // 4096 assignments per CTA
+constexpr int kSteps = 4;
+constexpr int kPerWarp = kSteps * 32;          // 128 assignments per warp
+constexpr int kChunk = kWarps * kPerWarp;      // 1024 assignments per CTA
 
 struct ChunkGeom {
   long long seg_len;   // assignments per sender block (T*K/R)

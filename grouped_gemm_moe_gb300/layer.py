@@ -141,19 +141,37 @@ class MoELayer:
     def step_from_host(self, logits_h: torch.Tensor, x_h: torch.Tensor, dout_h: torch.Tensor,
                        out_h: torch.Tensor, dx_h: torch.Tensor):
         """One forward + backward whose inputs start in (pinned) host memory and
-        whose outputs end there: copies in, runs the layer, copies out, all
-        enqueued on the current stream. Returns the bytes copied each way."""
+        whose outputs end there. logits and x are copied in on the current
+        stream; dout is copied in on a side stream while the forward runs, and
+        the output is copied out on the side stream while the backward runs.
+        The current stream joins the side stream before returning, so work
+        enqueued after this call sees every copy finished. Returns the bytes
+        copied each way."""
+        dev = self.device
         if not hasattr(self, "_in_logits"):
-            self._in_logits = torch.empty(self.T, self.E, dtype=torch.float32, device=self.device)
-            self._in_x = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=self.device)
-            self._in_dout = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=self.device)
+            self._in_logits = torch.empty(self.T, self.E, dtype=torch.float32, device=dev)
+            self._in_x = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=dev)
+            self._in_dout = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=dev)
+            self._side = torch.cuda.Stream(device=dev)
+        cur = torch.cuda.current_stream(dev)
+        side = self._side
+        side.wait_stream(cur)                 # earlier readers of _in_dout / out are done
         self._in_logits.copy_(logits_h, non_blocking=True)
         self._in_x.copy_(x_h, non_blocking=True)
-        self._in_dout.copy_(dout_h, non_blocking=True)
+        with torch.cuda.stream(side):
+            self._in_dout.copy_(dout_h, non_blocking=True)
+            dout_ready = torch.cuda.Event()
+            dout_ready.record(side)
         out = self.forward(self._in_logits, self._in_x)
+        fwd_done = torch.cuda.Event()
+        fwd_done.record(cur)
+        with torch.cuda.stream(side):
+            side.wait_event(fwd_done)
+            out_h.copy_(out, non_blocking=True)
+        cur.wait_event(dout_ready)
         dx = self.backward(self._in_dout)
-        out_h.copy_(out, non_blocking=True)
         dx_h.copy_(dx, non_blocking=True)
+        cur.wait_stream(side)
         h2d = logits_h.numel() * 4 + x_h.numel() * 2 + dout_h.numel() * 2
         d2h = out_h.numel() * 2 + dx_h.numel() * 2 + self.host_splits.numel() * 4
         return h2d, d2h

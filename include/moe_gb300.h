@@ -128,8 +128,8 @@ int moe_build_permutation(const int32_t* topk_idx, int T, int E, int K,
  *   workspace. The per-chunk expert histogram lives instead in one file-scope
  *   device array of MOE_STATIC_HIST_INTS int32 (1 MiB) that every GPU loading
  *   the library holds until the process exits.
- *   Limit: ceil(T*K / 4096) * E <= MOE_STATIC_HIST_INTS (for example E = 128
- *   up to T*K = 8,388,608); larger problems return MOE_ERR_WORKSPACE before
+ *   Limit: ceil(T*K / 1024) * E <= MOE_STATIC_HIST_INTS (for example E = 128
+ *   up to T*K = 2,097,152); larger problems return MOE_ERR_WORKSPACE before
  *   anything is enqueued. Other limits as moe_build_permutation.
  *   The first call on a device looks up that device's address of the array
  *   (cudaGetSymbolAddress, with the device current) and caches it; make that
@@ -192,7 +192,7 @@ int moe_dispatch(const moe_bf16* x, int T, int d, int K, const int32_t* perm,
  *   y  [M,d] bf16 out.   h [M,I] bf16 out (needed by the down projection).
  *   gu [M,2I] bf16 out, or NULL to skip saving it.
  *   ws: moe_workspace_size(MOE_OP_GROUPED_FFN, ...), status word only.
- * Limits: d % 64 == 0, I % 128 == 0, E <= 1024. Also used with E = 1 and
+ * Limits: d % 128 == 0, I % 128 == 0, E <= 1024. Also used with E = 1 and
  * offsets {0, T} for always-on shared experts ([SF] "What this adds"). */
 int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E, int M, int d, int I,
                     const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,

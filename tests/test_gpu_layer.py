@@ -137,3 +137,24 @@ def test_exactly_one_device_to_host_copy_per_forward(tmp_path):
     d2h, copies = (int(v) for v in r.stdout.strip().split()[-2:])
     assert d2h == 1, r.stdout
     assert copies == 1, r.stdout
+
+
+def test_step_from_host_matches_device_path():
+    """The pinned-host-buffer step (copies overlapped with compute on a side
+    stream) gives bit-identical outputs to the device-resident path: every
+    kernel is deterministic, so any ordering bug would show as a difference."""
+    cfg = W.small_config("host", T=1024, d=256, E=16, K=4, I=256, R=4)
+    inp = W.make_inputs(cfg, with_backward=True)
+    layer = L.layer_from_config(cfg, inp, dev())
+    out_d = layer.forward(inp["logits"].to(dev()), inp["x"].to(dev())).clone()
+    dx_d = layer.backward(inp["dout"].to(dev())).clone()
+    lh, xh, dh = (inp[k].pin_memory() for k in ("logits", "x", "dout"))
+    out_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    dx_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    for _ in range(3):
+        out_h.zero_()
+        dx_h.zero_()
+        layer.step_from_host(lh, xh, dh, out_h, dx_h)
+        torch.cuda.synchronize()
+        assert torch.equal(out_h, out_d.cpu())
+        assert torch.equal(dx_h, dx_d.cpu())

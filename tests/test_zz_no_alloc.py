@@ -62,6 +62,6 @@ def test_static_scratch_rejects_problems_beyond_its_size():
     lib = B.load()
     fake = ctypes.c_void_p(0x10000)   # never dereferenced: the size check comes first
     E, K = 1024, 8
-    T = ((1 << 18) // E + 1) * 4096 // K      # one chunk row more than the array holds
+    T = ((1 << 18) // E + 1) * 1024 // K      # one chunk row more than the array holds
     rc = lib.moe_build_permutation_static(fake, T, E, K, fake, fake, fake, fake, None)
     assert rc == B.MOE_ERR_WORKSPACE

@@ -217,6 +217,10 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// At most one of this thread's committed bulk store groups is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // This thread's committed bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -891,6 +895,39 @@ __device__ __forceinline__ void issue_pair(const PTile& tl, int kb, uint32_t ran
   }
 }
 
+// Pair-kernel epilogue shared memory: bf16 output staging for bulk tensor stores,
+// per epilogue warp one [32 rows x 64 columns] 128-byte-swizzled box per output
+// stream (gate/up: H, G, U; down and dX: two buffers of Y), and for dh the
+// four G/U prefetch boxes, which the dG/dU results overwrite before their store.
+template <int KIND>
+__host__ __device__ constexpr uint32_t pair_epi_bytes() {
+  return KIND == FWD_GATEUP ? 4u * 3u * 4096u : (KIND == BWD_DH ? 4u * 16384u : 4u * 2u * 4096u);
+}
+
+// Writes 32 consecutive columns (values v) of this lane's row into a
+// [32 rows x 64 bf16] box with 128-byte swizzle, at 16-byte chunk j0 .. j0+3.
+__device__ __forceinline__ void stage_row32(uint8_t* box, int lane, int j0, const float (&v)[32]) {
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int off = lane * 128 + (((j0 + jj) ^ (lane & 7)) << 4);
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = v[8 * jj + i];
+    *reinterpret_cast<uint4*>(box + off) = pack8(f);
+  }
+}
+
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float (&v)[32]) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = v[8 * jj + i];
+    p[jj] = pack8(f);
+  }
+}
+
 template <int KIND, int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -907,13 +944,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   constexpr uint32_t TMEM_COLS = 2 * BN;
   constexpr uint32_t IDESC = make_idesc<BN, false, B_MN, 2 * BM>();
   constexpr uint32_t MN_ATOM = 64 * 128;
-  (void)tmC1;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* epi = smem + STAGES * STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + epi_bytes<KIND>());
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + pair_epi_bytes<KIND>());
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, aux[4]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -944,8 +980,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB0)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB1)) : "memory");
-    if constexpr (KIND == BWD_DH)
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC1)) : "memory");
   }
   if (warp == 1) {   // one warp in each CTA of the pair allocates collectively
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -1072,6 +1108,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    // Each warp drains 32 accumulator rows. A slice whose 32 rows all belong to
+    // the tile's expert goes out through shared-memory staging and bulk tensor
+    // stores; a slice that crosses the expert's end is stored row by row, so no
+    // write reaches the next expert's rows.
     const int q = warp & 3;
     const int ew = warp - 2;
     const int r = q * 32 + lane;
@@ -1080,22 +1120,25 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t acc_phase = 0;
     uint32_t aux_phase = 0;
     bool aux_pending = false;
+    int buf = 0;
     for (int t = cid; t < total; t += ncl) {
       const PTile tl = decode_pair<KIND, BN>(t, static_cast<int>(rank), p, s_off, s_mp);
       const bool valid = r < tl.rows;
       const size_t grow = static_cast<size_t>(tl.row0 + r);
+      const int growq = tl.row0 + q * 32;          // first row of this warp's slice
+      const bool full = (tl.rows - q * 32) >= 32;  // every row of the slice is valid
       if constexpr (KIND == BWD_DH) {
-        uint8_t* aux = epi + ew * 16384;
+        uint8_t* aux = epi + ew * 16384;   // boxes: G[c0,+64) G[c0+64,+64) U[c0,+64) U[c0+64,+64)
         const uint32_t aux_addr = smem_u32(aux);
         const uint32_t ab = aux_bar(ew);
-        const int grow0 = tl.row0 + q * 32;
         auto request = [&](int c0) {
           if (lane == 0) {
+            bulk_wait_read_all();          // earlier dG/dU stores from these boxes are done
             mbar_expect_tx(ab, 16384);
-            tma_load_2d(aux_addr, &tmC0, ab, tl.n0 + c0, grow0);
-            tma_load_2d(aux_addr + 4096, &tmC0, ab, tl.n0 + c0 + 64, grow0);
-            tma_load_2d(aux_addr + 8192, &tmC0, ab, p.I + tl.n0 + c0, grow0);
-            tma_load_2d(aux_addr + 12288, &tmC0, ab, p.I + tl.n0 + c0 + 64, grow0);
+            tma_load_2d(aux_addr, &tmC0, ab, tl.n0 + c0, growq);
+            tma_load_2d(aux_addr + 4096, &tmC0, ab, tl.n0 + c0 + 64, growq);
+            tma_load_2d(aux_addr + 8192, &tmC0, ab, p.I + tl.n0 + c0, growq);
+            tma_load_2d(aux_addr + 12288, &tmC0, ab, p.I + tl.n0 + c0 + 64, growq);
           }
           aux_pending = true;
         };
@@ -1127,14 +1170,21 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
               for (int i = 0; i < 8; ++i) u[8 * hh + i] = f[i];
             }
-            if (valid) {
-              float dg[16], du[16];
+            float dg[16], du[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float sg = 1.f / (1.f + expf(-g[i]));
-                dg[i] = dh[i] * u[i] * sg * (1.f + g[i] * (1.f - sg));
-                du[i] = dh[i] * g[i] * sg;
+            for (int i = 0; i < 16; ++i) {
+              const float sg = __fdividef(1.f, 1.f + __expf(-g[i]));
+              dg[i] = dh[i] * u[i] * sg * (1.f + g[i] * (1.f - sg));
+              du[i] = dh[i] * g[i] * sg;
+            }
+            if (full) {   // in place over G and U: this lane's own row chunks
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int off = lane * 128 + (((j0 + hh) ^ (lane & 7)) << 4);
+                *reinterpret_cast<uint4*>(aux + box * 4096 + off) = pack8(&dg[8 * hh]);
+                *reinterpret_cast<uint4*>(aux + 8192 + box * 4096 + off) = pack8(&du[8 * hh]);
               }
+            } else if (valid) {
               __nv_bfloat16* orow = p.out + grow * (2 * p.I);
               store16_bf16(orow + tl.n0 + c0 + c, dg);
               store16_bf16(orow + p.I + tl.n0 + c0 + c, du);
@@ -1142,6 +1192,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           fence_proxy_async();
           __syncwarp();
+          if (full && lane == 0) {
+            tma_store_2d(&tmC1, aux_addr, tl.n0 + c0, growq);
+            tma_store_2d(&tmC1, aux_addr + 4096, tl.n0 + c0 + 64, growq);
+            tma_store_2d(&tmC1, aux_addr + 8192, p.I + tl.n0 + c0, growq);
+            tma_store_2d(&tmC1, aux_addr + 12288, p.I + tl.n0 + c0 + 64, growq);
+            bulk_commit();
+          }
         }
         if (!ok) break;
       } else {
@@ -1150,27 +1207,69 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
         if constexpr (KIND == FWD_GATEUP) {
           constexpr int HALF = BN / 2;
-          for (int c = 0; c < HALF; c += 16) {
-            float g[16], u[16], h[16];
-            tmem_ld16(tacc + c, g);
-            tmem_ld16(tacc + HALF + c, u);
-            tmem_wait_ld();
-            if (valid) {
+          uint8_t* stH = epi + ew * 12288;
+          uint8_t* stG = stH + 4096;
+          uint8_t* stU = stH + 8192;
+          for (int c64 = 0; c64 < HALF; c64 += 64) {
+            if (full) {
+              if (lane == 0) bulk_wait_read_all();   // the previous boxes have been read
+              __syncwarp();
+            }
+            for (int sub = 0; sub < 64; sub += 32) {
+              float g[32], u[32], h[32];
+              tmem_ld32(tacc + c64 + sub, g);
+              tmem_ld32(tacc + HALF + c64 + sub, u);
+              tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) h[i] = silu_f(g[i]) * u[i];
-              store16_bf16(p.out + grow * p.I + tl.n0 + c, h);
-              if (p.out2) {
-                store16_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c, g);
-                store16_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c, u);
+              for (int i = 0; i < 32; ++i) h[i] = silu_f(g[i]) * u[i];
+              if (full) {
+                stage_row32(stH, lane, sub >> 3, h);
+                stage_row32(stG, lane, sub >> 3, g);
+                stage_row32(stU, lane, sub >> 3, u);
+              } else if (valid) {
+                store32_bf16(p.out + grow * p.I + tl.n0 + c64 + sub, h);
+                if (p.out2) {
+                  store32_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c64 + sub, g);
+                  store32_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c64 + sub, u);
+                }
+              }
+            }
+            if (full) {
+              fence_proxy_async();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmC0, smem_u32(stH), tl.n0 + c64, growq);
+                if (p.out2) {
+                  tma_store_2d(&tmC1, smem_u32(stG), tl.n0 + c64, growq);
+                  tma_store_2d(&tmC1, smem_u32(stU), p.I + tl.n0 + c64, growq);
+                }
+                bulk_commit();
               }
             }
           }
-        } else {
-          for (int c = 0; c < BN; c += 16) {
-            float v[16];
-            tmem_ld16(tacc + c, v);
-            tmem_wait_ld();
-            if (valid) store16_bf16(p.out + grow * p.ld_out + tl.n0 + c, v);
+        } else {  // FWD_DOWN, BWD_DX: one bf16 output, two staging boxes in turn
+          for (int c64 = 0; c64 < BN; c64 += 64) {
+            uint8_t* st = epi + ew * 8192 + buf * 4096;
+            if (full) {
+              if (lane == 0) bulk_wait_read_1();   // the store that used this box is done
+              __syncwarp();
+            }
+            for (int sub = 0; sub < 64; sub += 32) {
+              float v[32];
+              tmem_ld32(tacc + c64 + sub, v);
+              tmem_wait_ld();
+              if (full) stage_row32(st, lane, sub >> 3, v);
+              else if (valid) store32_bf16(p.out + grow * p.ld_out + tl.n0 + c64 + sub, v);
+            }
+            if (full) {
+              fence_proxy_async();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmC0, smem_u32(st), tl.n0 + c64, growq);
+                bulk_commit();
+              }
+              buf ^= 1;
+            }
           }
         }
       }
@@ -1186,8 +1285,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         while (!mbar_try(aux_bar(ew), aux_phase) && globaltimer() - t0 < kTimeoutNs) {
         }
       }
-      __syncwarp();
     }
+    if (lane == 0) bulk_wait_all();   // bulk stores complete before shared memory is released
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1267,7 +1367,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
 
 template <int KIND, int BN, int STAGES>
 size_t pair_smem_bytes(int E) {
-  return 1024 + STAGES * (BM * BK * 2 + (BN / 2) * BK * 2) + epi_bytes<KIND>() +
+  return 1024 + STAGES * (BM * BK * 2 + (BN / 2) * BK * 2) + pair_epi_bytes<KIND>() +
          8 * (2 * STAGES + 9) + 16 + sizeof(int) * 2 * (E + 1) + 16;
 }
 
@@ -1324,7 +1424,8 @@ int launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& 
 // Pair pipeline depth: 32 KB stages (64 KB of [G|U] prefetch buffers for dh).
 template <int KIND, int BN>
 constexpr int pair_stages() {
-  return KIND == BWD_DH ? (BN == 256 ? 4 : 5) : (BN == 256 ? 6 : 8);
+  return KIND == BWD_DH ? (BN == 256 ? 4 : 5)
+                        : KIND == FWD_GATEUP ? (BN == 256 ? 4 : 6) : (BN == 256 ? 5 : 7);
 }
 
 template <int KIND>
@@ -1341,7 +1442,10 @@ int launch_pair_bn(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CU
 // The N width a pair tile uses for an output of n columns (n % 128 == 0).
 inline int pair_bn(int n) { return (n % 256 == 0 && MOE_PAIR_BN_MAX >= 256) ? 256 : 128; }
 
-static_assert(1024 + 6 * (16384 + 16384) + 8 * 21 + 32 + 8 * 1025 <= 232448, "pair smem");
+static_assert(1024 + 5 * (16384 + 16384) + 32768 + 8 * 19 + 32 + 8 * 1025 <= 232448, "pair smem");
+static_assert(1024 + 4 * (16384 + 16384) + 49152 + 8 * 17 + 32 + 8 * 1025 <= 232448, "pair gu smem");
+static_assert(1024 + 7 * (16384 + 8192) + 32768 + 8 * 23 + 32 + 8 * 1025 <= 232448, "pair 128 smem");
+static_assert(1024 + 6 * (16384 + 8192) + 49152 + 8 * 21 + 32 + 8 * 1025 <= 232448, "pair gu 128 smem");
 static_assert(1024 + 4 * (16384 + 16384) + 65536 + 8 * 17 + 32 + 8 * 1025 <= 232448, "pair dh smem");
 
 // Pipeline depth: as many operand stages as fit next to the kind's epilogue buffers
@@ -1405,10 +1509,13 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
   p.I = I;
   p.status = static_cast<int*>(ws);
   const long long mt_upper = (M + BM - 1) / BM + E;
-  CUtensorMap ta, tb0, tb1;
-  // gate/up projection with the SwiGLU epilogue
+  CUtensorMap ta, tb0, tb1, tc0, tc1;
+  // gate/up projection with the SwiGLU epilogue (H and [G|U] leave through bulk stores)
   if (!make_map(&ta, xp, d, M, 64, BM) || !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, 64) ||
-      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, 64))
+      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, 64) ||
+      !make_map(&tc0, h, I, M, 64, 32) ||
+      !make_map(&tc1, gu ? static_cast<const void*>(gu) : static_cast<const void*>(h),
+                gu ? 2 * static_cast<uint64_t>(I) : I, M, 64, 32))
     return MOE_ERR_CUDA;
   const int bn_gu = (MOE_PAIR_BN_MAX >= 256) ? 256 : 128;   // half gate, half up columns
   p.n_tiles = I / (bn_gu / 2);
@@ -1416,18 +1523,19 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
   p.out = reinterpret_cast<__nv_bfloat16*>(h);
   p.out2 = reinterpret_cast<__nv_bfloat16*>(gu);
   p.ld_out = I;
-  int rc = launch_pair_bn<FWD_GATEUP>(bn_gu, ta, tb0, tb1, ta, ta, p, mt_upper * p.n_tiles, st);
+  int rc = launch_pair_bn<FWD_GATEUP>(bn_gu, ta, tb0, tb1, tc0, tc1, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // down projection
   const int bn = pair_bn(d);
-  if (!make_map(&ta, h, I, M, 64, BM) || !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, 64))
+  if (!make_map(&ta, h, I, M, 64, BM) || !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, 64) ||
+      !make_map(&tc0, y, d, M, 64, 32))
     return MOE_ERR_CUDA;
   p.n_tiles = d / bn;
   p.k_blocks = I / BK;
   p.out = reinterpret_cast<__nv_bfloat16*>(y);
   p.out2 = nullptr;
   p.ld_out = d;
-  return launch_pair_bn<FWD_DOWN>(bn, ta, tb0, tb0, ta, ta, p, mt_upper * p.n_tiles, st);
+  return launch_pair_bn<FWD_DOWN>(bn, ta, tb0, tb0, tc0, tc0, p, mt_upper * p.n_tiles, st);
 }
 
 extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
@@ -1475,27 +1583,29 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   const int bn_h = pair_bn(I);
   if (!make_map(&ta, dy, d, M, 64, BM) ||
       !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h / 2) ||
-      !make_map(&tc0, gu, 2 * static_cast<uint64_t>(I), M, 64, 32))
+      !make_map(&tc0, gu, 2 * static_cast<uint64_t>(I), M, 64, 32) ||
+      !make_map(&tc1, dgu, 2 * static_cast<uint64_t>(I), M, 64, 32))
     return MOE_ERR_CUDA;
   p.n_tiles = I / bn_h;
   p.k_blocks = d / BK;
   p.out = dgu;
   p.aux = reinterpret_cast<const __nv_bfloat16*>(gu);
   p.ld_out = 2 * I;
-  int rc = launch_pair_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc0, p, mt_upper * p.n_tiles, st);
+  int rc = launch_pair_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc1, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // dX = dG Wg^T + dU Wu^T
   const int bn_x = pair_bn(d);
   if (!make_map(&ta, dgu, 2 * static_cast<uint64_t>(I), M, 64, BM) ||
       !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2) ||
-      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2))
+      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2) ||
+      !make_map(&tc0, dxp, d, M, 64, 32))
     return MOE_ERR_CUDA;
   p.n_tiles = d / bn_x;
   p.k_blocks = 2 * I / BK;
   p.out = reinterpret_cast<__nv_bfloat16*>(dxp);
   p.aux = nullptr;
   p.ld_out = d;
-  rc = launch_pair_bn<BWD_DX>(bn_x, ta, tb0, tb1, ta, ta, p, mt_upper * p.n_tiles, st);
+  rc = launch_pair_bn<BWD_DX>(bn_x, ta, tb0, tb1, tc0, tc0, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // [dWg | dWu] = X^T [dG | dU]
   if (!make_map(&ta, xp, d, M, 64, 64) || !make_map(&tb0, dgu, 2 * static_cast<uint64_t>(I), M, 64, 64) ||

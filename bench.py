@@ -239,18 +239,43 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_step(cfg, T_s):
-    """One oracle forward+backward on the first T_s tokens' worth of inputs."""
-    import numpy as np  # noqa: F401
-    from grouped_gemm_moe_gb300 import workloads as W
-    from oracle import moe_oracle as O
-    inp = W.make_inputs(cfg, T=T_s, with_backward=True)
-    np_inp = {k: W.to_f64(v) for k, v in inp.items()}
-    R = cfg.R if T_s % cfg.R == 0 else 1
-    t0 = time.perf_counter()
-    fwd = O.layer_forward(np_inp, cfg.K, R, cfg.renorm)
-    O.layer_backward(np_inp, fwd, np_inp["dout"], cfg.K, cfg.renorm)
-    return time.perf_counter() - t0
+class OracleSample:
+    """The CPU oracle on a bounded token sample of a workload. Inputs are drawn
+    once (full-size expert weights, up to ``t_max`` tokens) and converted to
+    float64 once; a step runs the oracle's forward and backward on the first T
+    tokens, and only that is timed."""
+
+    def __init__(self, cfg, t_max: int = 512):
+        from grouped_gemm_moe_gb300 import workloads as W
+        self.cfg = cfg
+        t_max -= t_max % cfg.R
+        inp = W.make_inputs(cfg, T=t_max, with_backward=True)
+        self.np = {k: W.to_f64(v) for k, v in inp.items()}
+        self.t_max = t_max
+
+    def step(self, T: int) -> float:
+        from oracle import moe_oracle as O
+        cfg = self.cfg
+        inp = dict(self.np)
+        for k in ("logits", "x", "dout"):
+            inp[k] = self.np[k][:T]
+        t0 = time.perf_counter()
+        fwd = O.layer_forward(inp, cfg.K, cfg.R, cfg.renorm)
+        O.layer_backward(inp, fwd, inp["dout"], cfg.K, cfg.renorm)
+        return time.perf_counter() - t0
+
+    def tokens_for(self, seconds: float) -> int:
+        """Token count whose step takes about ``seconds`` (linear fit through two
+        probe sizes: the oracle has a fixed per-step cost of its own)."""
+        R = self.cfg.R
+        a, b = 2 * R, 8 * R
+        self.step(a)                       # first call: page faults of the fp64 gradient arrays
+        ta, tb = self.step(a), self.step(b)
+        per_tok = max((tb - ta) / (b - a), 1e-9)
+        fixed = max(ta - per_tok * a, 0.0)
+        T = int((seconds - fixed) / per_tok) if seconds > fixed else R
+        T = max(R, min(self.t_max, T))
+        return T - T % R
 
 
 def cpu_cores():
@@ -261,14 +286,10 @@ def cpu_cores():
 
 
 def cpu_baseline(cfg, tokens):
-    R = cfg.R
+    smp = OracleSample(cfg)
     if tokens <= 0:
-        # calibrate: aim at roughly 15 s of CPU work
-        t_small = oracle_step(cfg, R * 4)
-        per_tok = t_small / (R * 4)
-        tokens = int(min(2048, max(R * 4, 15.0 / max(per_tok, 1e-6))))
-        tokens -= tokens % R
-    dt = oracle_step(cfg, tokens)
+        tokens = smp.tokens_for(15.0)
+    dt = smp.step(tokens)
     return {"value": tokens / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "sample": f"{tokens} of {cfg.T} tokens of the same workload (full expert weights), "
                       f"fwd+bwd, float64 NumPy, one run of {dt:.2f} s"}
@@ -278,16 +299,12 @@ def run_reference(args, cfg, world, rank):
     if rank != 0:
         return
     from grouped_gemm_moe_gb300 import workloads as W
-    budget = 120.0
-    probe = oracle_step(cfg, cfg.R * 2)
-    per_tok = probe / (cfg.R * 2)
+    smp = OracleSample(cfg)
     n_steps = args.steps + args.warmup
-    tokens = int(max(cfg.R, min(cfg.T, budget / n_steps / max(per_tok, 1e-6))))
-    tokens -= tokens % cfg.R
-    tokens = max(tokens, cfg.R)
+    tokens = smp.tokens_for(max(90.0 / n_steps, 0.2))
     for _ in range(args.warmup):
-        oracle_step(cfg, tokens)
-    times = [oracle_step(cfg, tokens) for _ in range(args.steps)]
+        smp.step(tokens)
+    times = [smp.step(tokens) for _ in range(args.steps)]
     ms = statistics.mean(times) * 1e3
     value = tokens / (ms / 1e3)
     line = {
@@ -298,7 +315,8 @@ def run_reference(args, cfg, world, rank):
         "config": {"workload": f"{cfg.name}: {W.describe(cfg)}, fwd+bwd",
                    "sample_tokens_per_step": tokens},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"{tokens} of {cfg.T} tokens per step, float64 NumPy oracle"},
+                         "sample": f"{tokens} of {cfg.T} tokens per step (full expert weights), "
+                                   f"float64 NumPy oracle"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -15,6 +15,8 @@
 // map one thread to one 16-byte vector of an output row, so a warp touches 512
 // contiguous bytes; each thread of the reductions issues its K independent
 // gathered loads before it accumulates (fp32, slot order, no atomics).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -59,6 +61,83 @@ dispatch_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm, i
       }
     }
   }
+}
+
+// xp[p] = x[perm[p] / K] on the bulk-copy engine: one thread per CTA moves
+// whole rows (contiguous, 16-byte multiples) global -> shared -> global through
+// a ring of kBulkSlots row buffers, loads running kBulkLag rows ahead of the
+// stores. Every wait is bounded; a wait that runs out ends the CTA's loop.
+constexpr int kBulkSlots = 8;
+constexpr int kBulkLag = 4;
+
+__device__ __forceinline__ bool bulk_bar_wait(uint32_t bar, uint32_t parity) {
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 1000000000ull) return false;
+  }
+}
+
+__global__ void __launch_bounds__(32)
+dispatch_bulk_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ perm, int K,
+                     int row_bytes, long long rows, uint8_t* __restrict__ xp) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t bars[kBulkSlots];
+  if (threadIdx.x != 0) return;
+  const uint32_t ring_addr = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+  const uint32_t bar_addr = static_cast<uint32_t>(__cvta_generic_to_shared(bars));
+  for (int s = 0; s < kBulkSlots; ++s)
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_addr + 8 * s) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const long long first = blockIdx.x, step = gridDim.x;
+  const long long n = (rows > first) ? (rows - first + step - 1) / step : 0;
+  long long loaded = 0, stored = 0;   // rows whose load was issued / whose store was issued
+  for (long long i = 0; i < n + kBulkLag; ++i) {
+    if (i < n) {   // load row i into slot i % kBulkSlots
+      const int slot = static_cast<int>(i % kBulkSlots);
+      if (i >= kBulkSlots)   // the store of row i - kBulkSlots has read this slot
+        asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kBulkSlots - kBulkLag - 1) : "memory");
+      const long long p = first + i * step;
+      const long long t = __ldg(perm + p) / K;
+      const uint32_t bar = bar_addr + 8 * slot;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                   "r"(row_bytes)
+                   : "memory");
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+              "r"(ring_addr + slot * row_bytes),
+          "l"(x + t * row_bytes), "r"(row_bytes), "r"(bar)
+          : "memory");
+      loaded = i + 1;
+    }
+    const long long j = i - kBulkLag;
+    if (j >= 0 && j < n) {   // store row j once it has landed
+      const int slot = static_cast<int>(j % kBulkSlots);
+      if (!bulk_bar_wait(bar_addr + 8 * slot, static_cast<uint32_t>((j / kBulkSlots) & 1))) break;
+      const long long p = first + j * step;
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                       xp + p * row_bytes),
+                   "r"(ring_addr + slot * row_bytes), "r"(row_bytes)
+                   : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      stored = j + 1;
+    }
+  }
+  // loads that were issued but never stored (only after a wait ran out) must land first
+  for (long long r = stored; r < loaded; ++r)
+    bulk_bar_wait(bar_addr + 8 * static_cast<int>(r % kBulkSlots),
+                  static_cast<uint32_t>((r / kBulkSlots) & 1));
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // out[t] = bf16( sum_j w[t,j] * rows[inv_perm[t*K+j]] + extra[t] ); w == nullptr means 1.
@@ -189,12 +268,34 @@ extern "C" int moe_dispatch(const moe_bf16* x, int T, int d, int K, const int32_
   if (T == 0) return MOE_OK;
   if (!x || !perm || !xp) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(perm) || !aligned16(xp)) return MOE_ERR_MISALIGNED;
-  const int nv = d / 8;
   const long long rows = static_cast<long long>(T) * K;
+  const int row_bytes = d * 2;
+  const size_t ring = static_cast<size_t>(kBulkSlots) * row_bytes;
+  cudaStream_t st = as_stream(stream);
+  if (ring <= 96 * 1024) {
+    static thread_local int configured = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured != dev) {
+      cudaFuncSetAttribute(dispatch_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           96 * 1024);
+      configured = dev;
+    }
+    // enough CTAs that each SM keeps several rings busy
+    const int per_sm = static_cast<int>(std::min<size_t>(8, (200 * 1024) / (ring + 1024)));
+    long long grid = static_cast<long long>(num_sms()) * (per_sm > 0 ? per_sm : 1);
+    if (grid > rows) grid = rows;
+    ProfScope prof("dispatch", st);
+    dispatch_bulk_kernel<<<static_cast<int>(grid), 32, ring, st>>>(
+        reinterpret_cast<const uint8_t*>(x), perm, K, row_bytes, rows,
+        reinterpret_cast<uint8_t*>(xp));
+    return check_launch();
+  }
+  const int nv = d / 8;
   const int grid = grid_for(rows, kThreads / 32);
-  ProfScope prof("dispatch", as_stream(stream));
-  dispatch_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(
-      reinterpret_cast<const uint4*>(x), perm, K, nv, rows, reinterpret_cast<uint4*>(xp));
+  ProfScope prof("dispatch", st);
+  dispatch_kernel<<<grid, kThreads, 0, st>>>(reinterpret_cast<const uint4*>(x), perm, K, nv, rows,
+                                             reinterpret_cast<uint4*>(xp));
   return check_launch();
 }
 

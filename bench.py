@@ -150,20 +150,27 @@ def peaks():
 
 # ------------------------------------------------------------------ work model
 def kernel_work(name: str, cfg, shared: bool):
-    """Algorithmic work of one launch: ("tensor", flops) or ("hbm", bytes)."""
+    """Algorithmic work of one launch: (flops, bytes). Bytes count each input
+    read once and each output written once (bf16 activations and weights,
+    fp32 weight gradients, int32 indices), i.e. no re-reads."""
     T, d, E, K, I = cfg.T, cfg.d, cfg.E, cfg.K, cfg.I
     TK = T * K
     if shared:
-        M, Ie = T, cfg.shared_I
+        M, Ie, Ee = T, cfg.shared_I, 1
     else:
-        M, Ie = TK, I
+        M, Ie, Ee = TK, I, E
+    w1 = 2 * Ee * d * Ie * 2          # W_gate + W_up, bf16
+    wd = Ee * Ie * d * 2              # W_down, bf16
     gemm = {
-        "gemm_gate_up": 4 * M * d * Ie, "gemm_down": 2 * M * Ie * d, "gemm_dh": 2 * M * d * Ie,
-        "gemm_dx": 4 * M * d * Ie, "gemm_wgrad_gate_up": 4 * M * d * Ie,
-        "gemm_wgrad_down": 2 * M * Ie * d,
+        "gemm_gate_up": (4 * M * d * Ie, M * d * 2 + w1 + M * Ie * 2 + M * 2 * Ie * 2),
+        "gemm_down": (2 * M * Ie * d, M * Ie * 2 + wd + M * d * 2),
+        "gemm_dh": (2 * M * d * Ie, M * d * 2 + wd + 2 * (M * 2 * Ie * 2)),
+        "gemm_dx": (4 * M * d * Ie, M * 2 * Ie * 2 + w1 + M * d * 2),
+        "gemm_wgrad_gate_up": (4 * M * d * Ie, M * d * 2 + M * 2 * Ie * 2 + 2 * Ee * d * Ie * 4),
+        "gemm_wgrad_down": (2 * M * Ie * d, M * Ie * 2 + M * d * 2 + Ee * Ie * d * 4),
     }
     if name in gemm:
-        return "tensor", gemm[name]
+        return gemm[name]
     hbm = {
         "route_topk": T * (4 * E + 8 * K),
         "route_topk_backward": T * (12 * K + 4 * E),
@@ -173,7 +180,22 @@ def kernel_work(name: str, cfg, shared: bool):
         "combine_backward": T * (2 * d + 4 * d * K + 12 * K),
         "dispatch_backward": T * (2 * d * K + 4 * K + 2 * d + (2 * d if cfg.shared_I else 0)),
     }
-    return "hbm", hbm.get(name, 0)
+    return 0, hbm.get(name, 0)
+
+
+def roofline_of(flops: float, nbytes: float, ms: float, pk) -> dict:
+    """The bound of one launch is whichever of its flops at the bf16 tensor peak
+    or its bytes at HBM bandwidth takes longer; achieved is in that unit."""
+    t_tc = flops / (pk["bf16_tflops_sustained"] * 1e12)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    if t_tc >= t_hbm and flops > 0:
+        ach = flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"],
+                "roofline_ms": t_tc * 1e3}
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / pk["hbm_gbs"], "roofline_ms": t_hbm * 1e3}
 
 
 def label_records(records, steps):
@@ -410,35 +432,31 @@ def main():
     tot = sum(c["total_ms"] for c in per.values()) or 1.0
     kernels = {}
     for k, c in per.items():
-        kind, work = kernel_work(c["name"], cfg, c["shared"])
+        fl, nb = kernel_work(c["name"], cfg, c["shared"])
         avg = c["total_ms"] / c["launches"]
-        if kind == "tensor":
-            ach, unit, peak = work / (avg / 1e3) / 1e12, "TFLOP/s", pk["bf16_tflops_sustained"]
-        else:
-            ach, unit, peak = work / (avg / 1e3) / 1e9, "GB/s", pk["hbm_gbs"]
+        rf = roofline_of(fl, nb, avg, pk)
         kernels[k] = {"launches": c["launches"], "avg_ms": round(avg, 5),
-                      "share": round(c["total_ms"] / tot, 4), "achieved": round(ach, 1),
-                      "unit": unit, "frac": round(ach / peak, 4)}
+                      "share": round(c["total_ms"] / tot, 4), "bound": rf["bound"],
+                      "achieved": round(rf["achieved"], 1), "unit": rf["unit"],
+                      "frac": round(rf["frac"], 4), "roofline_ms": round(rf["roofline_ms"], 5)}
     dom = max(per, key=lambda k: per[k]["total_ms"])
-    dkind, dwork = kernel_work(per[dom]["name"], cfg, per[dom]["shared"])
+    dfl, dnb = kernel_work(per[dom]["name"], cfg, per[dom]["shared"])
     davg = per[dom]["total_ms"] / per[dom]["launches"]
-    if dkind == "tensor":
-        achieved = dwork / (davg / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved,
-                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops_sustained"],
-                "frac_of_burst_peak": achieved / pk["bf16_tflops"],
-                "peak_source": f"{pk['source']} bf16 sustained", "traffic": None,
-                "work_per_launch": f"{dwork:.4g} flop"}
-    else:
-        achieved = dwork / (davg / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                "peak_source": f"{pk['source']} HBM copy", "traffic": None,
-                "work_per_launch": f"{dwork:.4g} B"}
-    flops_step = sum(kernel_work(c["name"], cfg, c["shared"])[1] * c["launches"]
-                     for c in per.values()
-                     if kernel_work(c["name"], cfg, c["shared"])[0] == "tensor") / args.steps
+    rf = roofline_of(dfl, dnb, davg, pk)
+    roof = {"bound": rf["bound"], "kernel": dom, "achieved": rf["achieved"], "peak": rf["peak"],
+            "unit": rf["unit"], "frac": rf["frac"],
+            "peak_source": pk["source"] + (" bf16 sustained" if rf["bound"] == "tensor"
+                                           else " HBM copy (read+write)"),
+            "traffic": None,
+            "work_per_launch": {"flop": dfl, "bytes": dnb},
+            "avg_launch_ms": davg}
+    flops_step = sum(kernel_work(c["name"], cfg, c["shared"])[0] * c["launches"]
+                     for c in per.values()) / args.steps
+    bytes_step = sum(kernel_work(c["name"], cfg, c["shared"])[1] * c["launches"]
+                     for c in per.values()) / args.steps
+    layer_roof_ms = max(flops_step / (pk["bf16_tflops_sustained"] * 1e12),
+                        bytes_step / (pk["hbm_gbs"] * 1e9)) * 1e3
+    sum_roof_ms = sum(v["roofline_ms"] * v["launches"] for v in kernels.values()) / args.steps
     clocks = sampler.stop() if sampler else None
 
     # end to end through the layer API with pinned host buffers
@@ -477,7 +495,11 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "flushed by a 256 MiB write before every timed step (outside its events)",
                        "step_tflop": flops_step / 1e12,
-                       "layer_tflops_achieved": flops_step / (ms / 1e3) / 1e12},
+                       "step_gbytes_algorithmic": bytes_step / 1e9,
+                       "layer_tflops_achieved": flops_step / (ms / 1e3) / 1e12,
+                       "layer_roofline_ms": layer_roof_ms,
+                       "layer_frac_of_roofline": layer_roof_ms / ms,
+                       "sum_of_kernel_rooflines_ms": sum_roof_ms},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": len(records), "clocks": clocks,
             "step_ms_min_max": [min(step_ms), max(step_ms)],

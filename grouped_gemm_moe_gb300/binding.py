@@ -55,6 +55,7 @@ SIGNATURES = {
     "moe_combine_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_dispatch_backward": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_read_device_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
+    "moe_debug_wait_timeout": (_I, [_P, _I, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_last_cuda_error": (_I, []),
     "moe_version": (_I, []),
@@ -356,6 +357,13 @@ def moe_profile_stop():
         _check("moe_profile_record", lib.moe_profile_record(i, ctypes.byref(name), ctypes.byref(ms)))
         out.append((name.value.decode(), float(ms.value)))
     return out
+
+
+def moe_debug_wait_timeout(ws: torch.Tensor, timeout_us: int):
+    """Runs the GEMM kernels' bounded wait on a barrier nothing completes; the
+    status word of ``ws`` then reads MOE_ERR_DEVICE_TIMEOUT."""
+    _check("moe_debug_wait_timeout", load().moe_debug_wait_timeout(_ptr(ws), int(timeout_us),
+                                                                    _stream(ws.device)))
 
 
 def moe_read_device_status(ws: torch.Tensor) -> int:

@@ -110,13 +110,14 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Returns false if this CTA is aborting (another role timed out) or the wait
 // itself ran past kTimeoutNs (then it raises the abort flag and the status).
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                            volatile int* abort_flag, int* status) {
+                                            volatile int* abort_flag, int* status,
+                                            uint64_t timeout_ns = kTimeoutNs) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
+      if (globaltimer() - t0 > timeout_ns) {
         *abort_flag = 1;
         report_status(status, MOE_ERR_DEVICE_TIMEOUT);
         return false;
@@ -1301,6 +1302,22 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
+// ----------------------------------------------------------------- diagnostics
+// One thread waits, through the GEMMs' bounded wait, on an mbarrier that nothing
+// arrives on; the wait runs out after timeout_ns and records the timeout.
+__global__ void wait_timeout_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_slow(b, 0, &abort_flag, status, timeout_ns);
+}
+
 // ----------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1631,4 +1648,12 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   p.outf1 = nullptr;
   return launch_bn<WGRAD_D>(bn_d, ta, tb0, tb0, tc0, tc0, p,
                             static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
+}
+
+extern "C" int moe_debug_wait_timeout(void* ws, int timeout_us, void* stream) {
+  using namespace moe;
+  if (!ws || !aligned16(ws) || timeout_us < 1 || timeout_us > 10000000) return MOE_ERR_INVALID_ARG;
+  gemm::wait_timeout_kernel<<<1, 32, 0, as_stream(stream)>>>(
+      static_cast<int*>(ws), static_cast<uint64_t>(timeout_us) * 1000ull);
+  return check_launch();
 }

@@ -258,6 +258,14 @@ int moe_profile_start(int capacity);
 int moe_profile_stop(void);
 int moe_profile_record(int i, const char** name, float* ms);
 
+/* Diagnostics: runs the bounded device-side wait that every mbarrier wait of
+ * the GEMM kernels uses, on an mbarrier that nothing completes, with a limit of
+ * timeout_us microseconds (1 .. 10,000,000). When the limit runs out the
+ * kernel writes MOE_ERR_DEVICE_TIMEOUT into the status word of `ws` (any
+ * workspace of at least 256 bytes) and returns normally, so the context stays
+ * usable; read the result with moe_read_device_status. */
+int moe_debug_wait_timeout(void* ws, int timeout_us, void* stream);
+
 /* Reads the workspace's device status word after synchronising `stream`,
  * stores it in *host_status (a moe_status value, 0 if no kernel reported an
  * error) and clears it. The only call in this library that synchronises. */

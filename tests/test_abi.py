@@ -100,6 +100,13 @@ def test_argument_validation_rows_and_gemm(lib):
              FAKE, FAKE, 256, None) == B.MOE_ERR_WORKSPACE
 
 
+def test_debug_wait_argument_checks(lib):
+    assert lib.moe_debug_wait_timeout(None, 1000, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_wait_timeout(FAKE, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_wait_timeout(FAKE, 20000000, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_wait_timeout(MIS, 1000, None) == B.MOE_ERR_INVALID_ARG
+
+
 def test_workspace_sizes(lib):
     hdr = B.WORKSPACE_HEADER
     assert B.workspace_size(B.MOE_OP_GROUPED_FFN, 8192, 128, 8, 1, 2048, 768) == hdr

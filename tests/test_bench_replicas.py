@@ -52,5 +52,12 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.aggregate_value(2.0, 1000, 1) == 500000.0
-    assert bench.kernel_work("gemm_gate_up", __import__(
-        "grouped_gemm_moe_gb300.workloads", fromlist=["x"]).CONFIGS["qwen3"], False)[0] == "tensor"
+    from grouped_gemm_moe_gb300 import workloads as W
+    cfg = W.CONFIGS["qwen3"]
+    fl, nb = bench.kernel_work("gemm_gate_up", cfg, False)
+    assert fl == 4 * cfg.T * cfg.K * cfg.d * cfg.I
+    # weights read once: 2 * E * d * I bf16 values are part of the bytes
+    assert nb > 2 * cfg.E * cfg.d * cfg.I * 2
+    pk = {"hbm_gbs": 6800.0, "bf16_tflops_sustained": 1700.0, "bf16_tflops": 1900.0}
+    assert bench.roofline_of(fl, 1.0, 1.0, pk)["bound"] == "tensor"
+    assert bench.roofline_of(1.0, nb, 1.0, pk)["bound"] == "hbm"

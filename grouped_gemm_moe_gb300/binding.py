@@ -47,6 +47,8 @@ SIGNATURES = {
     "moe_build_permutation": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_build_permutation_static": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_ep_layout": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_build_permutation_ep": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                      _SZ, _P]),
     "moe_dispatch": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_ffn": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
@@ -236,6 +238,36 @@ def moe_ep_layout(topk_idx: torch.Tensor, E: int, R: int, host_splits: Optional[
         _ptr(topk_idx), T, E, K, R, _ptr(splits), _ptr(send), _ptr(a2a), _ptr(reg),
         _ptr(host_splits), _ptr(ws), ws.numel(), _stream(dev)))
     return splits, send, a2a, reg, host_splits
+
+
+def moe_build_permutation_ep(topk_idx: torch.Tensor, E: int, R: int,
+                             host_splits: Optional[torch.Tensor] = None,
+                             ws: Optional[torch.Tensor] = None, out=None):
+    """Both moe_build_permutation and moe_ep_layout from one pass. Returns
+    (counts, offsets, perm, inv_perm, ep_splits, send_index, a2a_index, regroup_index,
+    host_splits); ``host_splits=False`` skips the device-to-host copy."""
+    _need(topk_idx, torch.int32, 2, "topk_idx")
+    T, K = topk_idx.shape
+    dev = topk_idx.device
+    n = R * E + R * R
+    if host_splits is None:
+        host_splits = torch.empty(n, dtype=torch.int32, pin_memory=True)
+    elif host_splits is False:
+        host_splits = None
+    nbytes = workspace_size(MOE_OP_EP_LAYOUT, T, E, K, R)
+    if nbytes == 0:
+        raise ValueError("R must divide E and T")
+    if ws is None:
+        ws = new_workspace(nbytes, dev)
+    if out is None:
+        e = lambda *s: torch.empty(*s, dtype=torch.int32, device=dev)  # noqa: E731
+        out = (e(E), e(E + 1), e(T * K), e(T * K), e(n), e(T * K), e(T * K), e(T * K))
+    counts, offsets, perm, inv, splits, send, a2a, reg = out
+    _check("moe_build_permutation_ep", load().moe_build_permutation_ep(
+        _ptr(topk_idx), T, E, K, R, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+        _ptr(splits), _ptr(send), _ptr(a2a), _ptr(reg), _ptr(host_splits), _ptr(ws), ws.numel(),
+        _stream(dev)))
+    return counts, offsets, perm, inv, splits, send, a2a, reg, host_splits
 
 
 def moe_dispatch(x: torch.Tensor, perm: torch.Tensor, K: int, out: Optional[torch.Tensor] = None):

@@ -137,6 +137,7 @@ scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
   for (int i = threadIdx.x; i < kWarps * E; i += kThreads) wh[i] = 0;
   for (int e = threadIdx.x; e < E; e += kThreads) {
     int tot = 0, b_all = 0, b_s = 0, c_s = 0, c_sb = 0;
+#pragma unroll 16
     for (int k = 0; k < NC; ++k) {
       const int h = __ldg(hist + static_cast<size_t>(k) * E + e);
       tot += h;
@@ -162,14 +163,13 @@ scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
   warp_count(idx, wstart, end, wh + w * E);
   __syncthreads();
 
-  if (!EP) {
-    if (c == 0) {
-      for (int e = threadIdx.x; e <= E; e += kThreads) {
-        po.offsets[e] = off[e];
-        if (e < E) po.counts[e] = off[e + 1] - off[e];
-      }
+  if (c == 0 && (!EP || po.counts)) {   // counts and offsets (the EP pass writes them on request)
+    for (int e = threadIdx.x; e <= E; e += kThreads) {
+      po.offsets[e] = off[e];
+      if (e < E) po.counts[e] = off[e + 1] - off[e];
     }
-  } else if (c % g.cps == 0) {
+  }
+  if (EP && c % g.cps == 0) {
     for (int e = threadIdx.x; e < E; e += kThreads) eo.splits[static_cast<size_t>(s) * E + e] = craw[e];
     for (int d = threadIdx.x; d < eo.R; d += kThreads)
       eo.splits[static_cast<size_t>(eo.R) * E + static_cast<size_t>(s) * eo.R + d] =
@@ -214,6 +214,10 @@ scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
       eo.send_index[q] = static_cast<int32_t>(a);
       eo.a2a_index[r] = q;
       eo.regroup_index[p] = r;
+      if (po.perm) {
+        po.perm[p] = static_cast<int32_t>(a);
+        po.inv_perm[a] = p;
+      }
     }
   }
 }
@@ -314,6 +318,46 @@ extern "C" int moe_ep_layout(const int32_t* topk_idx, int T, int E, int K, int R
     if (!ws || ws_bytes < permutation_workspace(TK, E, R) || !aligned16(ws))
       return MOE_ERR_WORKSPACE;
     PermOut po{};
+    EpOut eo{ep_splits, send_index, a2a_index, regroup_index, R, E / R};
+    const int rc = launch_counting_sort(true, topk_idx, TK, E, R, po, eo, ws, ws_bytes, st);
+    if (rc) return rc;
+  }
+  if (host_splits) {
+    const cudaError_t e = cudaMemcpyAsync(host_splits, ep_splits, split_bytes,
+                                          cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
+  }
+  return check_launch();
+}
+
+extern "C" int moe_build_permutation_ep(const int32_t* topk_idx, int T, int E, int K, int R,
+                                        int32_t* counts, int32_t* offsets, int32_t* perm,
+                                        int32_t* inv_perm, int32_t* ep_splits,
+                                        int32_t* send_index, int32_t* a2a_index,
+                                        int32_t* regroup_index, int32_t* host_splits, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  using namespace moe;
+  if (T < 0 || E < 1 || E > 1024 || K < 1 || K > E || R < 1 || R > 64 || E % R || T % R)
+    return MOE_ERR_INVALID_ARG;
+  const long long TK = static_cast<long long>(T) * K;
+  if (TK >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || !ep_splits) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  const size_t split_bytes = sizeof(int32_t) * (static_cast<size_t>(R) * E + R * R);
+  if (TK == 0) {
+    cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st);
+    cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), st);
+    cudaMemsetAsync(ep_splits, 0, split_bytes, st);
+  } else {
+    if (!topk_idx || !perm || !inv_perm || !send_index || !a2a_index || !regroup_index)
+      return MOE_ERR_INVALID_ARG;
+    if (!aligned16(topk_idx) || !aligned16(counts) || !aligned16(offsets) || !aligned16(perm) ||
+        !aligned16(inv_perm) || !aligned16(ep_splits) || !aligned16(send_index) ||
+        !aligned16(a2a_index) || !aligned16(regroup_index))
+      return MOE_ERR_MISALIGNED;
+    if (!ws || ws_bytes < permutation_workspace(TK, E, R) || !aligned16(ws))
+      return MOE_ERR_WORKSPACE;
+    PermOut po{counts, offsets, perm, inv_perm};
     EpOut eo{ep_splits, send_index, a2a_index, regroup_index, R, E / R};
     const int rc = launch_counting_sort(true, topk_idx, TK, E, R, po, eo, ws, ws_bytes, st);
     if (rc) return rc;

@@ -2,11 +2,11 @@
 // "Expert Parallel (EP)" -> "Producing assignments": scores [T,E] against all
 // experts, top-K selection of expert_IDs and router_weights [T,K]).
 //
-// One warp per token. Lane l holds experts l, l+32, l+64, ... in registers.
-// Each of the K rounds is a butterfly arg-max over (logit, -id) across the
-// warp: the larger logit wins, equal logits go to the lower id (a float
-// comparison, so -0.0 and +0.0 tie). The winner's owner lane marks it taken.
-// The softmax max is the round-0 winner; its denominator is a warp sum.
+// Forward: a group of G lanes per token (see route_topk_kernel). Each of the K
+// rounds is a butterfly arg-max over (logit, -id) across the group: the larger
+// logit wins, equal logits go to the lower id (a float comparison, so -0.0 and
+// +0.0 tie). The softmax max is the round-0 winner; its denominators are group
+// sums. Backward: one warp per token.
 #include "common.cuh"
 
 namespace moe {
@@ -14,24 +14,29 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
-template <int V>  // V = ceil(E / 32) values per lane
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+// One group of G lanes per token (G in 4..32, a power of two); lane l of a
+// group holds experts l, l+G, l+2G, ... (V values). Each of the K rounds is a
+// local best over the lane's untaken values and a butterfly over the group on
+// (logit, -id). The winner's owner marks it taken and remembers its slot; the
+// weights are written per taken value at the end.
+template <int G, int V>
+__global__ void __launch_bounds__(256)
 route_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renorm,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* row = logits + static_cast<size_t>(t) * E;
+  const int gl = threadIdx.x & (G - 1);
+  const long long tok = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / G;
+  const bool active = tok < T;
+  const float* row = logits + (active ? tok : 0) * static_cast<long long>(E);
   float v[V];
-  unsigned taken = 0;  // bit i: value i of this lane already selected
+  int slot[V];
+  unsigned taken = 0;  // bit i: value i of this lane is selected (or padding)
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int e = lane + 32 * i;
+    const int e = gl + G * i;
     v[i] = (e < E) ? __ldg(row + e) : 0.f;
-    if (e >= E) taken |= 1u << i;          // padding never competes
+    slot[i] = 0;
+    if (e >= E) taken |= 1u << i;
   }
-  float my_v = 0.f;
-  int my_id = 0;
   float top = 0.f;
   for (int j = 0; j < K; ++j) {
     float bv = -INFINITY;
@@ -39,35 +44,50 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int ren
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       if (taken & (1u << i)) continue;
-      const int e = lane + 32 * i;
-      if (bi == 0x7fffffff || v[i] > bv) { bv = v[i]; bi = e; }   // ids ascend with i
+      if (bi == 0x7fffffff || v[i] > bv) { bv = v[i]; bi = gl + G * i; }   // ids ascend with i
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int o = G / 2; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       const bool better = (oi != 0x7fffffff) &&
                           (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
       if (better) { bv = ov; bi = oi; }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == j) { my_v = bv; my_id = bi; }
+    if ((bi & (G - 1)) == gl) {
+      const int wi = bi / G;
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        if (i == wi) { taken |= 1u << i; slot[i] = j; }
+    }
     if (j == 0) top = bv;
   }
-  // softmax over all E (max = top), then optional renormalisation over the K selected
-  float s_all = 0.f;
+  // softmax over all E (max = top), optionally renormalised over the K selected
+  float s_all = 0.f, s_sel = 0.f;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) s_all += expf(v[i] - top);
+    const int e = gl + G * i;
+    if (e < E) {
+      const float x = expf(v[i] - top);
+      s_all += x;
+      if (taken & (1u << i)) s_sel += x;
+    }
   }
-  s_all = warp_sum(s_all);
-  const float ex = (lane < K) ? expf(my_v - top) : 0.f;
-  const float s_sel = warp_sum(ex);
-  if (lane < K) {
-    const size_t o = static_cast<size_t>(t) * K + lane;
-    topk_idx[o] = my_id;
-    topk_w[o] = renorm ? ex / s_sel : ex / s_all;
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) {
+    s_all += __shfl_xor_sync(0xffffffffu, s_all, o);
+    s_sel += __shfl_xor_sync(0xffffffffu, s_sel, o);
+  }
+  if (!active) return;
+  const float denom = renorm ? s_sel : s_all;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = gl + G * i;
+    if (e < E && (taken & (1u << i))) {
+      const long long o = tok * K + slot[i];
+      topk_idx[o] = e;
+      topk_w[o] = expf(v[i] - top) / denom;
+    }
   }
 }
 
@@ -132,16 +152,15 @@ int dispatch_v(int E, Args... args) {
   return Launcher<32>::run(args...);
 }
 
-template <int V>
-struct FwdLauncher {
-  static int run(const float* logits, int T, int E, int K, int renorm, int32_t* idx, float* w,
-                 cudaStream_t st) {
-    const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    ProfScope prof("route_topk", st);
-    route_topk_kernel<V><<<blocks, kWarpsPerBlock * 32, 0, st>>>(logits, T, E, K, renorm, idx, w);
-    return check_launch();
-  }
-};
+template <int G, int V>
+int launch_fwd(const float* logits, int T, int E, int K, int renorm, int32_t* idx, float* w,
+               cudaStream_t st) {
+  const long long threads = static_cast<long long>(T) * G;
+  const int blocks = static_cast<int>((threads + 255) / 256);
+  ProfScope prof("route_topk", st);
+  route_topk_kernel<G, V><<<blocks, 256, 0, st>>>(logits, T, E, K, renorm, idx, w);
+  return check_launch();
+}
 
 template <int V>
 struct BwdLauncher {
@@ -165,7 +184,13 @@ extern "C" int moe_route_topk(const float* logits, int T, int E, int K, int reno
   if (T == 0) return MOE_OK;
   if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(topk_w)) return MOE_ERR_MISALIGNED;
-  return dispatch_v<FwdLauncher>(E, logits, T, E, K, renorm, topk_idx, topk_w, as_stream(stream));
+  cudaStream_t st = as_stream(stream);
+  // group width: at most 16 logits per lane up to E = 512, 32 beyond
+  if (E <= 64) return launch_fwd<4, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  if (E <= 128) return launch_fwd<8, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  if (E <= 256) return launch_fwd<16, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  if (E <= 512) return launch_fwd<32, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  return launch_fwd<32, 32>(logits, T, E, K, renorm, topk_idx, topk_w, st);
 }
 
 extern "C" int moe_route_topk_backward(const float* logits, const int32_t* topk_idx,

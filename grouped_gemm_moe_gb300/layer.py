@@ -1,7 +1,8 @@
 """One MoE layer's forward and backward on one GPU, as a fixed sequence of
 library calls on the current CUDA stream with every buffer preallocated.
 
-Forward:  moe_route_topk -> moe_build_permutation -> moe_ep_layout (one
+Forward:  moe_route_topk -> moe_build_permutation_ep (the permutation and
+          the simulated expert-parallel layout from one pass, with the one
           device-to-host copy of the splits) -> moe_dispatch ->
           moe_grouped_ffn (routed experts; shared experts as E=1 on x) ->
           moe_combine.
@@ -101,11 +102,10 @@ class MoELayer:
         K, E, R = self.K, self.E, self.R
         self._run("route_topk", B.moe_route_topk, logits, K, self.renorm,
                   out=(self.topk_idx, self.topk_w))
-        self._run("build_permutation", B.moe_build_permutation, self.topk_idx, E, ws=self.ws_perm,
-                  out=(self.counts, self.offsets, self.perm, self.inv_perm))
-        self._run("ep_layout", B.moe_ep_layout, self.topk_idx, E, R,
+        self._run("build_permutation_ep", B.moe_build_permutation_ep, self.topk_idx, E, R,
                   host_splits=self.host_splits if copy_splits else False, ws=self.ws_ep,
-                  out=(self.ep_splits, self.send_index, self.a2a_index, self.regroup_index))
+                  out=(self.counts, self.offsets, self.perm, self.inv_perm, self.ep_splits,
+                       self.send_index, self.a2a_index, self.regroup_index))
         self._run("dispatch", B.moe_dispatch, x, self.perm, K, out=self.xp)
         self._run("grouped_ffn", B.moe_grouped_ffn, self.xp, self.offsets, w["w_gate"], w["w_up"],
                   w["w_down"], ws=self.ws_ffn, out=(self.y, self.h, self.gu))

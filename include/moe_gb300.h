@@ -173,6 +173,16 @@ int moe_ep_layout(const int32_t* topk_idx, int T, int E, int K, int R,
                   int32_t* regroup_index, int32_t* host_splits,
                   void* ws, size_t ws_bytes, void* stream);
 
+/* A2 + A3 + A4 in one pass: the outputs of moe_build_permutation and of
+ * moe_ep_layout (same arguments, layouts, host copy and limits as the two
+ * calls) from one histogram and one scatter over topk_idx, sharing the
+ * workspace of moe_workspace_size(MOE_OP_EP_LAYOUT, T, E, K, R, 0, 0). */
+int moe_build_permutation_ep(const int32_t* topk_idx, int T, int E, int K, int R,
+                             int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                             int32_t* ep_splits, int32_t* send_index, int32_t* a2a_index,
+                             int32_t* regroup_index, int32_t* host_splits,
+                             void* ws, size_t ws_bytes, void* stream);
+
 /* A5. Dispatch gather ([TAS] "Producing assignments": the assignment buffer
  * in expert-major order; [MOD] "Design": the index_select half of the
  * permutation pair): xp[p] = x[perm[p] / K], an exact copy.

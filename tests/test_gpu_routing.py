@@ -148,3 +148,38 @@ def test_ep_layout_shapes(T, E, K, R):
     rng = np.random.default_rng(T * 7 + R)
     ridx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
     _check_ep(ridx, T, E, K, R)
+
+
+def _check_perm_ep(ridx, T, E, K, R):
+    out = B.moe_build_permutation_ep(to_dev(ridx, torch.int32), E, R)
+    torch.cuda.synchronize()
+    counts, offsets, perm, inv, splits, send, a2a, reg, host = out
+    rc, ro = O.expert_counts_offsets(ridx, E)
+    rp, ri = O.stable_permutation(ridx, E)
+    ref = O.ep_layout(ridx, T, E, K, R)
+    assert np.array_equal(i64(counts), rc)
+    assert np.array_equal(i64(offsets), ro)
+    assert np.array_equal(i64(perm), rp)
+    assert np.array_equal(i64(inv), ri)
+    s = i64(splits)
+    assert np.array_equal(s[:R * E].reshape(R, E), ref["ep_counts"])
+    assert np.array_equal(s[R * E:].reshape(R, R), ref["send_splits"])
+    assert np.array_equal(host.numpy().astype(np.int64), s)
+    assert np.array_equal(i64(send), ref["send_index"])
+    assert np.array_equal(i64(a2a), ref["a2a_index"])
+    assert np.array_equal(i64(reg), ref["regroup_index"])
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_build_permutation_ep_workloads(name):
+    """The fused pass gives exactly the outputs of the two separate entry points."""
+    cfg = W.CONFIGS[name]
+    _check_perm_ep(_idx_for(cfg), cfg.T, cfg.E, cfg.K, cfg.R)
+
+
+@pytest.mark.parametrize("T,E,K,R", [(4, 4, 2, 2), (64, 8, 2, 1), (8192, 64, 6, 64),
+                                     (6000, 16, 4, 4), (12, 6, 3, 3), (3, 1024, 1, 1)])
+def test_build_permutation_ep_shapes(T, E, K, R):
+    rng = np.random.default_rng(T * 11 + R)
+    ridx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    _check_perm_ep(ridx, T, E, K, R)

@@ -13,8 +13,11 @@ combine, and the backward of each. Rank 0 prints one JSON line.
   on the launching stream; before every timed step, outside its events, L2 is
   flushed by writing a 256 MiB buffer and then reading another 256 MiB one (so
   no dirty flush lines are left for the step's first kernel to write back).
-* e2e: the same metric through the layer API with pinned host buffers: each
-  step copies logits, x and dout in and the output and input gradient out.
+* e2e: the same metric through the layer API with pinned host buffers
+  (MoELayer.run_from_host over the timed steps): each step copies logits, x
+  and dout in and the output and input gradient out; step i+1's upload and
+  step i's download overlap compute on two copy streams, and the first upload
+  and the last download fall inside the timed region.
 * roofline: the dominant kernel's algorithmic flops (or bytes) per launch over
   its average launch duration, from per-launch events the library records on
   the launching stream during the timed steps.
@@ -474,14 +477,12 @@ def main():
         lh, xh, dh = pin(inp["logits"]), pin(inp["x"]), pin(inp["dout"])
         out_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
         dx_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
-        for _ in range(2):
-            layer.step_from_host(lh, xh, dh, out_h, dx_h)
+        layer.run_from_host([(lh, xh, dh, out_h, dx_h)] * 2)
         torch.cuda.synchronize()
         barrier()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        for _ in range(args.steps):
-            h2d, d2h = layer.step_from_host(lh, xh, dh, out_h, dx_h)
+        h2d, d2h = layer.run_from_host([(lh, xh, dh, out_h, dx_h)] * args.steps)
         e.record(stream)
         torch.cuda.synchronize()
         barrier()

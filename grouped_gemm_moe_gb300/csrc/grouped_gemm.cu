@@ -318,7 +318,10 @@ __host__ __device__ constexpr uint32_t make_idesc() {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
+// silu(g) = g * sigmoid(g) with the fast exponential and reciprocal: a few
+// ulp of fp32, far below the bf16 rounding of H. For g < -87 the denominator
+// overflows and the quotient is 0, the limit of silu.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
 
 __device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const float (&v)[16]) {
   uint4 a, b;
@@ -754,7 +757,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               float dg[16], du[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
-                const float s = 1.f / (1.f + expf(-g[i]));
+                const float s = __fdividef(1.f, 1.f + __expf(-g[i]));
                 dg[i] = dh[i] * u[i] * s * (1.f + g[i] * (1.f - s));
                 du[i] = dh[i] * g[i] * s;
               }
@@ -1302,6 +1305,318 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
+// ----------------------------------------------------------------- CTA-pair weight gradients
+// dW[e] = A_e^T B_e with K = expert e's rows (ragged): A = X (or H) and
+// B = [dG|dU] (or dY), both MN-major boxes of the row-major activations. A pair
+// tile is 256 rows of dW (128 per CTA: the M split of the pair MMA) by 256
+// columns (each CTA loads 128 of them as its half of B), so a CTA moves 32 KB
+// per k-block instead of the 48 KB of a single-CTA 128 x 256 tile.
+//
+// Both CTAs' boxes complete on the leader's full barrier, as in the forward
+// pair kernel. The ragged last k-block of an expert is handled by the leader's
+// MMA warp alone: it issues only the K16 steps that hold valid rows and zeroes,
+// in both CTAs' A (the follower's through distributed shared memory), the rows
+// of the one step that straddles the expert's end; a shared::cluster proxy
+// fence then orders those writes before its own MMA.
+//
+// Accumulator buffers: the leader's epilogue warps arrive on its
+// accumulator-empty barrier locally, the follower's remotely with a relaxed
+// arrive. The barrier orders only TMEM reads before the leader's next MMA into
+// the same columns: tcgen05.wait::ld has completed those reads before the
+// arrive is issued, and no memory written by the epilogue is published through
+// it. (A cluster-scope release from warps with bulk stores in flight costs this
+// kernel about a third of its time.)
+//
+// The epilogue streams fp32 rows out through two alternating [32 x 32] staging
+// blocks per warp and bulk tensor stores. When the M extent is an odd multiple
+// of 128, the follower's rows of the last m-tile lie past it: its A boxes read
+// the fill value and it stores nothing.
+struct WTile {
+  int e;
+  int row0;   // expert's first packed row (the K start)
+  int rows;   // expert's rows (K)
+  int m0;     // this CTA's first dW row
+  int n0;     // the tile's first dW column (this CTA loads n0 + 128*rank ..)
+  int nkb;
+};
+
+template <int KIND>
+__device__ __forceinline__ WTile decode_wgrad_pair(int t, int rank, const Params& p,
+                                                   const int* s_off) {
+  WTile tl;
+  const int per_e = p.m_tiles * p.n_tiles;
+  tl.e = t / per_e;
+  const int rem = t - tl.e * per_e;
+  const int mt = rem / p.n_tiles;
+  const int nt = rem - mt * p.n_tiles;
+  tl.m0 = mt * 2 * BM + rank * BM;
+  tl.n0 = nt * 256;
+  tl.row0 = s_off[tl.e];
+  tl.rows = s_off[tl.e + 1] - tl.row0;
+  tl.nkb = (tl.rows + BK - 1) / BK;
+  return tl;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+constexpr uint32_t kWgradPairEpiBytes = 4u * 2u * 4096u;
+constexpr int kWgradPairBars(int stages) { return 2 * stages + 5; }
+
+template <int KIND, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
+                               const __grid_constant__ CUtensorMap tmB,
+                               const __grid_constant__ CUtensorMap tmC0,
+                               const __grid_constant__ CUtensorMap tmC1, const Params p) {
+  static_assert(KIND == WGRAD_GU || KIND == WGRAD_D, "pair weight-gradient kernel");
+  constexpr int BN = 256;
+  constexpr uint32_t MN_ATOM = 64 * 128;
+  constexpr uint32_t A_BYTES = BM * BK * 2;
+  constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr uint32_t IDESC = make_idesc<BN, true, true, 2 * BM>();
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* epi = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + kWgradPairEpiBytes);
+  // bars: full[STAGES] (leader), empty[STAGES], tfull[2], tempty[2] (leader), drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kWgradPairBars(STAGES));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = (rank == 0);
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
+  const int mdim = (KIND == WGRAD_GU) ? p.d : p.I;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    // the leader's accumulator-empty barriers collect the four epilogue warps of both CTAs
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 8); }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC1)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  uint32_t peer_base;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];"
+               : "=r"(peer_base)
+               : "r"(map_to_rank(smem_u32(tmem_slot), rank ^ 1u))
+               : "memory");
+  const bool tmem_ok = (peer_base == tmem_base);
+  if (!tmem_ok && threadIdx.x == 0) report_status(p.status, MOE_ERR_DEVICE_CHECK);
+  const int total = tmem_ok ? p.E * p.m_tiles * p.n_tiles : 0;
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(n_clusters_x());
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t fpar = 0, fused = 0;   // per stage: parity of the next phase, used at all
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl) {
+        const WTile tl = decode_wgrad_pair<KIND>(t, static_cast<int>(rank), p, s_off);
+        const int nb = tl.n0 + static_cast<int>(rank) * (BN / 2);
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const int ky = tl.row0 + kb * BK;
+          const uint32_t fb = full_bar(stage);
+          if (leader) mbar_expect_tx(fb, 2 * STAGE_BYTES);   // both CTAs' boxes
+          const uint32_t fr = map_to_rank(fb, 0);
+          tma_load_2d_pair(sa, &tmA, fr, tl.m0, ky);
+          tma_load_2d_pair(sa + MN_ATOM, &tmA, fr, tl.m0 + 64, ky);
+          tma_load_2d_pair(sa + A_BYTES, &tmB, fr, nb, ky);
+          tma_load_2d_pair(sa + A_BYTES + MN_ATOM, &tmB, fr, nb + 64, ky);
+          fpar ^= 1u << stage;
+          fused |= 1u << stage;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (leader) {
+        // the leader's full barriers count both CTAs' loads: wait for the last phases
+        for (int s = 0; s < STAGES; ++s) {
+          if (!(fused & (1u << s))) continue;
+          const uint32_t par = ((fpar >> s) & 1u) ^ 1u;
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try(full_bar(s), par) && globaltimer() - t0 < kTimeoutNs) {
+          }
+        }
+      } else if (!ok) {
+        const uint64_t t0 = globaltimer();   // loads may still land after a timeout
+        while (globaltimer() - t0 < 1000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t peer_smem = map_to_rank(smem_base, 1);
+      for (int t = cid; t < total && ok; t += ncl) {
+        const WTile tl = decode_wgrad_pair<KIND>(t, 0, p, s_off);
+        if (tl.nkb == 0) continue;
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t sa = smem_base + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const int kvalid = min(BK, tl.rows - kb * BK);
+          const int nsteps = (kvalid + 15) >> 4;          // K16 steps with a valid row
+          const int zlo = kvalid, zhi = nsteps * 16;       // rows to zero in the last step
+          if (zlo < zhi) {
+            // rows [zlo, zhi) of both CTAs' A belong to the next expert
+            const uint32_t peer_a = peer_smem + stage * STAGE_BYTES;
+            const int nbytes = (zhi - zlo) * 128;
+            for (int i = lane; i < 2 * (nbytes >> 4); i += 32) {
+              const int atom = i / (nbytes >> 4);
+              const int off = zlo * 128 + ((i - atom * (nbytes >> 4)) << 4) + atom * MN_ATOM;
+              *reinterpret_cast<uint4*>(smem + stage * STAGE_BYTES + off) = make_uint4(0, 0, 0, 0);
+              asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(peer_a + off),
+                           "r"(0u)
+                           : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+            __syncwarp();
+          }
+          if (lane == 0) {
+            for (int kk = 0; kk < nsteps; ++kk) {
+              const uint64_t ad = smem_desc(sa + kk * 2048, MN_ATOM, 1024);
+              const uint64_t bd = smem_desc(sb + kk * 2048, MN_ATOM, 1024);
+              tc_mma_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit_pair_both(empty_bar(stage));
+          }
+          __syncwarp();
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit_pair_both(tfull_bar(acc));
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (lane == 0) {
+        tc_commit_pair_local(drain_bar);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try(drain_bar, 0) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int buf = 0;
+    for (int t = cid; t < total; t += ncl) {
+      const WTile tl = decode_wgrad_pair<KIND>(t, static_cast<int>(rank), p, s_off);
+      const bool empty = (tl.nkb == 0);   // expert without rows: its gradient is zero
+      if (!empty) {
+        if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+        tc_fence_after();
+      }
+      const bool in_range = tl.m0 < mdim;   // false only for the follower past an odd M extent
+      const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
+      const int mrow = tl.m0 + q * 32;
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        if (!empty) {
+          tmem_ld32(tacc + c, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        if (!in_range) continue;
+        uint8_t* stg = epi + ew * 8192 + buf * 4096;
+        if (lane == 0) bulk_wait_read_1();   // the store that last used this block has read it
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float4* dst = reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4));
+          *dst = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          const int n = tl.n0 + c;
+          if constexpr (KIND == WGRAD_GU) {
+            if (n < p.I) tma_store_2d(&tmC0, smem_u32(stg), n, tl.e * p.d + mrow);
+            else tma_store_2d(&tmC1, smem_u32(stg), n - p.I, tl.e * p.d + mrow);
+          } else {
+            tma_store_2d(&tmC0, smem_u32(stg), n, tl.e * p.I + mrow);
+          }
+          bulk_commit();
+        }
+        buf ^= 1;
+      }
+      if (empty) continue;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty_bar(acc));
+        else mbar_arrive_cluster_relaxed(map_to_rank(tempty_bar(acc), 0));
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
 // ----------------------------------------------------------------- diagnostics
 // One thread waits, through the GEMMs' bounded wait, on an mbarrier that nothing
 // arrives on; the wait runs out after timeout_ns and records the timeout.
@@ -1388,16 +1703,13 @@ size_t pair_smem_bytes(int E) {
          8 * (2 * STAGES + 9) + 16 + sizeof(int) * 2 * (E + 1) + 16;
 }
 
-// Launches the CTA-pair kernel on as many clusters of two as can be resident.
-template <int KIND, int BN, int STAGES>
-int launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
-                long long tiles_upper, cudaStream_t st) {
-  auto kern = grouped_gemm_pair_kernel<KIND, BN, STAGES>;
-  const size_t sm = pair_smem_bytes<KIND, BN, STAGES>(p.E);
-  const size_t sm_max = pair_smem_bytes<KIND, BN, STAGES>(1024);
-  static thread_local int configured = -1;
-  static thread_local int max_clusters = 0;
+// Launches a cluster-of-two kernel on as many clusters as can be resident
+// (at most tiles_upper). The shared-memory opt-in and the occupancy query run
+// once per kernel instantiation and device (the caller owns those two slots).
+template <typename... KArgs, typename... Args>
+int launch_cluster2(void (*kern)(KArgs...), size_t sm, size_t sm_max, int* configured,
+                    int* max_clusters, long long tiles_upper, const char* name, cudaStream_t st,
+                    const Args&... args) {
   int dev = 0;
   cudaGetDevice(&dev);
   cudaLaunchAttribute attr[1];
@@ -1411,7 +1723,7 @@ int launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& 
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (configured != dev) {
+  if (*configured != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sm_max));
     if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
@@ -1424,18 +1736,63 @@ int launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& 
       set_last_cuda_error(e == cudaSuccess ? cudaErrorInvalidConfiguration : e);
       return MOE_ERR_CUDA;
     }
-    max_clusters = n;
-    configured = dev;
+    *max_clusters = n;
+    *configured = dev;
   }
-  long long ncl = max_clusters;
+  long long ncl = *max_clusters;
   if (tiles_upper < ncl) ncl = tiles_upper;
   if (ncl < 1) return MOE_OK;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * ncl), 1, 1);
-  static const char* kNames[] = {"gemm_gate_up", "gemm_down", "gemm_dh", "gemm_dx", "", ""};
-  ProfScope prof(kNames[KIND], st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b0, b1, c0, c1, p);
+  ProfScope prof(name, st);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
   if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
   return check_launch();
+}
+
+// Launches the CTA-pair kernel of a forward or input-gradient kind.
+template <int KIND, int BN, int STAGES>
+int launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
+                long long tiles_upper, cudaStream_t st) {
+  static thread_local int configured = -1;
+  static thread_local int max_clusters = 0;
+  static const char* kNames[] = {"gemm_gate_up", "gemm_down", "gemm_dh", "gemm_dx", "", ""};
+  return launch_cluster2(grouped_gemm_pair_kernel<KIND, BN, STAGES>,
+                         pair_smem_bytes<KIND, BN, STAGES>(p.E),
+                         pair_smem_bytes<KIND, BN, STAGES>(1024), &configured, &max_clusters,
+                         tiles_upper, kNames[KIND], st, a, b0, b1, c0, c1, p);
+}
+
+// Weight gradients on CTA pairs: six 32 KB stages while the expert table fits
+// beside them (E <= 448), five otherwise.
+template <int STAGES>
+constexpr size_t pair_wgrad_smem_bytes(int E) {
+  return 1024 + STAGES * (BM * BK * 2 + 128 * BK * 2) + kWgradPairEpiBytes +
+         8 * kWgradPairBars(STAGES) + 16 + sizeof(int) * (E + 1) + 16;
+}
+constexpr int kWgradPair6MaxE = 448;
+static_assert(pair_wgrad_smem_bytes<6>(kWgradPair6MaxE) <= 232448, "pair wgrad smem (6 stages)");
+static_assert(pair_wgrad_smem_bytes<5>(1024) <= 232448, "pair wgrad smem (5 stages)");
+
+template <int KIND, int STAGES>
+int launch_pair_wgrad_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c0,
+                             const CUtensorMap& c1, const Params& p, long long tiles,
+                             cudaStream_t st) {
+  static thread_local int configured = -1;
+  static thread_local int max_clusters = 0;
+  return launch_cluster2(grouped_gemm_pair_wgrad_kernel<KIND, STAGES>,
+                         pair_wgrad_smem_bytes<STAGES>(p.E),
+                         pair_wgrad_smem_bytes<STAGES>(STAGES == 6 ? kWgradPair6MaxE : 1024),
+                         &configured, &max_clusters, tiles,
+                         KIND == WGRAD_GU ? "gemm_wgrad_gate_up" : "gemm_wgrad_down", st, a, b,
+                         c0, c1, p);
+}
+
+template <int KIND>
+int launch_pair_wgrad(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c0,
+                      const CUtensorMap& c1, const Params& p, long long tiles, cudaStream_t st) {
+  if (p.E <= kWgradPair6MaxE) return launch_pair_wgrad_stages<KIND, 6>(a, b, c0, c1, p, tiles, st);
+  return launch_pair_wgrad_stages<KIND, 5>(a, b, c0, c1, p, tiles, st);
 }
 
 // Pair pipeline depth: 32 KB stages (64 KB of [G|U] prefetch buffers for dh).
@@ -1629,24 +1986,30 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
       !make_map(&tc0, dw_gate, I, static_cast<uint64_t>(E) * d, 32, 32, true) ||
       !make_map(&tc1, dw_up, I, static_cast<uint64_t>(E) * d, 32, 32, true))
     return MOE_ERR_CUDA;
-  p.m_tiles = d / BM;
+  // CTA pairs over 256 dW rows x 256 columns (2I is a multiple of 256)
+  p.m_tiles = (d + 2 * BM - 1) / (2 * BM);
   p.n_tiles = 2 * I / 256;
   p.outf0 = dw_gate;
   p.outf1 = dw_up;
   p.out = nullptr;
-  rc = launch_bn<WGRAD_GU>(256, ta, tb0, tb0, tc0, tc1, p,
-                           static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
+  rc = launch_pair_wgrad<WGRAD_GU>(ta, tb0, tc0, tc1, p,
+                                   static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
   if (rc) return rc;
-  // dWd = H^T dY
-  const int bn_d = (d % 256 == 0) ? 256 : 128;
+  // dWd = H^T dY: CTA pairs when d is a multiple of 256, else single-CTA 128 x 128 tiles
   if (!make_map(&ta, h, I, M, 64, 64) || !make_map(&tb0, dy, d, M, 64, 64) ||
       !make_map(&tc0, dw_down, d, static_cast<uint64_t>(E) * I, 32, 32, true))
     return MOE_ERR_CUDA;
-  p.m_tiles = I / BM;
-  p.n_tiles = d / bn_d;
   p.outf0 = dw_down;
   p.outf1 = nullptr;
-  return launch_bn<WGRAD_D>(bn_d, ta, tb0, tb0, tc0, tc0, p,
+  if (d % 256 == 0) {
+    p.m_tiles = (I + 2 * BM - 1) / (2 * BM);
+    p.n_tiles = d / 256;
+    return launch_pair_wgrad<WGRAD_D>(ta, tb0, tc0, tc0, p,
+                                      static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
+  }
+  p.m_tiles = I / BM;
+  p.n_tiles = d / 128;
+  return launch_bn<WGRAD_D>(128, ta, tb0, tb0, tc0, tc0, p,
                             static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
 }
 

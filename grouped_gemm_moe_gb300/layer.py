@@ -176,6 +176,83 @@ class MoELayer:
         d2h = out_h.numel() * 2 + dx_h.numel() * 2 + self.host_splits.numel() * 4
         return h2d, d2h
 
+    def run_from_host(self, steps):
+        """A sequence of forward + backward steps whose inputs start in pinned
+        host memory and whose outputs end there. ``steps`` is a list of
+        ``(logits_h, x_h, dout_h, out_h, dx_h)``.
+
+        Inputs go to the device through two alternating input slots on an
+        upload stream, so step i+1's copy runs while step i computes; out and
+        dx go back on a download stream while the next pass runs. Every step
+        still moves its own inputs in and its outputs out. The current stream
+        joins both copy streams before returning. Returns the bytes copied each
+        way per step (of the last step)."""
+        dev = self.device
+        if not hasattr(self, "_slots"):
+            bf = torch.bfloat16
+            self._slots = [(torch.empty(self.T, self.E, dtype=torch.float32, device=dev),
+                            torch.empty(self.T, self.d, dtype=bf, device=dev),
+                            torch.empty(self.T, self.d, dtype=bf, device=dev)) for _ in range(2)]
+            self._up = torch.cuda.Stream(device=dev)
+            self._down = torch.cuda.Stream(device=dev)
+        cur = torch.cuda.current_stream(dev)
+        up, down = self._up, self._down
+        up.wait_stream(cur)      # earlier readers of the slots and of out / dx are done
+        down.wait_stream(cur)
+        n = len(steps)
+        in_ready = [None] * n
+        slot_free = [None] * n
+
+        def upload(i):
+            slot = self._slots[i % 2]
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(slot_free[i - 2])   # step i-2 no longer reads this slot
+                for dst, src in zip(slot, steps[i][:3]):
+                    dst.copy_(src, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(up)
+            in_ready[i] = ev
+
+        def after(stream):
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            return ev
+
+        if n:
+            upload(0)
+        out_copied = dx_copied = None
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            logits, x, dout = self._slots[i % 2]
+            out_h, dx_h = steps[i][3], steps[i][4]
+            cur.wait_event(in_ready[i])
+            if out_copied is not None:
+                cur.wait_event(out_copied)      # the previous step's out has left the device
+            out = self.forward(logits, x)
+            fwd_done = after(cur)
+            with torch.cuda.stream(down):
+                down.wait_event(fwd_done)
+                out_h.copy_(out, non_blocking=True)
+                out_copied = after(down)
+            if dx_copied is not None:
+                cur.wait_event(dx_copied)
+            dx = self.backward(dout)
+            slot_free[i] = after(cur)
+            with torch.cuda.stream(down):
+                down.wait_event(slot_free[i])
+                dx_h.copy_(dx, non_blocking=True)
+                dx_copied = after(down)
+        cur.wait_stream(down)
+        cur.wait_stream(up)
+        if not n:
+            return 0, 0
+        lh, xh, dh, oh, dxh = steps[-1]
+        h2d = lh.numel() * 4 + xh.numel() * 2 + dh.numel() * 2
+        d2h = oh.numel() * 2 + dxh.numel() * 2 + self.host_splits.numel() * 4
+        return h2d, d2h
+
     def device_status(self) -> int:
         """First nonzero device status among the GEMM workspaces (synchronises)."""
         wss = [self.ws_ffn, self.ws_bwd] + ([self.ws_sfwd, self.ws_sbwd] if self.shared else [])

@@ -158,3 +158,36 @@ def test_step_from_host_matches_device_path():
         torch.cuda.synchronize()
         assert torch.equal(out_h, out_d.cpu())
         assert torch.equal(dx_h, dx_d.cpu())
+
+
+def test_run_from_host_pipelined_steps_match_device_path():
+    """Four pipelined steps over three different batches (uploads of step i+1
+    overlapping step i, two input slots) give, per step, the bit-identical
+    out and dx of the device-resident path on that batch."""
+    cfg = W.small_config("host", T=1024, d=256, E=16, K=4, I=256, R=4)
+    inp = W.make_inputs(cfg, with_backward=True)
+    layer = L.layer_from_config(cfg, inp, dev())
+    g = torch.Generator().manual_seed(5)
+    batches = []
+    for b in range(3):
+        lg = inp["logits"] if b == 0 else torch.randn(cfg.T, cfg.E, generator=g)
+        x = inp["x"] if b == 0 else torch.randn(cfg.T, cfg.d, generator=g).to(torch.bfloat16)
+        do = inp["dout"] if b == 0 else torch.randn(cfg.T, cfg.d, generator=g).to(torch.bfloat16)
+        batches.append((lg, x, do))
+    want = []
+    for lg, x, do in batches:
+        o = layer.forward(lg.to(dev()), x.to(dev())).clone()
+        want.append((o.cpu(), layer.backward(do.to(dev())).clone().cpu()))
+    order = [0, 1, 2, 1]
+    steps = []
+    for b in order:
+        lg, x, do = batches[b]
+        steps.append((lg.pin_memory(), x.pin_memory(), do.pin_memory(),
+                      torch.zeros(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory(),
+                      torch.zeros(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()))
+    h2d, d2h = layer.run_from_host(steps)
+    torch.cuda.synchronize()
+    assert h2d == cfg.T * cfg.E * 4 + 2 * cfg.T * cfg.d * 2
+    for (_, _, _, oh, dxh), b in zip(steps, order):
+        assert torch.equal(oh, want[b][0])
+        assert torch.equal(dxh, want[b][1])

@@ -178,13 +178,44 @@ def kernel_work(name: str, cfg, shared: bool):
     hbm = {
         "route_topk": T * (4 * E + 8 * K),
         "route_topk_backward": T * (12 * K + 4 * E),
-        "perm_hist": 4 * TK, "perm_scatter": 12 * TK, "ep_hist": 4 * TK, "ep_scatter": 16 * TK,
+        "perm_hist": 4 * TK, "perm_scatter": 12 * TK, "ep_hist": 4 * TK,
+        # the layer's fused call also writes perm and inv_perm from the EP scatter
+        "ep_scatter": 24 * TK,
         "dispatch": T * (2 * d * (1 + K) + 4 * K),
         "combine": T * (2 * d * K + 8 * K + 2 * d + (2 * d if cfg.shared_I else 0)),
         "combine_backward": T * (2 * d + 4 * d * K + 12 * K),
         "dispatch_backward": T * (2 * d * K + 4 * K + 2 * d + (2 * d if cfg.shared_I else 0)),
     }
     return 0, hbm.get(name, 0)
+
+
+KERNEL_SOURCE = {"route": "route.cu", "perm": "permute.cu", "ep_": "permute.cu",
+                 "dispatch": "gather.cu", "combine": "gather.cu", "gemm": "grouped_gemm.cu"}
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary under
+    profiles/: a line 'traffic-record: kernel=<name> bytes_per_launch=<B>
+    source=<file> sha256=<hex>'. The figure counts only while the kernel's
+    source file still hashes to the recorded value (None otherwise)."""
+    import glob
+    import hashlib
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = next((f for pre, f in KERNEL_SOURCE.items() if kernel.startswith(pre)), None)
+    if src is None:
+        return None
+    path = os.path.join(here, "grouped_gemm_moe_gb300", "csrc", src)
+    if not os.path.exists(path):
+        return None
+    digest = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    for md in sorted(glob.glob(os.path.join(here, "profiles", "*.md"))):
+        for line in open(md):
+            if not line.startswith("traffic-record:"):
+                continue
+            kv = dict(f.split("=", 1) for f in line.split()[1:] if "=" in f)
+            if kv.get("kernel") == kernel and kv.get("source") == src and kv.get("sha256") == digest:
+                return float(kv["bytes_per_launch"])
+    return None
 
 
 def roofline_of(flops: float, nbytes: float, ms: float, pk) -> dict:
@@ -458,7 +489,7 @@ def main():
             "unit": rf["unit"], "frac": rf["frac"],
             "peak_source": pk["source"] + (" bf16 sustained" if rf["bound"] == "tensor"
                                            else " HBM copy (read+write)"),
-            "traffic": None,
+            "traffic": measured_traffic(dom),
             "work_per_launch": {"flop": dfl, "bytes": dnb},
             "avg_launch_ms": davg}
     flops_step = sum(kernel_work(c["name"], cfg, c["shared"])[0] * c["launches"]

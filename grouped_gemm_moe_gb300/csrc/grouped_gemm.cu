@@ -900,12 +900,12 @@ __device__ __forceinline__ void issue_pair(const PTile& tl, int kb, uint32_t ran
 }
 
 // Pair-kernel epilogue shared memory: bf16 output staging for bulk tensor stores,
-// per epilogue warp one [32 rows x 64 columns] 128-byte-swizzled box per output
-// stream (gate/up: H, G, U; down and dX: two buffers of Y), and for dh the
-// four G/U prefetch boxes, which the dG/dU results overwrite before their store.
+// per epilogue warp two alternating [32 rows x 64 columns] 128-byte-swizzled
+// boxes (gate/up streams H, G and U through them in turn), and for dh the four
+// G/U prefetch boxes, which the dG/dU results overwrite before their store.
 template <int KIND>
 __host__ __device__ constexpr uint32_t pair_epi_bytes() {
-  return KIND == FWD_GATEUP ? 4u * 3u * 4096u : (KIND == BWD_DH ? 4u * 16384u : 4u * 2u * 4096u);
+  return KIND == BWD_DH ? 4u * 16384u : 4u * 2u * 4096u;
 }
 
 // Writes 32 consecutive columns (values v) of this lane's row into a
@@ -1210,45 +1210,58 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         tc_fence_after();
         const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
         if constexpr (KIND == FWD_GATEUP) {
+          // H, then (when saved) G and U leave one stream at a time through the
+          // warp's two alternating [32 x 64] boxes; the accumulator is read again for
+          // each stream rather than holding all three in registers, which keeps the
+          // staging at 8 KB per warp and leaves shared memory for a deeper ring.
           constexpr int HALF = BN / 2;
-          uint8_t* stH = epi + ew * 12288;
-          uint8_t* stG = stH + 4096;
-          uint8_t* stU = stH + 8192;
+          const int nstreams = p.out2 ? 3 : 1;
           for (int c64 = 0; c64 < HALF; c64 += 64) {
-            if (full) {
-              if (lane == 0) bulk_wait_read_all();   // the previous boxes have been read
-              __syncwarp();
-            }
-            for (int sub = 0; sub < 64; sub += 32) {
-              float g[32], u[32], h[32];
-              tmem_ld32(tacc + c64 + sub, g);
-              tmem_ld32(tacc + HALF + c64 + sub, u);
-              tmem_wait_ld();
+            if (!full) {   // a slice that crosses the expert's end: row-wise stores
+              for (int sub = 0; sub < 64; sub += 32) {
+                float g[32], u[32], h[32];
+                tmem_ld32(tacc + c64 + sub, g);   // warp-wide: every lane loads
+                tmem_ld32(tacc + HALF + c64 + sub, u);
+                tmem_wait_ld();
+                if (valid) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) h[i] = silu_f(g[i]) * u[i];
-              if (full) {
-                stage_row32(stH, lane, sub >> 3, h);
-                stage_row32(stG, lane, sub >> 3, g);
-                stage_row32(stU, lane, sub >> 3, u);
-              } else if (valid) {
-                store32_bf16(p.out + grow * p.I + tl.n0 + c64 + sub, h);
-                if (p.out2) {
-                  store32_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c64 + sub, g);
-                  store32_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c64 + sub, u);
+                  for (int i = 0; i < 32; ++i) h[i] = silu_f(g[i]) * u[i];
+                  store32_bf16(p.out + grow * p.I + tl.n0 + c64 + sub, h);
+                  if (p.out2) {
+                    store32_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c64 + sub, g);
+                    store32_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c64 + sub, u);
+                  }
                 }
               }
+              continue;
             }
-            if (full) {
+            for (int sidx = 0; sidx < nstreams; ++sidx) {
+              uint8_t* st = epi + ew * 8192 + buf * 4096;
+              if (lane == 0) bulk_wait_read_1();   // the store that used this box is done
+              __syncwarp();
+              for (int sub = 0; sub < 64; sub += 32) {
+                float v[32];
+                if (sidx == 0) {
+                  float g[32], u[32];
+                  tmem_ld32(tacc + c64 + sub, g);
+                  tmem_ld32(tacc + HALF + c64 + sub, u);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) v[i] = silu_f(g[i]) * u[i];
+                } else {
+                  tmem_ld32(tacc + (sidx == 1 ? 0 : HALF) + c64 + sub, v);
+                  tmem_wait_ld();
+                }
+                stage_row32(st, lane, sub >> 3, v);
+              }
               fence_proxy_async();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tmC0, smem_u32(stH), tl.n0 + c64, growq);
-                if (p.out2) {
-                  tma_store_2d(&tmC1, smem_u32(stG), tl.n0 + c64, growq);
-                  tma_store_2d(&tmC1, smem_u32(stU), p.I + tl.n0 + c64, growq);
-                }
+                if (sidx == 0) tma_store_2d(&tmC0, smem_u32(st), tl.n0 + c64, growq);
+                else tma_store_2d(&tmC1, smem_u32(st), (sidx == 1 ? 0 : p.I) + tl.n0 + c64, growq);
                 bulk_commit();
               }
+              buf ^= 1;
             }
           }
         } else {  // FWD_DOWN, BWD_DX: one bf16 output, two staging boxes in turn
@@ -1813,13 +1826,11 @@ constexpr int pair_max_e() {
 // latency.
 template <int KIND, int BN>
 constexpr int pair_stages() {
-  return KIND == BWD_DH ? (BN == 256 ? 4 : 5)
-                        : KIND == FWD_GATEUP ? (BN == 256 ? 4 : 6) : (BN == 256 ? 5 : 7);
+  return KIND == BWD_DH ? (BN == 256 ? 4 : 5) : (BN == 256 ? 5 : 7);
 }
 template <int KIND, int BN>
 constexpr int pair_stages_deep() {
-  return KIND == BWD_DH ? (BN == 256 ? 5 : 6)
-                        : KIND == FWD_GATEUP ? (BN == 256 ? 5 : 7) : (BN == 256 ? 6 : 8);
+  return KIND == BWD_DH ? (BN == 256 ? 5 : 6) : (BN == 256 ? 6 : 8);
 }
 
 template <int KIND, int BN>

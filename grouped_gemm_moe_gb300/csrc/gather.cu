@@ -177,60 +177,60 @@ gather_sum_kernel(const uint4* __restrict__ rows, const float* __restrict__ w,
   }
 }
 
-// One warp per token: dy[p] = bf16(w[a] * dout[t]) and dw[a] = <dout[t], y[p]>
-// for its K assignments a = t*K + j, p = inv_perm[a]. Each lane walks its
-// 16-byte columns once, with the K gathered loads of a column in flight
-// together and one dot-product accumulator per slot. dy is the exact product
-// rounded once, so it is bit-identical to any correctly rounded evaluation.
-template <int KMAX>
+// One warp per assignment a = t*K + j (p = inv_perm[a]): dy[p] = bf16(w[a] *
+// dout[t]) and dw[a] = <dout[t], y[p]>. Each lane walks its 16-byte columns
+// c = lane, lane+32, ... in order, with kUnroll columns' loads in flight before
+// it computes, so the dot product sums in a fixed order; the K warps of a
+// token run next to each other and share dout[t] through the caches. dy is
+// the exact product rounded once, so it is bit-identical to any correctly
+// rounded evaluation. 64 registers per thread: four 256-thread blocks (32
+// warps) per SM, each warp with 4 KB of loads in flight.
+constexpr int kCbUnroll = 4;
+
 __global__ void __launch_bounds__(kThreads)
 combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ y,
-                        const float* __restrict__ w, const int32_t* __restrict__ inv_perm, int T,
-                        int K, int nv, uint4* __restrict__ dy, float* __restrict__ dw) {
+                        const float* __restrict__ w, const int32_t* __restrict__ inv_perm,
+                        long long TK, int K, int nv, uint4* __restrict__ dy,
+                        float* __restrict__ dw) {
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (kThreads / 32);
-  for (long long t = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
-       t < T; t += warps) {
+  for (long long a = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+       a < TK; a += warps) {
+    const long long t = a / K;
     const uint4* drow = dout + t * nv;
-    long long prow[KMAX];
-    float wa[KMAX], dot[KMAX];
+    const long long prow = static_cast<long long>(__ldg(inv_perm + a)) * nv;
+    const uint4* yrow = y + prow;
+    uint4* orow = dy + prow;
+    const float wa = __ldg(w + a);
+    float dot = 0.f;
+    for (int c0 = lane; c0 < nv; c0 += 32 * kCbUnroll) {
+      uint4 dv[kCbUnroll], yv[kCbUnroll];
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      dot[j] = 0.f;
-      if (j < K) {
-        prow[j] = static_cast<long long>(__ldg(inv_perm + t * K + j)) * nv;
-        wa[j] = __ldg(w + t * K + j);
+      for (int u = 0; u < kCbUnroll; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < nv) {
+          dv[u] = ldg_nc_v4(drow + c);
+          yv[u] = ldg_nc_v4(yrow + c);
+        }
       }
-    }
-    for (int c = lane; c < nv; c += 32) {
-      const uint4 dv = ldg_nc_v4(drow + c);
-      uint4 yv[KMAX];
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (j < K) yv[j] = ldg_nc_v4(y + prow[j] + c);
-      float fd[8];
-      unpack8(dv, fd);
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < K) {
-          float fy[8], g[8];
-          unpack8(yv[j], fy);
+      for (int u = 0; u < kCbUnroll; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < nv) {
+          float fd[8], fy[8], g[8];
+          unpack8(dv[u], fd);
+          unpack8(yv[u], fy);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            dot[j] = fmaf(fd[q], fy[q], dot[j]);
-            g[q] = mul_bf16_exact(wa[j], fd[q]);
+            dot = fmaf(fd[q], fy[q], dot);
+            g[q] = mul_bf16_exact(wa, fd[q]);
           }
-          stg_v4(dy + prow[j] + c, pack8(g));
+          stg_v4(orow + c, pack8(g));
         }
       }
     }
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      if (j < K) {
-        const float s = warp_sum(dot[j]);
-        if (lane == 0) dw[t * K + j] = s;
-      }
-    }
+    const float sum = warp_sum(dot);
+    if (lane == 0) dw[a] = sum;
   }
 }
 
@@ -334,20 +334,14 @@ extern "C" int moe_combine_backward(const moe_bf16* dout, const moe_bf16* y, con
   if (!aligned16(dout) || !aligned16(y) || !aligned16(topk_w) || !aligned16(inv_perm) ||
       !aligned16(dy) || !aligned16(dtopk_w))
     return MOE_ERR_MISALIGNED;
+  const long long TK = static_cast<long long>(T) * K;
   const int per_block = kThreads / 32;
-  long long blocks = (T + per_block - 1) / per_block;
-  const long long cap = static_cast<long long>(num_sms()) * 16;
+  long long blocks = (TK + per_block - 1) / per_block;
+  const long long cap = static_cast<long long>(num_sms()) * 48;
   if (blocks > cap) blocks = cap;
   ProfScope prof("combine_backward", as_stream(stream));
-  auto go = [&](auto kern) {
-    kern<<<static_cast<int>(blocks), kThreads, 0, as_stream(stream)>>>(
-        reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(y), topk_w, inv_perm,
-        T, K, d / 8, reinterpret_cast<uint4*>(dy), dtopk_w);
-  };
-  if (K <= 2) go(combine_backward_kernel<2>);
-  else if (K <= 4) go(combine_backward_kernel<4>);
-  else if (K <= 8) go(combine_backward_kernel<8>);
-  else if (K <= 16) go(combine_backward_kernel<16>);
-  else go(combine_backward_kernel<32>);
+  combine_backward_kernel<<<static_cast<int>(blocks), kThreads, 0, as_stream(stream)>>>(
+      reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(y), topk_w, inv_perm, TK,
+      K, d / 8, reinterpret_cast<uint4*>(dy), dtopk_w);
   return check_launch();
 }

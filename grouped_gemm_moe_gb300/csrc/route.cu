@@ -2,11 +2,12 @@
 // "Expert Parallel (EP)" -> "Producing assignments": scores [T,E] against all
 // experts, top-K selection of expert_IDs and router_weights [T,K]).
 //
-// Forward: a group of G lanes per token (see route_topk_kernel). Each of the K
-// rounds is a butterfly arg-max over (logit, -id) across the group: the larger
-// logit wins, equal logits go to the lower id (a float comparison, so -0.0 and
-// +0.0 tie). The softmax max is the round-0 winner; its denominators are group
-// sums. Backward: one warp per token.
+// Forward: one warp per token; lane l holds experts l, l+32, ... Logits become
+// order-preserving unsigned keys (-0.0 and +0.0 share one key, so they tie),
+// and each of the K rounds is a warp-wide max over the lanes' best untaken
+// keys followed by a warp-wide min over the ids that hold it: the larger logit
+// wins, equal logits go to the lower id. The softmax max is the round-0
+// winner. Backward: one warp per token.
 #include "common.cuh"
 
 namespace moe {
@@ -14,80 +15,67 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
-// One group of G lanes per token (G in 4..32, a power of two); lane l of a
-// group holds experts l, l+G, l+2G, ... (V values). Each of the K rounds is a
-// local best over the lane's untaken values and a butterfly over the group on
-// (logit, -id). The winner's owner marks it taken and remembers its slot; the
-// weights are written per taken value at the end.
-template <int G, int V>
-__global__ void __launch_bounds__(256)
+// Order-preserving map of a finite float to an unsigned key; 0 is never a key.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  if (f == 0.f) f = 0.f;   // -0.0 -> +0.0
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// V = ceil(E / 32) logits per lane. Round j: each lane's best untaken key
+// (lowest id on equal keys), the warp max M of those (redux.sync), then the
+// lowest id among lanes whose best is M (redux.sync). Lane j keeps slot j's
+// id and logit, and lanes 0..K-1 write the K slots with coalesced stores.
+template <int V>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
 route_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renorm,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
-  const int gl = threadIdx.x & (G - 1);
-  const long long tok = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / G;
-  const bool active = tok < T;
-  const float* row = logits + (active ? tok : 0) * static_cast<long long>(E);
+  const int lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;   // whole warps only
+  const float* row = logits + t * E;
   float v[V];
-  int slot[V];
-  unsigned taken = 0;  // bit i: value i of this lane is selected (or padding)
+  uint32_t key[V];
+  uint32_t avail = 0;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int e = gl + G * i;
+    const int e = lane + 32 * i;
     v[i] = (e < E) ? __ldg(row + e) : 0.f;
-    slot[i] = 0;
-    if (e >= E) taken |= 1u << i;
+    key[i] = (e < E) ? order_key(v[i]) : 0u;
+    if (e < E) avail |= 1u << i;
   }
-  float top = 0.f;
+  float top = 0.f, mine = 0.f;
+  int mine_id = 0;
   for (int j = 0; j < K; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    uint32_t bk = 0;
+    int bi = 0;
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-      if (taken & (1u << i)) continue;
-      if (bi == 0x7fffffff || v[i] > bv) { bv = v[i]; bi = gl + G * i; }   // ids ascend with i
-    }
-#pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const bool better = (oi != 0x7fffffff) &&
-                          (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-      if (better) { bv = ov; bi = oi; }
-    }
-    if ((bi & (G - 1)) == gl) {
-      const int wi = bi / G;
-#pragma unroll
-      for (int i = 0; i < V; ++i)
-        if (i == wi) { taken |= 1u << i; slot[i] = j; }
-    }
-    if (j == 0) top = bv;
+    for (int i = 0; i < V; ++i)
+      if (((avail >> i) & 1u) && key[i] > bk) { bk = key[i]; bi = i; }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = (bk == m && bk != 0u) ? static_cast<uint32_t>(lane + 32 * bi) : 0xffffffffu;
+    const uint32_t id = __reduce_min_sync(0xffffffffu, cand);
+    if (static_cast<int>(id & 31u) == lane) avail &= ~(1u << (id >> 5));
+    const float val = key_value(m);
+    if (j == 0) top = val;
+    if (lane == j) { mine = val; mine_id = static_cast<int>(id); }
   }
-  // softmax over all E (max = top), optionally renormalised over the K selected
-  float s_all = 0.f, s_sel = 0.f;
+  // softmax over all E (max = top), or over the K selected when renormalising
+  float part = 0.f;
+  if (renorm) {
+    if (lane < K) part = expf(mine - top);
+  } else {
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int e = gl + G * i;
-    if (e < E) {
-      const float x = expf(v[i] - top);
-      s_all += x;
-      if (taken & (1u << i)) s_sel += x;
-    }
+    for (int i = 0; i < V; ++i)
+      if (lane + 32 * i < E) part += expf(v[i] - top);
   }
-#pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) {
-    s_all += __shfl_xor_sync(0xffffffffu, s_all, o);
-    s_sel += __shfl_xor_sync(0xffffffffu, s_sel, o);
-  }
-  if (!active) return;
-  const float denom = renorm ? s_sel : s_all;
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int e = gl + G * i;
-    if (e < E && (taken & (1u << i))) {
-      const long long o = tok * K + slot[i];
-      topk_idx[o] = e;
-      topk_w[o] = expf(v[i] - top) / denom;
-    }
+  const float denom = warp_sum(part);
+  if (lane < K) {
+    topk_idx[t * K + lane] = mine_id;
+    topk_w[t * K + lane] = expf(mine - top) / denom;
   }
 }
 
@@ -152,15 +140,16 @@ int dispatch_v(int E, Args... args) {
   return Launcher<32>::run(args...);
 }
 
-template <int G, int V>
-int launch_fwd(const float* logits, int T, int E, int K, int renorm, int32_t* idx, float* w,
-               cudaStream_t st) {
-  const long long threads = static_cast<long long>(T) * G;
-  const int blocks = static_cast<int>((threads + 255) / 256);
-  ProfScope prof("route_topk", st);
-  route_topk_kernel<G, V><<<blocks, 256, 0, st>>>(logits, T, E, K, renorm, idx, w);
-  return check_launch();
-}
+template <int V>
+struct FwdLauncher {
+  static int run(const float* logits, int T, int E, int K, int renorm, int32_t* idx, float* w,
+                 cudaStream_t st) {
+    const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    ProfScope prof("route_topk", st);
+    route_topk_kernel<V><<<blocks, kWarpsPerBlock * 32, 0, st>>>(logits, T, E, K, renorm, idx, w);
+    return check_launch();
+  }
+};
 
 template <int V>
 struct BwdLauncher {
@@ -184,13 +173,7 @@ extern "C" int moe_route_topk(const float* logits, int T, int E, int K, int reno
   if (T == 0) return MOE_OK;
   if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(topk_w)) return MOE_ERR_MISALIGNED;
-  cudaStream_t st = as_stream(stream);
-  // group width: at most 16 logits per lane up to E = 512, 32 beyond
-  if (E <= 64) return launch_fwd<4, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
-  if (E <= 128) return launch_fwd<8, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
-  if (E <= 256) return launch_fwd<16, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
-  if (E <= 512) return launch_fwd<32, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
-  return launch_fwd<32, 32>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  return dispatch_v<FwdLauncher>(E, logits, T, E, K, renorm, topk_idx, topk_w, as_stream(stream));
 }
 
 extern "C" int moe_route_topk_backward(const float* logits, const int32_t* topk_idx,

@@ -20,7 +20,9 @@ combine, and the backward of each. Rank 0 prints one JSON line.
   and the last download fall inside the timed region.
 * roofline: the dominant kernel's algorithmic flops (or bytes) per launch over
   its average launch duration, from per-launch events the library records on
-  the launching stream during the timed steps.
+  the launching stream during a second pass of the same timed steps (the
+  first pass, which gives `value`, has no events between launches, so each
+  kernel can be launched while its predecessor finishes).
 * cpu_baseline: the CPU oracle timed on a bounded sample of the same workload.
 * --impl reference: the CPU oracle as the reference arm (rank 0 only).
 
@@ -446,7 +448,6 @@ def main():
 
     barrier()
     torch.cuda.synchronize()
-    B.moe_profile_start(64 * args.steps + 64)
     evs = []
     for i in range(args.steps):
         flush_l2()
@@ -458,8 +459,18 @@ def main():
         evs.append((s, e))
     torch.cuda.synchronize()
     barrier()
-    records = B.moe_profile_stop()
     step_ms = [s.elapsed_time(e) for s, e in evs]
+    # per-kernel durations: the same K steps again, each library launch bracketed by
+    # events on its stream (kept out of the pass above, where events between launches
+    # would hold back each kernel's early launch behind its predecessor)
+    B.moe_profile_start(64 * args.steps + 64)
+    for i in range(args.steps):
+        flush_l2()
+        layer.forward(logits, x)
+        layer.backward(dout)
+    torch.cuda.synchronize()
+    barrier()
+    records = B.moe_profile_stop()
     ms = max_over_ranks(statistics.mean(step_ms), world, dev)
     value = aggregate_value(ms, cfg.T, world)
 

@@ -44,7 +44,54 @@ struct ProfScope {
   ~ProfScope() { prof_end(st); }
 };
 
+// Launches a kernel with programmatic dependent launch: it may be scheduled
+// while the previous kernel of the stream is still finishing, so it must run
+// pdl_wait() before it reads anything an earlier launch wrote (every kernel of
+// this library does so first thing). cluster_x > 1 adds a cluster dimension.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      unsigned cluster_x, const Args&... args) {
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  return check_launch();
+}
+
 // Device side ----------------------------------------------------------------
+
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their memory is visible, then let the next launch of the
+// stream be scheduled (its own pdl_wait() still waits for this grid to end).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Both, as the first statement of a kernel.
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }

@@ -40,6 +40,7 @@ constexpr int kRowVecs = 8;   // 16-byte vectors per lane per pass (4 KB per war
 __global__ void __launch_bounds__(kThreads)
 dispatch_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int K, int nv,
                 long long rows, uint4* __restrict__ xp) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const long long nwarps = static_cast<long long>(gridDim.x) * (kThreads / 32);
   for (long long p = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
@@ -91,6 +92,7 @@ __device__ __forceinline__ bool bulk_bar_wait(uint32_t bar, uint32_t parity) {
 __global__ void __launch_bounds__(32)
 dispatch_bulk_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ perm, int K,
                      int row_bytes, long long rows, uint8_t* __restrict__ xp) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t bars[kBulkSlots];
   if (threadIdx.x != 0) return;
@@ -146,6 +148,7 @@ __global__ void __launch_bounds__(kThreads)
 gather_sum_kernel(const uint4* __restrict__ rows, const float* __restrict__ w,
                   const int32_t* __restrict__ inv_perm, int K, int nv, long long total,
                   const uint4* __restrict__ extra, uint4* __restrict__ out) {
+  pdl_enter();
   const long long stride = static_cast<long long>(gridDim.x) * kThreads;
   for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < total;
        i += stride) {
@@ -192,6 +195,7 @@ combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict_
                         const float* __restrict__ w, const int32_t* __restrict__ inv_perm,
                         long long TK, int K, int nv, uint4* __restrict__ dy,
                         float* __restrict__ dw) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (kThreads / 32);
   for (long long a = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
@@ -243,17 +247,14 @@ int launch_gather_sum(const void* rows, const float* w, const int32_t* inv_perm,
   auto x = static_cast<const uint4*>(extra);
   auto o = static_cast<uint4*>(out);
   ProfScope prof(w ? "combine" : "dispatch_backward", st);
-  if (K <= 2)
-    gather_sum_kernel<2><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
-  else if (K <= 4)
-    gather_sum_kernel<4><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
-  else if (K <= 8)
-    gather_sum_kernel<8><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
-  else if (K <= 16)
-    gather_sum_kernel<16><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
-  else
-    gather_sum_kernel<32><<<grid, kThreads, 0, st>>>(r, w, inv_perm, K, nv, total, x, o);
-  return check_launch();
+  auto go = [&](auto kern) {
+    return launch_pdl(kern, grid, kThreads, 0, st, 1, r, w, inv_perm, K, nv, total, x, o);
+  };
+  if (K <= 2) return go(gather_sum_kernel<2>);
+  if (K <= 4) return go(gather_sum_kernel<4>);
+  if (K <= 8) return go(gather_sum_kernel<8>);
+  if (K <= 16) return go(gather_sum_kernel<16>);
+  return go(gather_sum_kernel<32>);
 }
 
 bool shape_ok(int T, int K, int d) { return T >= 0 && K >= 1 && K <= 32 && d > 0 && d % 8 == 0; }
@@ -286,17 +287,15 @@ extern "C" int moe_dispatch(const moe_bf16* x, int T, int d, int K, const int32_
     long long grid = static_cast<long long>(num_sms()) * (per_sm > 0 ? per_sm : 1);
     if (grid > rows) grid = rows;
     ProfScope prof("dispatch", st);
-    dispatch_bulk_kernel<<<static_cast<int>(grid), 32, ring, st>>>(
-        reinterpret_cast<const uint8_t*>(x), perm, K, row_bytes, rows,
-        reinterpret_cast<uint8_t*>(xp));
-    return check_launch();
+    return launch_pdl(dispatch_bulk_kernel, static_cast<unsigned>(grid), 32, ring, st, 1,
+                      reinterpret_cast<const uint8_t*>(x), perm, K, row_bytes, rows,
+                      reinterpret_cast<uint8_t*>(xp));
   }
   const int nv = d / 8;
   const int grid = grid_for(rows, kThreads / 32);
   ProfScope prof("dispatch", st);
-  dispatch_kernel<<<grid, kThreads, 0, st>>>(reinterpret_cast<const uint4*>(x), perm, K, nv, rows,
-                                             reinterpret_cast<uint4*>(xp));
-  return check_launch();
+  return launch_pdl(dispatch_kernel, grid, kThreads, 0, st, 1, reinterpret_cast<const uint4*>(x),
+                    perm, K, nv, rows, reinterpret_cast<uint4*>(xp));
 }
 
 extern "C" int moe_combine(const moe_bf16* y, const float* topk_w, const int32_t* inv_perm, int T,
@@ -340,8 +339,8 @@ extern "C" int moe_combine_backward(const moe_bf16* dout, const moe_bf16* y, con
   const long long cap = static_cast<long long>(num_sms()) * 48;
   if (blocks > cap) blocks = cap;
   ProfScope prof("combine_backward", as_stream(stream));
-  combine_backward_kernel<<<static_cast<int>(blocks), kThreads, 0, as_stream(stream)>>>(
-      reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(y), topk_w, inv_perm, TK,
-      K, d / 8, reinterpret_cast<uint4*>(dy), dtopk_w);
-  return check_launch();
+  return launch_pdl(combine_backward_kernel, static_cast<unsigned>(blocks), kThreads, 0,
+                    as_stream(stream), 1, reinterpret_cast<const uint4*>(dout),
+                    reinterpret_cast<const uint4*>(y), topk_w, inv_perm, TK, K, d / 8,
+                    reinterpret_cast<uint4*>(dy), dtopk_w);
 }

@@ -536,6 +536,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  pdl_wait();   // offsets and operands come from earlier launches
+  pdl_launch_dependents();
   for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
   __syncthreads();
   if constexpr (!kWgrad) {
@@ -994,6 +996,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
+  pdl_wait();   // offsets and operands come from earlier launches
+  pdl_launch_dependents();
   for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
   __syncthreads();
   if (warp == 0) {   // exclusive prefix of per-expert m-tile pairs
@@ -1435,6 +1439,8 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
+  pdl_wait();   // offsets and operands come from earlier launches
+  pdl_launch_dependents();
   for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
   tc_fence_before();
   __syncthreads();
@@ -1702,8 +1708,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
   static const char* kNames[] = {"gemm_gate_up", "gemm_down", "gemm_dh", "gemm_dx",
                                  "gemm_wgrad_gate_up", "gemm_wgrad_down"};
   ProfScope prof(kNames[KIND], st);
-  kern<<<static_cast<int>(grid), kThreads, sm, st>>>(a, b0, b1, c0, c1, p);
-  return check_launch();
+  return launch_pdl(kern, static_cast<unsigned>(grid), kThreads, sm, st, 1, a, b0, b1, c0, c1, p);
 }
 
 #ifndef MOE_PAIR_BN_MAX
@@ -1755,11 +1760,8 @@ int launch_cluster2(void (*kern)(KArgs...), size_t sm, size_t sm_max, int* confi
   long long ncl = *max_clusters;
   if (tiles_upper < ncl) ncl = tiles_upper;
   if (ncl < 1) return MOE_OK;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * ncl), 1, 1);
   ProfScope prof(name, st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
-  if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
-  return check_launch();
+  return launch_pdl(kern, static_cast<unsigned>(2 * ncl), kThreads, sm, st, 2, args...);
 }
 
 // Launches the CTA-pair kernel of a forward or input-gradient kind with the

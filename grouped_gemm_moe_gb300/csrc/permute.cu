@@ -82,6 +82,7 @@ __device__ __forceinline__ void warp_exscan(int* a, int n) {
 
 __global__ void __launch_bounds__(kThreads)
 hist_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int32_t* __restrict__ hist) {
+  pdl_enter();
   extern __shared__ int smem[];
   int* wh = smem;  // [kWarps][E]
   for (int i = threadIdx.x; i < kWarps * E; i += kThreads) wh[i] = 0;
@@ -120,6 +121,7 @@ template <bool EP>
 __global__ void __launch_bounds__(kThreads)
 scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
                const int32_t* __restrict__ hist, PermOut po, EpOut eo) {
+  pdl_enter();
   extern __shared__ int smem[];
   int* wh = smem;                    // [kWarps][E]
   int* off = wh + kWarps * E;        // [E+1] offsets
@@ -249,18 +251,18 @@ int launch_counting_sort(bool ep, const int32_t* idx, long long TK, int E, int R
     configured_dev = dev;
   }
   (void)ws_bytes;
+  int rc;
   {
     ProfScope prof(ep ? "ep_hist" : "perm_hist", st);
-    hist_kernel<<<NC, kThreads, sh_hist, st>>>(idx, E, g, hist);
+    rc = launch_pdl(hist_kernel, NC, kThreads, sh_hist, st, 1, idx, E, g, hist);
   }
-  int rc = check_launch();
   if (rc) return rc;
   ProfScope prof(ep ? "ep_scatter" : "perm_scatter", st);
   if (ep)
-    scatter_kernel<true><<<NC, kThreads, sh_scatter, st>>>(idx, E, g, NC, hist, po, eo);
-  else
-    scatter_kernel<false><<<NC, kThreads, sh_scatter, st>>>(idx, E, g, NC, hist, po, eo);
-  return check_launch();
+    return launch_pdl(scatter_kernel<true>, NC, kThreads, sh_scatter, st, 1, idx, E, g, NC, hist,
+                      po, eo);
+  return launch_pdl(scatter_kernel<false>, NC, kThreads, sh_scatter, st, 1, idx, E, g, NC, hist, po,
+                    eo);
 }
 
 }  // namespace
@@ -445,11 +447,10 @@ extern "C" int moe_build_permutation_static(const int32_t* topk_idx, int T, int 
   EpOut eo{};
   {
     ProfScope prof("perm_hist", st);
-    hist_kernel<<<NC, kThreads, sh_hist, st>>>(topk_idx, E, g, hist);
+    rc = launch_pdl(hist_kernel, NC, kThreads, sh_hist, st, 1, topk_idx, E, g, hist);
   }
-  rc = check_launch();
   if (rc) return rc;
   ProfScope prof("perm_scatter", st);
-  scatter_kernel<false><<<NC, kThreads, sh_scatter, st>>>(topk_idx, E, g, NC, hist, po, eo);
-  return check_launch();
+  return launch_pdl(scatter_kernel<false>, NC, kThreads, sh_scatter, st, 1, topk_idx, E, g, NC, hist,
+                    po, eo);
 }

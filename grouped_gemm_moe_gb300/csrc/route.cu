@@ -33,6 +33,7 @@ template <int V>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 route_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int renorm,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const long long t = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;   // whole warps only
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 route_topk_backward_kernel(const float* __restrict__ logits, const int32_t* __restrict__ topk_idx,
                            const float* __restrict__ topk_w, const float* __restrict__ dtopk_w,
                            int T, int E, int K, int renorm, float* __restrict__ dlogits) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -146,8 +148,8 @@ struct FwdLauncher {
                  cudaStream_t st) {
     const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
     ProfScope prof("route_topk", st);
-    route_topk_kernel<V><<<blocks, kWarpsPerBlock * 32, 0, st>>>(logits, T, E, K, renorm, idx, w);
-    return check_launch();
+    return launch_pdl(route_topk_kernel<V>, blocks, kWarpsPerBlock * 32, 0, st, 1, logits, T, E, K,
+                      renorm, idx, w);
   }
 };
 
@@ -157,9 +159,8 @@ struct BwdLauncher {
                  int E, int K, int renorm, float* dl, cudaStream_t st) {
     const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
     ProfScope prof("route_topk_backward", st);
-    route_topk_backward_kernel<V><<<blocks, kWarpsPerBlock * 32, 0, st>>>(logits, idx, w, dw, T,
-                                                                           E, K, renorm, dl);
-    return check_launch();
+    return launch_pdl(route_topk_backward_kernel<V>, blocks, kWarpsPerBlock * 32, 0, st, 1, logits,
+                      idx, w, dw, T, E, K, renorm, dl);
   }
 };
 

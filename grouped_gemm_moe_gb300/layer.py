@@ -45,7 +45,6 @@ class MoELayer:
         self.xp = e(TK, d, dt=bf)
         self.y, self.h, self.gu = e(TK, d, dt=bf), e(TK, I, dt=bf), e(TK, 2 * I, dt=bf)
         self.out = e(T, d, dt=bf)
-        self.ws_perm = B.new_workspace(B.workspace_size(B.MOE_OP_BUILD_PERMUTATION, T, E, K), dev)
         self.ws_ep = B.new_workspace(B.workspace_size(B.MOE_OP_EP_LAYOUT, T, E, K, R), dev)
         self.ws_ffn = B.new_workspace(B.workspace_size(B.MOE_OP_GROUPED_FFN, T, E, K, 1, d, I), dev)
         # backward buffers
@@ -73,6 +72,8 @@ class MoELayer:
         self.logits = None
         self.x = None
         self.timeline: Optional[List] = None   # when a list, (name, start_event, end_event) per call
+        self._mark_splits = False
+        self.splits_issued = None
 
     # -------------------------------------------------------------- timing hooks
     def _mark(self, name):
@@ -106,6 +107,9 @@ class MoELayer:
                   host_splits=self.host_splits if copy_splits else False, ws=self.ws_ep,
                   out=(self.counts, self.offsets, self.perm, self.inv_perm, self.ep_splits,
                        self.send_index, self.a2a_index, self.regroup_index))
+        if self._mark_splits:   # the splits' device-to-host copy has been issued
+            self.splits_issued = torch.cuda.Event()
+            self.splits_issued.record(torch.cuda.current_stream(self.device))
         self._run("dispatch", B.moe_dispatch, x, self.perm, K, out=self.xp)
         self._run("grouped_ffn", B.moe_grouped_ffn, self.xp, self.offsets, w["w_gate"], w["w_up"],
                   w["w_down"], ws=self.ws_ffn, out=(self.y, self.h, self.gu))
@@ -183,10 +187,13 @@ class MoELayer:
 
         Inputs go to the device through two alternating input slots on an
         upload stream, so step i+1's copy runs while step i computes; out and
-        dx go back on a download stream while the next pass runs. Every step
-        still moves its own inputs in and its outputs out. The current stream
-        joins both copy streams before returning. Returns the bytes copied each
-        way per step (of the last step)."""
+        dx go back on a download stream while the next pass runs. The large
+        copies are issued only after the step's own small copy of the EP
+        splits (on the compute stream), so that copy never queues behind a
+        33 MB transfer. Every step still moves its own inputs in and its
+        outputs out. The current stream joins both copy streams before
+        returning. Returns the bytes copied each way per step (of the last
+        step)."""
         dev = self.device
         if not hasattr(self, "_slots"):
             bf = torch.bfloat16
@@ -201,49 +208,55 @@ class MoELayer:
         down.wait_stream(cur)
         n = len(steps)
         in_ready = [None] * n
-        slot_free = [None] * n
-
-        def upload(i):
-            slot = self._slots[i % 2]
-            with torch.cuda.stream(up):
-                if i >= 2:
-                    up.wait_event(slot_free[i - 2])   # step i-2 no longer reads this slot
-                for dst, src in zip(slot, steps[i][:3]):
-                    dst.copy_(src, non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(up)
-            in_ready[i] = ev
 
         def after(stream):
             ev = torch.cuda.Event()
             ev.record(stream)
             return ev
 
+        def upload(i, gate=None):
+            with torch.cuda.stream(up):
+                if gate is not None:
+                    up.wait_event(gate)
+                for dst, src in zip(self._slots[i % 2], steps[i][:3]):
+                    dst.copy_(src, non_blocking=True)
+                in_ready[i] = after(up)
+
         if n:
             upload(0)
         out_copied = dx_copied = None
-        for i in range(n):
-            if i + 1 < n:
-                upload(i + 1)
-            logits, x, dout = self._slots[i % 2]
-            out_h, dx_h = steps[i][3], steps[i][4]
-            cur.wait_event(in_ready[i])
-            if out_copied is not None:
-                cur.wait_event(out_copied)      # the previous step's out has left the device
-            out = self.forward(logits, x)
-            fwd_done = after(cur)
-            with torch.cuda.stream(down):
-                down.wait_event(fwd_done)
-                out_h.copy_(out, non_blocking=True)
-                out_copied = after(down)
-            if dx_copied is not None:
-                cur.wait_event(dx_copied)
-            dx = self.backward(dout)
-            slot_free[i] = after(cur)
-            with torch.cuda.stream(down):
-                down.wait_event(slot_free[i])
-                dx_h.copy_(dx, non_blocking=True)
-                dx_copied = after(down)
+        pending_dx = None        # the previous step's dx_h, downloaded once this step's splits left
+        self._mark_splits = True
+        try:
+            for i in range(n):
+                logits, x, dout = self._slots[i % 2]
+                out_h, dx_h = steps[i][3], steps[i][4]
+                cur.wait_event(in_ready[i])
+                if out_copied is not None:
+                    cur.wait_event(out_copied)      # the previous step's out has left the device
+                out = self.forward(logits, x)
+                splits = self.splits_issued      # after the previous backward, in stream order
+                fwd_done = after(cur)
+                with torch.cuda.stream(down):
+                    if pending_dx is not None:
+                        down.wait_event(splits)
+                        pending_dx.copy_(self.dx, non_blocking=True)
+                        dx_copied = after(down)
+                    down.wait_event(fwd_done)
+                    out_h.copy_(out, non_blocking=True)
+                    out_copied = after(down)
+                if i + 1 < n:
+                    upload(i + 1, gate=splits)   # slot (i+1) % 2 was last read by step i-1
+                if dx_copied is not None:
+                    cur.wait_event(dx_copied)       # the previous dx has left before it is rewritten
+                self.backward(dout)
+                pending_dx = dx_h
+            if pending_dx is not None:
+                with torch.cuda.stream(down):
+                    down.wait_stream(cur)
+                    pending_dx.copy_(self.dx, non_blocking=True)
+        finally:
+            self._mark_splits = False
         cur.wait_stream(down)
         cur.wait_stream(up)
         if not n:

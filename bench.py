@@ -510,6 +510,38 @@ def main():
     layer_roof_ms = max(flops_step / (pk["bf16_tflops_sustained"] * 1e12),
                         bytes_step / (pk["hbm_gbs"] * 1e9)) * 1e3
     sum_roof_ms = sum(v["roofline_ms"] * v["launches"] for v in kernels.values()) / args.steps
+
+    # load-balance metrics, loss and gradient on the same routing (not part of the
+    # headline step): K timed iterations with per-launch events, L2 flushed before each
+    lb_frac, lb_pmean, lb_stats = (torch.empty(cfg.E, device=dev), torch.empty(cfg.E, device=dev),
+                                   torch.empty(4, device=dev))
+    lb_ws = B.new_workspace(B.workspace_size(B.MOE_OP_LOAD_BALANCE, cfg.T, cfg.E, cfg.K), dev)
+    lb_dl = torch.zeros(cfg.T, cfg.E, device=dev)
+    for _ in range(3):
+        B.moe_load_balance(logits, layer.counts, cfg.K, ws=lb_ws, out=(lb_frac, lb_pmean, lb_stats))
+        B.moe_load_balance_backward(logits, lb_frac, 0.01, dlogits=lb_dl, accumulate=True)
+    torch.cuda.synchronize()
+    B.moe_profile_start(16 * args.steps + 16)
+    for _ in range(args.steps):
+        flush_l2()
+        B.moe_load_balance(logits, layer.counts, cfg.K, ws=lb_ws, out=(lb_frac, lb_pmean, lb_stats))
+        B.moe_load_balance_backward(logits, lb_frac, 0.01, dlogits=lb_dl, accumulate=True)
+    torch.cuda.synchronize()
+    lb_rec = {}
+    for n, kms in B.moe_profile_stop():
+        lb_rec.setdefault(n, []).append(kms)
+    TE = cfg.T * cfg.E
+    lb_bytes = {"load_balance": 4 * TE, "load_balance_final": 4 * 256 * cfg.E + 12 * cfg.E,
+                "load_balance_backward": 12 * TE + 4 * cfg.E}
+    load_balance = {"workload": "qwen3 routing, logits [8192,128] fp32", "kernels": {}}
+    for n, v in lb_rec.items():
+        avg = statistics.mean(v)
+        bw = lb_bytes.get(n, 0) / (avg * 1e-3) / 1e9
+        load_balance["kernels"][n] = {"launches": len(v), "avg_us": round(avg * 1e3, 2),
+                                      "bytes": lb_bytes.get(n, 0), "achieved_gbs": round(bw, 1),
+                                      "frac_hbm": round(bw / pk["hbm_gbs"], 4)}
+    load_balance["loss"] = float(lb_stats[0])
+    load_balance["max_over_uniform"] = float(lb_stats[1])
     clocks = sampler.stop() if sampler else None
 
     # end to end through the layer API with pinned host buffers
@@ -552,7 +584,7 @@ def main():
                        "layer_frac_of_roofline": layer_roof_ms / ms,
                        "sum_of_kernel_rooflines_ms": sum_roof_ms},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": len(records), "clocks": clocks,
+            "gpu_launches": len(records), "clocks": clocks, "load_balance": load_balance,
             "step_ms_min_max": [min(step_ms), max(step_ms)],
             "kernels": kernels, "device": torch.cuda.get_device_name(dev),
         }

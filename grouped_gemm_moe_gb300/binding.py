@@ -32,6 +32,7 @@ MOE_OP_BUILD_PERMUTATION = 1
 MOE_OP_EP_LAYOUT = 2
 MOE_OP_GROUPED_FFN = 3
 MOE_OP_GROUPED_FFN_BACKWARD = 4
+MOE_OP_LOAD_BALANCE = 5
 
 WORKSPACE_HEADER = 256
 
@@ -44,6 +45,8 @@ SIGNATURES = {
     "moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_route_topk": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_route_topk_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_load_balance": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_load_balance_backward": (_I, [_P, _P, _I, _I, ctypes.c_float, _I, _P, _P]),
     "moe_build_permutation": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_build_permutation_static": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_ep_layout": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -165,6 +168,43 @@ def moe_route_topk_backward(logits: Optional[torch.Tensor], topk_idx: torch.Tens
         _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(dtopk_w), T, E, K, int(renorm), _ptr(dl),
         _stream(topk_idx.device)))
     return dl
+
+
+def moe_load_balance(logits: torch.Tensor, counts: torch.Tensor, K: int,
+                     ws: Optional[torch.Tensor] = None, out=None):
+    """Load-balance metrics and loss: returns (load_frac [E], prob_mean [E], stats [4]) with
+    stats = (loss, E * max load_frac, empty experts, sum load_frac), all fp32 on device."""
+    _need(logits, torch.float32, 2, "logits")
+    _need(counts, torch.int32, 1, "counts")
+    T, E = logits.shape
+    dev = logits.device
+    if ws is None:
+        ws = new_workspace(workspace_size(MOE_OP_LOAD_BALANCE, T, E, K), dev)
+    if out is None:
+        out = (torch.empty(E, dtype=torch.float32, device=dev),
+               torch.empty(E, dtype=torch.float32, device=dev),
+               torch.empty(4, dtype=torch.float32, device=dev))
+    frac, pmean, stats = out
+    _check("moe_load_balance", load().moe_load_balance(
+        _ptr(logits), _ptr(counts), T, E, int(K), _ptr(frac), _ptr(pmean), _ptr(stats), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(dev)))
+    return frac, pmean, stats
+
+
+def moe_load_balance_backward(logits: torch.Tensor, load_frac: torch.Tensor, scale: float,
+                              dlogits: Optional[torch.Tensor] = None, accumulate: bool = True):
+    """scale * d(load-balance loss)/d(logits), added into dlogits (or written if accumulate is
+    False or dlogits is None)."""
+    _need(logits, torch.float32, 2, "logits")
+    _need(load_frac, torch.float32, 1, "load_frac")
+    T, E = logits.shape
+    if dlogits is None:
+        dlogits = torch.empty(T, E, dtype=torch.float32, device=logits.device)
+        accumulate = False
+    _check("moe_load_balance_backward", load().moe_load_balance_backward(
+        _ptr(logits), _ptr(load_frac), T, E, float(scale), 1 if accumulate else 0, _ptr(dlogits),
+        _stream(logits.device)))
+    return dlogits
 
 
 def moe_build_permutation(topk_idx: torch.Tensor, E: int, ws: Optional[torch.Tensor] = None,

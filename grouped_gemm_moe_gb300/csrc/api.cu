@@ -9,6 +9,7 @@ namespace moe {
 
 size_t permutation_workspace(long long TK, int E, int R);   // permute.cu
 size_t ffn_backward_scratch(long long M, int I);            // grouped_gemm.cu
+size_t load_balance_workspace(int E);                       // route.cu
 
 namespace {
 thread_local int g_last_cuda_error = 0;
@@ -90,6 +91,8 @@ extern "C" size_t moe_workspace_size(int op, int T, int E, int K, int R, int d, 
     case MOE_OP_GROUPED_FFN_BACKWARD:
       if (I < 1 || d < 1) return 0;
       return kWorkspaceHeader + ffn_backward_scratch(TK, I);
+    case MOE_OP_LOAD_BALANCE:
+      return load_balance_workspace(E);
     default:
       return 0;
   }

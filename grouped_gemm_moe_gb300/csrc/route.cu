@@ -8,6 +8,8 @@
 // keys followed by a warp-wide min over the ids that hold it: the larger logit
 // wins, equal logits go to the lower id. The softmax max is the round-0
 // winner. Backward: one warp per token.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -132,6 +134,198 @@ route_topk_backward_kernel(const float* __restrict__ logits, const int32_t* __re
   if (lane < K) out[id] = p_sel * (dw - s);
 }
 
+// ----------------------------------------------------------------- load balance
+// Partial sums of the router probabilities: CTA b (kLbBlocks of them, a fixed
+// count, so the summation order does not depend on the device) gives each of
+// its warps the tokens t = b*8 + w, + 8*kLbBlocks, ...; lane l accumulates
+// softmax(logits[t]) at its experts l, l+32, ... in registers; the warps'
+// sums are added in warp order into partial[b][e].
+constexpr int kLbBlocks = 256;
+
+template <int V>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+load_balance_partial_kernel(const float* __restrict__ logits, int T, int E,
+                            float* __restrict__ partial) {
+  pdl_enter();
+  __shared__ float sums[kWarpsPerBlock][32 * V];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  for (long long t = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + warp; t < T;
+       t += static_cast<long long>(gridDim.x) * kWarpsPerBlock) {
+    const float* row = logits + t * E;
+    float v[V];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+      mx = fmaxf(mx, v[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      v[i] = (lane + 32 * i < E) ? expf(v[i] - mx) : 0.f;
+      s += v[i];
+    }
+    s = warp_sum(s);
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] += v[i] / s;
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i) sums[warp][lane + 32 * i] = acc[i];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float tot = 0.f;
+    for (int w = 0; w < kWarpsPerBlock; ++w) tot += sums[w][e];
+    partial[static_cast<size_t>(blockIdx.x) * E + e] = tot;
+  }
+}
+
+// One CTA: P_e = (sum of the partials) / T, f_e = counts_e / TK, and the loss
+// and metrics. The G = 1024 / E threads of expert e (e = tid % E) each sum the
+// partials b = j, j + G, ... and the G sums are added in j order; the loss and
+// metrics use fixed-shape block reductions, so every sum has a fixed order.
+constexpr int kLbFinalThreads = 1024;
+
+__global__ void __launch_bounds__(kLbFinalThreads)
+load_balance_final_kernel(const float* __restrict__ partial, int nblk,
+                          const int32_t* __restrict__ counts, int T, int E, int K,
+                          float* __restrict__ load_frac, float* __restrict__ prob_mean,
+                          float* __restrict__ stats) {
+  pdl_enter();
+  __shared__ float part[kLbFinalThreads];
+  __shared__ float red[4][kLbFinalThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = kLbFinalThreads / E;   // >= 1 for E <= 1024
+  if (tid < G * E) {
+    const int e = tid % E, j = tid / E;
+    float tot = 0.f;
+    for (int b = j; b < nblk; b += G) tot += partial[static_cast<size_t>(b) * E + e];
+    part[j * E + e] = tot;
+  }
+  __syncthreads();
+  const float inv_t = 1.f / static_cast<float>(T);
+  const float inv_tk = 1.f / (static_cast<float>(T) * static_cast<float>(K));
+  float fp = 0.f, fmax = 0.f, nempty = 0.f, fsum = 0.f;
+  if (tid < E) {
+    const int e = tid;
+    float tot = 0.f;
+    for (int j = 0; j < G; ++j) tot += part[j * E + e];
+    const float P = tot * inv_t;
+    const int c = counts[e];
+    const float f = static_cast<float>(c) * inv_tk;
+    prob_mean[e] = P;
+    load_frac[e] = f;
+    fp = f * P;
+    fmax = f;
+    nempty = (c == 0) ? 1.f : 0.f;
+    fsum = f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    fp += __shfl_xor_sync(0xffffffffu, fp, o);
+    fmax = fmaxf(fmax, __shfl_xor_sync(0xffffffffu, fmax, o));
+    nempty += __shfl_xor_sync(0xffffffffu, nempty, o);
+    fsum += __shfl_xor_sync(0xffffffffu, fsum, o);
+  }
+  if (lane == 0) { red[0][warp] = fp; red[1][warp] = fmax; red[2][warp] = nempty; red[3][warp] = fsum; }
+  __syncthreads();
+  if (tid == 0) {
+    float a = 0.f, m = 0.f, n = 0.f, fs = 0.f;
+    for (int w = 0; w < kLbFinalThreads / 32; ++w) {
+      a += red[0][w];
+      m = fmaxf(m, red[1][w]);
+      n += red[2][w];
+      fs += red[3][w];
+    }
+    stats[0] = static_cast<float>(E) * a;
+    stats[1] = static_cast<float>(E) * m;
+    stats[2] = n;
+    stats[3] = fs;
+  }
+}
+
+// One warp per token: g[t,i] = scale * (E/T) * p_i * (f_i - sum_e f_e p_e).
+template <int V>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+load_balance_backward_kernel(const float* __restrict__ logits, const float* __restrict__ frac,
+                             int T, int E, float coef, int accumulate,
+                             float* __restrict__ dlogits) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* row = logits + t * E;
+  float v[V], f[V];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+    f[i] = (e < E) ? __ldg(frac + e) : 0.f;
+    mx = fmaxf(mx, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    v[i] = (lane + 32 * i < E) ? expf(v[i] - mx) : 0.f;
+    s += v[i];
+  }
+  s = warp_sum(s);
+  float fdot = 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    v[i] /= s;   // p_i
+    fdot += f[i] * v[i];
+  }
+  fdot = warp_sum(fdot);
+  float* out = dlogits + t * E;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float g = coef * v[i] * (f[i] - fdot);
+      out[e] = accumulate ? out[e] + g : g;
+    }
+  }
+}
+
+template <int V>
+struct LbLauncher {
+  static int run(const float* logits, const int32_t* counts, int T, int E, int K, float* frac,
+                 float* pmean, float* stats, float* partial, cudaStream_t st) {
+    const int nblk = static_cast<int>(
+        std::min<long long>(kLbBlocks, (static_cast<long long>(T) + kWarpsPerBlock - 1) / kWarpsPerBlock));
+    int rc;
+    {
+      ProfScope prof("load_balance", st);
+      rc = launch_pdl(load_balance_partial_kernel<V>, nblk, kWarpsPerBlock * 32, 0, st, 1, logits,
+                      T, E, partial);
+    }
+    if (rc) return rc;
+    ProfScope prof("load_balance_final", st);
+    return launch_pdl(load_balance_final_kernel, 1, kLbFinalThreads, 0, st, 1,
+                      static_cast<const float*>(partial), nblk, counts, T, E, K, frac, pmean, stats);
+  }
+};
+
+template <int V>
+struct LbBwdLauncher {
+  static int run(const float* logits, const float* frac, int T, int E, float coef, int accumulate,
+                 float* dl, cudaStream_t st) {
+    const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    ProfScope prof("load_balance_backward", st);
+    return launch_pdl(load_balance_backward_kernel<V>, blocks, kWarpsPerBlock * 32, 0, st, 1,
+                      logits, frac, T, E, coef, accumulate, dl);
+  }
+};
+
 template <template <int> class Launcher, typename... Args>
 int dispatch_v(int E, Args... args) {
   if (E <= 32) return Launcher<1>::run(args...);
@@ -190,4 +384,39 @@ extern "C" int moe_route_topk_backward(const float* logits, const int32_t* topk_
     return MOE_ERR_MISALIGNED;
   return dispatch_v<BwdLauncher>(E, logits, topk_idx, topk_w, dtopk_w, T, E, K, renorm, dlogits,
                                  as_stream(stream));
+}
+
+namespace moe {
+size_t load_balance_workspace(int E) {
+  if (E < 1 || E > 1024) return 0;
+  return kWorkspaceHeader + static_cast<size_t>(kLbBlocks) * E * sizeof(float);
+}
+}  // namespace moe
+
+extern "C" int moe_load_balance(const float* logits, const int32_t* counts, int T, int E, int K,
+                                float* load_frac, float* prob_mean, float* stats, void* ws,
+                                size_t ws_bytes, void* stream) {
+  using namespace moe;
+  if (T < 1 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E) return MOE_ERR_INVALID_ARG;
+  if (!logits || !counts || !load_frac || !prob_mean || !stats) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(counts) || !aligned16(load_frac) || !aligned16(prob_mean) ||
+      !aligned16(stats))
+    return MOE_ERR_MISALIGNED;
+  if (!ws || !aligned16(ws) || ws_bytes < load_balance_workspace(E)) return MOE_ERR_WORKSPACE;
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kWorkspaceHeader);
+  return dispatch_v<LbLauncher>(E, logits, counts, T, E, K, load_frac, prob_mean, stats, partial,
+                                as_stream(stream));
+}
+
+extern "C" int moe_load_balance_backward(const float* logits, const float* load_frac, int T, int E,
+                                         float scale, int accumulate, float* dlogits,
+                                         void* stream) {
+  using namespace moe;
+  if (T < 0 || E < 1 || E > 1024) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !load_frac || !dlogits) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(load_frac) || !aligned16(dlogits)) return MOE_ERR_MISALIGNED;
+  const float coef = scale * static_cast<float>(E) / static_cast<float>(T);
+  return dispatch_v<LbBwdLauncher>(E, logits, load_frac, T, E, coef, accumulate ? 1 : 0, dlogits,
+                                   as_stream(stream));
 }

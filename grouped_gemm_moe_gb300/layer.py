@@ -9,6 +9,11 @@ Forward:  moe_route_topk -> moe_build_permutation_ep (the permutation and
 Backward: moe_combine_backward -> moe_grouped_ffn_backward (routed; shared)
           -> moe_dispatch_backward -> moe_route_topk_backward.
 
+With aux_loss_coef > 0 the forward also runs moe_load_balance (per-expert load
+fractions, mean router probabilities, the load-balance loss and load metrics,
+in lb_frac / lb_pmean / lb_stats) and the backward adds aux_loss_coef times
+the loss's gradient into dlogits with moe_load_balance_backward.
+
 This module only allocates tensors and orders the calls; each step is a
 kernel of libmoe_gb300.so.
 """
@@ -24,7 +29,7 @@ from . import binding as B
 class MoELayer:
     def __init__(self, T: int, d: int, E: int, K: int, I: int, R: int,
                  weights: Dict[str, torch.Tensor], renorm: int = 1,
-                 device: Optional[torch.device] = None):
+                 device: Optional[torch.device] = None, aux_loss_coef: float = 0.0):
         self.T, self.d, self.E, self.K, self.I, self.R = T, d, E, K, I, R
         self.renorm = renorm
         dev = torch.device(device) if device is not None else weights["w_gate"].device
@@ -69,6 +74,10 @@ class MoELayer:
             self.ws_sfwd = B.new_workspace(B.workspace_size(B.MOE_OP_GROUPED_FFN, T, 1, 1, 1, d, Is), dev)
             self.ws_sbwd = B.new_workspace(
                 B.workspace_size(B.MOE_OP_GROUPED_FFN_BACKWARD, T, 1, 1, 1, d, Is), dev)
+        self.aux_loss_coef = float(aux_loss_coef)
+        if self.aux_loss_coef > 0:
+            self.lb_frac, self.lb_pmean, self.lb_stats = e(E, dt=f32), e(E, dt=f32), e(4, dt=f32)
+            self.ws_lb = B.new_workspace(B.workspace_size(B.MOE_OP_LOAD_BALANCE, T, E, K), dev)
         self.logits = None
         self.x = None
         self.timeline: Optional[List] = None   # when a list, (name, start_event, end_event) per call
@@ -107,6 +116,9 @@ class MoELayer:
                   host_splits=self.host_splits if copy_splits else False, ws=self.ws_ep,
                   out=(self.counts, self.offsets, self.perm, self.inv_perm, self.ep_splits,
                        self.send_index, self.a2a_index, self.regroup_index))
+        if self.aux_loss_coef > 0:
+            self._run("load_balance", B.moe_load_balance, logits, self.counts, K, ws=self.ws_lb,
+                      out=(self.lb_frac, self.lb_pmean, self.lb_stats))
         if self._mark_splits:   # the splits' device-to-host copy has been issued
             self.splits_issued = torch.cuda.Event()
             self.splits_issued.record(torch.cuda.current_stream(self.device))
@@ -140,6 +152,9 @@ class MoELayer:
         self._run("route_topk_backward", B.moe_route_topk_backward,
                   None if self.renorm else self.logits, self.topk_idx, self.topk_w, self.dtopk_w,
                   self.E, self.renorm, out=self.dlogits)
+        if self.aux_loss_coef > 0:
+            self._run("load_balance_backward", B.moe_load_balance_backward, self.logits,
+                      self.lb_frac, self.aux_loss_coef, dlogits=self.dlogits, accumulate=True)
         return self.dx
 
     def step_from_host(self, logits_h: torch.Tensor, x_h: torch.Tensor, dout_h: torch.Tensor,
@@ -276,8 +291,10 @@ class MoELayer:
         return 0
 
 
-def layer_from_config(cfg, inputs: Dict[str, torch.Tensor], device) -> MoELayer:
+def layer_from_config(cfg, inputs: Dict[str, torch.Tensor], device,
+                      aux_loss_coef: float = 0.0) -> MoELayer:
     """Copies a workload's weights to ``device`` and builds the layer."""
     keys = ["w_gate", "w_up", "w_down"] + (["ws_gate", "ws_up", "ws_down"] if cfg.shared_I else [])
     weights = {k: inputs[k].to(device).contiguous() for k in keys}
-    return MoELayer(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.R, weights, cfg.renorm, device)
+    return MoELayer(cfg.T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.R, weights, cfg.renorm, device,
+                    aux_loss_coef)

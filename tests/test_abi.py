@@ -107,6 +107,19 @@ def test_debug_wait_argument_checks(lib):
     assert lib.moe_debug_wait_timeout(MIS, 1000, None) == B.MOE_ERR_INVALID_ARG
 
 
+def test_argument_validation_load_balance(lib):
+    f = lib.moe_load_balance
+    assert f(FAKE, FAKE, 16, 8, 2, FAKE, FAKE, FAKE, FAKE, 0, None) == B.MOE_ERR_WORKSPACE
+    assert f(FAKE, FAKE, 0, 8, 2, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == B.MOE_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 16, 8, 9, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == B.MOE_ERR_INVALID_ARG
+    assert f(MIS, FAKE, 16, 8, 2, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == B.MOE_ERR_MISALIGNED
+    g = lib.moe_load_balance_backward
+    assert g(FAKE, FAKE, 16, 2048, 1.0, 1, FAKE, None) == B.MOE_ERR_INVALID_ARG
+    assert g(None, FAKE, 16, 8, 1.0, 1, FAKE, None) == B.MOE_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, 0, 8, 1.0, 1, FAKE, None) == B.MOE_OK
+    assert B.workspace_size(B.MOE_OP_LOAD_BALANCE, 8192, 128, 8) == B.WORKSPACE_HEADER + 256 * 128 * 4
+
+
 def test_workspace_sizes(lib):
     hdr = B.WORKSPACE_HEADER
     assert B.workspace_size(B.MOE_OP_GROUPED_FFN, 8192, 128, 8, 1, 2048, 768) == hdr

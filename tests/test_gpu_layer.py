@@ -71,6 +71,29 @@ def test_layer_forward_backward(cfg):
         assert_rms_close(f64(layer.dws_down[0]), rb["dws_down"], name="dws_down")
 
 
+@pytest.mark.parametrize("renorm", [1, 0])
+def test_layer_with_load_balance_loss(renorm):
+    """aux_loss_coef > 0: the forward's load metrics and loss match the oracle,
+    and dlogits is the router gradient plus coef times the loss's gradient."""
+    cfg = W.small_config("lb", T=512, d=128, E=16, K=4, I=128, R=4, skew=True, renorm=renorm)
+    inp = W.make_inputs(cfg, with_backward=True)
+    np_inp = {k: W.to_f64(v) for k, v in inp.items()}
+    coef = 0.01
+    layer = L.layer_from_config(cfg, inp, dev(), aux_loss_coef=coef)
+    layer.forward(inp["logits"].to(dev()), inp["x"].to(dev()))
+    layer.backward(inp["dout"].to(dev()))
+    torch.cuda.synchronize()
+    ref = O.layer_forward(np_inp, cfg.K, cfg.R, cfg.renorm, pre=True)
+    rb = O.layer_backward(np_inp, ref, np_inp["dout"], cfg.K, cfg.renorm, pre=True)
+    lb = O.load_balance(np_inp["logits"], ref["topk_idx"], cfg.E)
+    s = f64(layer.lb_stats)
+    assert abs(s[0] - lb["loss"]) <= 1e-5 * lb["loss"]
+    assert s[2] == lb["n_empty"]
+    np.testing.assert_allclose(f64(layer.lb_frac), lb["f"], rtol=1e-7, atol=0)
+    want = rb["dlogits"] + O.load_balance_backward(np_inp["logits"], lb["f"], scale=coef)
+    assert_rms_close(f64(layer.dlogits), want, name="dlogits with load-balance term")
+
+
 _COUNTER_C = r"""
 #include <dlfcn.h>
 #include <stddef.h>

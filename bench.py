@@ -13,6 +13,8 @@ combine, and the backward of each. Rank 0 prints one JSON line.
   on the launching stream; before every timed step, outside its events, L2 is
   flushed by writing a 256 MiB buffer and then reading another 256 MiB one (so
   no dirty flush lines are left for the step's first kernel to write back).
+* step_ms_median, step_ms_min_max, aa: the spread of the timed steps and the
+  same K steps timed again back to back (A/A noise floor).
 * e2e: the same metric through the layer API with pinned host buffers
   (MoELayer.run_from_host over the timed steps): each step copies logits, x
   and dout in and the output and input gradient out; step i+1's upload and
@@ -190,6 +192,10 @@ def kernel_work(name: str, cfg, shared: bool):
     }
     return 0, hbm.get(name, 0)
 
+
+# nominal GB300 figures (context beside the measured peaks): HBM3e and dense bf16
+NOMINAL_GBS = 7900.0
+NOMINAL_TFLOPS = 2250.0
 
 KERNEL_SOURCE = {"route": "route.cu", "perm": "permute.cu", "ep_": "permute.cu",
                  "dispatch": "gather.cu", "combine": "gather.cu", "gemm": "grouped_gemm.cu"}
@@ -460,6 +466,19 @@ def main():
     torch.cuda.synchronize()
     barrier()
     step_ms = [s.elapsed_time(e) for s, e in evs]
+    # A/A: the same K steps again, back to back, for the run-to-run noise floor
+    evs2 = []
+    for i in range(args.steps):
+        flush_l2()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        layer.forward(logits, x)
+        layer.backward(dout)
+        e.record(stream)
+        evs2.append((s, e))
+    torch.cuda.synchronize()
+    barrier()
+    step_ms_aa = [s.elapsed_time(e) for s, e in evs2]
     # per-kernel durations: the same K steps again, each library launch bracketed by
     # events on its stream (kept out of the pass above, where events between launches
     # would hold back each kernel's early launch behind its predecessor)
@@ -501,6 +520,8 @@ def main():
             "peak_source": pk["source"] + (" bf16 sustained" if rf["bound"] == "tensor"
                                            else " HBM copy (read+write)"),
             "traffic": measured_traffic(dom),
+            "frac_of_nominal": rf["achieved"] / (NOMINAL_TFLOPS if rf["bound"] == "tensor"
+                                                 else NOMINAL_GBS),
             "work_per_launch": {"flop": dfl, "bytes": dnb},
             "avg_launch_ms": davg}
     flops_step = sum(kernel_work(c["name"], cfg, c["shared"])[0] * c["launches"]
@@ -586,6 +607,10 @@ def main():
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": len(records), "clocks": clocks, "load_balance": load_balance,
             "step_ms_min_max": [min(step_ms), max(step_ms)],
+            "step_ms_median": statistics.median(step_ms),
+            "aa": {"ms_per_step": statistics.mean(step_ms_aa),
+                   "rel_diff": abs(statistics.mean(step_ms_aa) - statistics.mean(step_ms))
+                   / statistics.mean(step_ms)},
             "kernels": kernels, "device": torch.cuda.get_device_name(dev),
         }
         print(json.dumps(line), flush=True)

@@ -10,24 +10,34 @@
 // the FSDP2 backend" names a grouped_mm backend over expert-sorted rows; that
 // is prior art, this is an independent kernel.
 //
-// Kernel shape (one template, six problem kinds):
-//   * persistent: one CTA per SM, static round-robin over a tile list that
-//     every CTA derives on device from the expert offsets (no host sync);
+// Kernel shape (two templates, six problem kinds, all on CTA pairs):
+//   * every GEMM runs on clusters of two CTAs sharing one tcgen05 MMA of
+//     M = 256 (cta_group::2): each CTA stages its 128 rows of A and half of
+//     B's N, the leader issues the MMA, and each CTA's TMEM holds its own 128
+//     rows of the accumulator;
+//   * persistent: one cluster per SM pair, static round-robin over a tile list
+//     that every CTA derives on device from the expert offsets (no host sync);
 //   * 192 threads, warp-specialised: warp 0 issues TMA loads into a ring of
-//     shared-memory stages, warp 1 owns TMEM and issues tcgen05.mma (one
-//     thread), warps 2-5 drain the accumulator with tcgen05.ld and run the
-//     fused epilogue (SwiGLU, SwiGLU backward, bf16 or fp32 stores);
-//   * 128 x BN x 64 tiles, BN = 256 or 128, fp32 accumulators double-buffered
-//     in TMEM (2*BN columns) so the epilogue of tile i overlaps the MMAs of
-//     tile i+1;
+//     shared-memory stages (completing on the leader's barrier), warp 1 owns
+//     TMEM and, in the leader, issues tcgen05.mma (one thread), warps 2-5 drain
+//     the accumulator with tcgen05.ld and run the fused epilogue (SwiGLU,
+//     SwiGLU backward, bf16 or fp32 stores through TMA bulk tensor stores);
+//   * 256 x BN x 64 pair tiles (BN = 256 or 128 for the forward and
+//     input-gradient kinds, 256 for the weight gradients), fp32 accumulators
+//     double-buffered in TMEM so the epilogue of tile i overlaps the MMAs of
+//     tile i+1; the ring depth grows when the expert count leaves shared
+//     memory for it;
 //   * operands use the 128-byte swizzle. K-major tiles come from row-major
 //     activations and from the weights in the backward; MN-major tiles from
 //     the weights in the forward and from both operands of the weight
 //     gradients, so no operand is ever transposed in memory;
 //   * ragged segments: forward / input-gradient tiles start at an expert's
 //     first row and mask stores past its last row; the weight gradients run a
-//     ragged K loop over the expert's rows and zero the rows of the last
-//     k-block that belong to the next expert before the MMA reads them.
+//     ragged K loop over the expert's rows, issue only the K16 steps that hold
+//     valid rows and zero the rows of the one step that straddles the
+//     expert's end before the MMA reads them;
+//   * each GEMM waits on its producer through programmatic dependent launch
+//     before it reads the expert offsets;
 //   * every mbarrier wait is bounded (a few seconds of %globaltimer); on
 //     timeout the CTA records MOE_ERR_DEVICE_TIMEOUT in the workspace status
 //     word, drains its own TMA loads and MMAs, frees TMEM and exits.
@@ -142,35 +152,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Pulls a tile into L2 only (no shared-memory destination, no completion).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns: thread i gets row (lane base + i).
@@ -332,507 +318,6 @@ __device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const float (&v
   uint4* p = reinterpret_cast<uint4*>(dst);
   p[0] = a;
   p[1] = b;
-}
-
-__device__ __forceinline__ void load16_bf16(const __nv_bfloat16* src, float (&v)[16]) {
-  const uint4* p = reinterpret_cast<const uint4*>(src);
-  float f[8];
-  unpack8(p[0], f);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = f[i];
-  unpack8(p[1], f);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[8 + i] = f[i];
-}
-
-__device__ __forceinline__ void store16_f32(float* dst, const float (&v)[16]) {
-  float4* p = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-}
-
-// ----------------------------------------------------------------- tiles
-struct Tile {
-  int e;        // expert
-  int row0;     // first packed row (forward / input gradients) or first k row (weight grads)
-  int rows;     // valid rows (forward / input gradients) or K rows (weight grads)
-  int m0;       // weight gradients: first output row
-  int n0;       // first output column (in the kind's N space)
-  int nkb;      // k-blocks
-};
-
-template <int KIND, int BN>
-__device__ __forceinline__ Tile decode_tile(int t, const Params& p, const int* s_off,
-                                            const int* s_mt) {
-  Tile tl;
-  if constexpr (KIND == WGRAD_GU || KIND == WGRAD_D) {
-    const int per_e = p.m_tiles * p.n_tiles;
-    tl.e = t / per_e;
-    const int rem = t - tl.e * per_e;
-    const int mt = rem / p.n_tiles;
-    const int nt = rem - mt * p.n_tiles;
-    tl.m0 = mt * BM;
-    tl.n0 = nt * BN;
-    tl.row0 = s_off[tl.e];
-    tl.rows = s_off[tl.e + 1] - tl.row0;
-    tl.nkb = (tl.rows + BK - 1) / BK;
-  } else {
-    const int mg = t / p.n_tiles;
-    const int nt = t - mg * p.n_tiles;
-    int lo = 0, hi = p.E - 1;   // largest e with s_mt[e] <= mg
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_mt[mid] <= mg) lo = mid; else hi = mid - 1;
-    }
-    tl.e = lo;
-    tl.row0 = s_off[lo] + (mg - s_mt[lo]) * BM;
-    tl.rows = min(BM, s_off[lo + 1] - tl.row0);
-    tl.m0 = 0;
-    tl.n0 = nt * (KIND == FWD_GATEUP ? BN / 2 : BN);
-    tl.nkb = p.k_blocks;
-  }
-  return tl;
-}
-
-// ----------------------------------------------------------------- kernel
-// The TMA boxes of one k-block of a tile: loaded into a pipeline stage
-// (PREFETCH = false) or only pulled into L2 (PREFETCH = true; measured slower
-// on the qwen3 workload when issued 8 k-blocks ahead, so the kernels do not use it).
-template <int KIND, int BN, bool PREFETCH>
-__device__ __forceinline__ void issue_kblock(const Tile& tl, int kb, const Params& p,
-                                             const CUtensorMap* tmA, const CUtensorMap* tmB0,
-                                             const CUtensorMap* tmB1, uint32_t sa, uint32_t sb,
-                                             uint32_t fb) {
-  constexpr uint32_t MN_ATOM = 64 * 128;
-  auto box = [&](const CUtensorMap* m, uint32_t dst, int x, int y) {
-    if constexpr (PREFETCH) tma_prefetch_2d(m, x, y);
-    else tma_load_2d(dst, m, fb, x, y);
-  };
-  if constexpr (KIND == FWD_GATEUP) {
-    box(tmA, sa, kb * BK, tl.row0);
-    const int yb = tl.e * p.d + kb * BK;
-#pragma unroll
-    for (int i = 0; i < BN / 128; ++i) {
-      box(tmB0, sb + i * MN_ATOM, tl.n0 + 64 * i, yb);
-      box(tmB1, sb + (BN / 128 + i) * MN_ATOM, tl.n0 + 64 * i, yb);
-    }
-  } else if constexpr (KIND == FWD_DOWN) {
-    box(tmA, sa, kb * BK, tl.row0);
-    const int yb = tl.e * p.I + kb * BK;
-#pragma unroll
-    for (int i = 0; i < BN / 64; ++i) box(tmB0, sb + i * MN_ATOM, tl.n0 + 64 * i, yb);
-  } else if constexpr (KIND == BWD_DH) {
-    box(tmA, sa, kb * BK, tl.row0);
-    box(tmB0, sb, kb * BK, tl.e * p.I + tl.n0);
-  } else if constexpr (KIND == BWD_DX) {
-    box(tmA, sa, kb * BK, tl.row0);
-    const int kx = kb * BK;
-    if (kx < p.I) box(tmB0, sb, kx, tl.e * p.d + tl.n0);
-    else box(tmB1, sb, kx - p.I, tl.e * p.d + tl.n0);
-  } else {  // weight gradients: both operands MN-major, K = token rows
-    const int ky = tl.row0 + kb * BK;
-    box(tmA, sa, tl.m0, ky);
-    box(tmA, sa + MN_ATOM, tl.m0 + 64, ky);
-#pragma unroll
-    for (int i = 0; i < BN / 64; ++i) box(tmB0, sb + i * MN_ATOM, tl.n0 + 64 * i, ky);
-  }
-}
-
-// Walks this CTA's (tile, k-block) sequence in the order the MMA consumes it,
-// skipping tiles without k-blocks.
-template <int KIND, int BN>
-struct KStream {
-  int t, kb, total;
-  bool valid;
-  Tile tl;
-  __device__ __forceinline__ void settle(const Params& p, const int* s_off, const int* s_mt) {
-    while (t < total) {
-      tl = decode_tile<KIND, BN>(t, p, s_off, s_mt);
-      if (tl.nkb > 0) break;
-      t += gridDim.x;
-    }
-    valid = t < total;
-  }
-  __device__ __forceinline__ void start(int t0, int tot, const Params& p, const int* s_off,
-                                        const int* s_mt) {
-    t = t0;
-    kb = 0;
-    total = tot;
-    settle(p, s_off, s_mt);
-  }
-  __device__ __forceinline__ void next(const Params& p, const int* s_off, const int* s_mt) {
-    if (++kb < tl.nkb) return;
-    kb = 0;
-    t += gridDim.x;
-    settle(p, s_off, s_mt);
-  }
-};
-
-// Epilogue shared memory per kind: weight gradients stage one [32 rows x 32 fp32]
-// block per epilogue warp for a bulk tensor store; gemm_dh prefetches, per
-// epilogue warp, the saved G and U of 32 rows x 128 columns (four [32 x 64]
-// bf16 boxes) for the tile it is about to drain.
-template <int KIND>
-__host__ __device__ constexpr uint32_t epi_bytes() {
-  return (KIND == WGRAD_GU || KIND == WGRAD_D) ? 4u * 4096u : (KIND == BWD_DH ? 4u * 16384u : 0u);
-}
-
-template <int KIND, int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
-                    const __grid_constant__ CUtensorMap tmC1, const Params p) {
-  constexpr bool kWgrad = (KIND == WGRAD_GU || KIND == WGRAD_D);
-  constexpr bool A_MN = kWgrad;
-  constexpr bool B_MN = (KIND == FWD_GATEUP || KIND == FWD_DOWN || kWgrad);
-  constexpr uint32_t A_BYTES = BM * BK * 2;
-  constexpr uint32_t B_BYTES = BN * BK * 2;
-  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr uint32_t TMEM_COLS = 2 * BN;
-  constexpr uint32_t IDESC = make_idesc<BN, A_MN, B_MN>();
-  constexpr uint32_t MN_ATOM = 64 * 128;   // one [64 rows x 128 B] TMA box
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* epi = smem + STAGES * STAGE_BYTES;            // epilogue region (epi_bytes)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + epi_bytes<KIND>());
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, aux[4]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
-  int* s_mt = s_off + (p.E + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t smem_base = smem_u32(smem);
-  const uint32_t bar_base = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar_base + 8u * s; };
-  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
-  auto aux_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + 5 + w); };
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 4); }
-    mbar_init(drain_bar, 1);
-    for (int w = 0; w < 4; ++w) mbar_init(aux_bar(w), 1);
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB0)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB1)) : "memory");
-    if constexpr (epi_bytes<KIND>() != 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC1)) : "memory");
-    }
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  pdl_wait();   // offsets and operands come from earlier launches
-  pdl_launch_dependents();
-  for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
-  __syncthreads();
-  if constexpr (!kWgrad) {
-    // exclusive prefix of per-expert m-tile counts (warp 0)
-    if (warp == 0) {
-      int carry = 0;
-      for (int base = 0; base <= p.E; base += 32) {
-        const int i = base + lane;
-        const int v = (i < p.E) ? (s_off[i + 1] - s_off[i] + BM - 1) / BM : 0;
-        int x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        if (i <= p.E) s_mt[i] = carry + x - v;
-        carry += __shfl_sync(0xffffffffu, x, 31);
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const int total = kWgrad ? p.E * p.m_tiles * p.n_tiles : s_mt[p.E] * p.n_tiles;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued[STAGES];
-#pragma unroll
-      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
-      KStream<KIND, BN> ld;
-      ld.start(blockIdx.x, total, p, s_off, s_mt);
-      while (ld.valid) {
-        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) break;
-        const uint32_t fb = full_bar(stage);
-        mbar_expect_tx(fb, STAGE_BYTES);
-        const uint32_t sa = smem_base + stage * STAGE_BYTES;
-        issue_kblock<KIND, BN, false>(ld.tl, ld.kb, p, &tmA, &tmB0, &tmB1, sa, sa + A_BYTES, fb);
-        issued[stage] += 1;
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        ld.next(p, s_off, s_mt);
-      }
-      // make sure no TMA write into this CTA's shared memory is still in flight
-      for (int s = 0; s < STAGES; ++s) {
-        if (!issued[s]) continue;
-        const uint32_t par = (issued[s] - 1u) & 1u;
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try(full_bar(s), par) && globaltimer() - t0 < kTimeoutNs) {
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = decode_tile<KIND, BN>(t, p, s_off, s_mt);
-      if (tl.nkb == 0) continue;
-      if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      for (int kb = 0; kb < tl.nkb; ++kb) {
-        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
-        const uint32_t sa = smem_base + stage * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
-        if constexpr (kWgrad) {
-          const int kvalid = tl.rows - kb * BK;
-          if (kvalid < BK) {
-            // rows [kvalid, 64) of this k-block belong to the next expert: zero them in A
-            uint8_t* a_gen = smem + stage * STAGE_BYTES;
-            const int first = kvalid * 128;
-            for (int off = first + lane * 16; off < static_cast<int>(MN_ATOM); off += 32 * 16) {
-              *reinterpret_cast<uint4*>(a_gen + off) = make_uint4(0, 0, 0, 0);
-              *reinterpret_cast<uint4*>(a_gen + MN_ATOM + off) = make_uint4(0, 0, 0, 0);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-          }
-        }
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            uint64_t ad, bd;
-            if constexpr (A_MN) ad = smem_desc(sa + kk * 2048, MN_ATOM, 1024);
-            else ad = smem_desc(sa + kk * 32, 16, 1024);
-            if constexpr (B_MN) bd = smem_desc(sb + kk * 2048, MN_ATOM, 1024);
-            else bd = smem_desc(sb + kk * 32, 16, 1024);
-            tc_mma(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit(empty_bar(stage));
-        }
-        __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-      }
-      if (!ok) break;
-      if (lane == 0) tc_commit(tfull_bar(acc));
-      __syncwarp();
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    }
-    // all MMAs issued by this CTA complete before TMEM is released
-    if (lane == 0) {
-      tc_commit(drain_bar);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try(drain_bar, 0) && globaltimer() - t0 < kTimeoutNs) {
-      }
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                  // TMEM lane quarter of this warp
-    const int ew = warp - 2;                 // epilogue warp index (its shared-memory slot)
-    const int r = q * 32 + lane;             // accumulator row of this thread
-    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    uint32_t aux_phase = 0;
-    bool aux_pending = false;                // a G/U prefetch was requested and not yet waited for
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile<KIND, BN>(t, p, s_off, s_mt);
-      if constexpr (kWgrad) {
-        // fp32 weight gradient of rows [m0 + 32q, +32) x [n0, n0 + BN): staged per 32 columns
-        // in a 128-byte-swizzled [32 x 32] block and written by a bulk tensor store.
-        uint8_t* stg = epi + ew * 4096;
-        const uint32_t stg_addr = smem_u32(stg);
-        const bool empty = (tl.nkb == 0);    // expert without rows: its gradient is zero
-        if (!empty) {
-          if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
-          tc_fence_after();
-        }
-        const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
-        const int mrow = tl.m0 + q * 32;
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          if (!empty) {
-            tmem_ld32(tacc + c, v);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          }
-          if (lane == 0) bulk_wait_read_all();     // the previous store has read the block
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float4* dst = reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4));
-            *dst = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) {
-            const int n = tl.n0 + c;
-            if constexpr (KIND == WGRAD_GU) {
-              if (n < p.I) tma_store_2d(&tmC0, stg_addr, n, tl.e * p.d + mrow);
-              else tma_store_2d(&tmC1, stg_addr, n - p.I, tl.e * p.d + mrow);
-            } else {
-              tma_store_2d(&tmC0, stg_addr, n, tl.e * p.I + mrow);
-            }
-            bulk_commit();
-          }
-        }
-        if (empty) continue;
-      } else if constexpr (KIND == BWD_DH) {
-        // Saved G and U for this warp's 32 rows arrive by TMA in 128-column passes;
-        // the first pass is requested before the accumulator is ready.
-        uint8_t* aux = epi + ew * 16384;     // boxes: G[c0, +64), G[c0+64, +64), U.., U..
-        const uint32_t aux_addr = smem_u32(aux);
-        const uint32_t ab = aux_bar(ew);
-        const int grow0 = tl.row0 + q * 32;
-        auto request = [&](int c0) {
-          if (lane == 0) {
-            mbar_expect_tx(ab, 16384);
-            tma_load_2d(aux_addr, &tmC0, ab, tl.n0 + c0, grow0);
-            tma_load_2d(aux_addr + 4096, &tmC0, ab, tl.n0 + c0 + 64, grow0);
-            tma_load_2d(aux_addr + 8192, &tmC0, ab, p.I + tl.n0 + c0, grow0);
-            tma_load_2d(aux_addr + 12288, &tmC0, ab, p.I + tl.n0 + c0 + 64, grow0);
-          }
-          aux_pending = true;
-        };
-        request(0);
-        if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
-        const bool valid = r < tl.rows;
-        const size_t grow = static_cast<size_t>(tl.row0 + r);
-        bool ok = true;
-        for (int c0 = 0; c0 < BN; c0 += 128) {
-          if (c0) request(c0);
-          if (!mbar_wait(ab, aux_phase, abort_flag, p.status)) { ok = false; break; }
-          aux_phase ^= 1u;
-          aux_pending = false;
-          for (int c = 0; c < 128; c += 16) {
-            float dh[16];
-            tmem_ld16(tacc + c0 + c, dh);
-            tmem_wait_ld();
-            // this row's 16 columns: two 16-byte chunks of a 128-byte-swizzled box row
-            const int box = c >> 6;
-            const int j0 = (c & 63) >> 3;
-            float g[16], u[16];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int off = lane * 128 + (((j0 + hh) ^ (lane & 7)) << 4);
-              float f[8];
-              unpack8(*reinterpret_cast<const uint4*>(aux + box * 4096 + off), f);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) g[8 * hh + i] = f[i];
-              unpack8(*reinterpret_cast<const uint4*>(aux + 8192 + box * 4096 + off), f);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) u[8 * hh + i] = f[i];
-            }
-            if (valid) {
-              float dg[16], du[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float s = __fdividef(1.f, 1.f + __expf(-g[i]));
-                dg[i] = dh[i] * u[i] * s * (1.f + g[i] * (1.f - s));
-                du[i] = dh[i] * g[i] * s;
-              }
-              __nv_bfloat16* orow = p.out + grow * (2 * p.I);
-              store16_bf16(orow + tl.n0 + c0 + c, dg);
-              store16_bf16(orow + p.I + tl.n0 + c0 + c, du);
-            }
-          }
-          fence_proxy_async();    // reads of this pass's boxes before the next TMA write
-          __syncwarp();
-        }
-        if (!ok) break;
-      } else {
-        if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
-        const bool valid = r < tl.rows;
-        const size_t grow = static_cast<size_t>(tl.row0 + r);
-        if constexpr (KIND == FWD_GATEUP) {
-          constexpr int HALF = BN / 2;
-          for (int c = 0; c < HALF; c += 16) {
-            float g[16], u[16], h[16];
-            tmem_ld16(tacc + c, g);
-            tmem_ld16(tacc + HALF + c, u);
-            tmem_wait_ld();
-            if (valid) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) h[i] = silu_f(g[i]) * u[i];
-              store16_bf16(p.out + grow * p.I + tl.n0 + c, h);
-              if (p.out2) {
-                store16_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c, g);
-                store16_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c, u);
-              }
-            }
-          }
-        } else {  // FWD_DOWN, BWD_DX: bf16 store
-          for (int c = 0; c < BN; c += 16) {
-            float v[16];
-            tmem_ld16(tacc + c, v);
-            tmem_wait_ld();
-            if (valid) store16_bf16(p.out + grow * p.ld_out + tl.n0 + c, v);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    }
-    if constexpr (kWgrad) {
-      if (lane == 0) bulk_wait_all();        // stores done before the CTA's shared memory goes
-      __syncwarp();
-    }
-    if constexpr (KIND == BWD_DH) {
-      // a prefetch still in flight because the loop stopped early: let it land (bounded)
-      if (lane == 0 && aux_pending) {
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try(aux_bar(ew), aux_phase) && globaltimer() - t0 < kTimeoutNs) {
-        }
-      }
-      __syncwarp();
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(TMEM_COLS)
-                 : "memory");
-  }
 }
 
 // ----------------------------------------------------------------- CTA-pair kernel
@@ -1577,6 +1062,7 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
         tc_fence_after();
       }
       const bool in_range = tl.m0 < mdim;   // false only for the follower past an odd M extent
+      const int ncols = (KIND == WGRAD_GU) ? 2 * p.I : p.d;
       const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
       const int mrow = tl.m0 + q * 32;
       for (int c = 0; c < BN; c += 32) {
@@ -1588,7 +1074,7 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        if (!in_range) continue;
+        if (!in_range || tl.n0 + c >= ncols) continue;   // past the M or N extent: not stored
         uint8_t* stg = epi + ew * 8192 + buf * 4096;
         if (lane == 0) bulk_wait_read_1();   // the store that last used this block has read it
         __syncwarp();
@@ -1679,36 +1165,6 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
             const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int KIND, int BN, int STAGES>
-size_t smem_bytes(int E) {
-  return 1024 + STAGES * (BM * BK * 2 + BN * BK * 2) + epi_bytes<KIND>() + 8 * (2 * STAGES + 9) +
-         16 + sizeof(int) * 2 * (E + 1) + 16;
-}
-
-template <int KIND, int BN, int STAGES>
-int launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-           const CUtensorMap& c0, const CUtensorMap& c1, const Params& p, long long tiles_upper,
-           cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<KIND, BN, STAGES>;
-  const size_t sm = smem_bytes<KIND, BN, STAGES>(p.E);
-  static thread_local int configured = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes<KIND, BN, STAGES>(1024)));
-    if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
-    configured = dev;
-  }
-  long long grid = num_sms();
-  if (tiles_upper < grid) grid = tiles_upper;
-  if (grid < 1) return MOE_OK;
-  static const char* kNames[] = {"gemm_gate_up", "gemm_down", "gemm_dh", "gemm_dx",
-                                 "gemm_wgrad_gate_up", "gemm_wgrad_down"};
-  ProfScope prof(kNames[KIND], st);
-  return launch_pdl(kern, static_cast<unsigned>(grid), kThreads, sm, st, 1, a, b0, b1, c0, c1, p);
 }
 
 #ifndef MOE_PAIR_BN_MAX
@@ -1865,25 +1321,6 @@ int launch_pair_bn(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CU
 inline int pair_bn(int n) { return (n % 256 == 0 && MOE_PAIR_BN_MAX >= 256) ? 256 : 128; }
 
 
-// Pipeline depth: as many operand stages as fit next to the kind's epilogue buffers
-// (227 KB of shared memory per CTA, expert tables for up to 1024 experts included).
-template <int KIND, int BN>
-constexpr int stages_for() {
-  return (KIND == BWD_DH) ? (BN == 256 ? 3 : 4) : (BN == 256 ? 4 : 6);
-}
-
-template <int KIND>
-int launch_bn(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-              const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
-              long long tiles_upper, cudaStream_t st) {
-  if (bn == 256)
-    return launch<KIND, 256, stages_for<KIND, 256>()>(a, b0, b1, c0, c1, p, tiles_upper, st);
-  return launch<KIND, 128, stages_for<KIND, 128>()>(a, b0, b1, c0, c1, p, tiles_upper, st);
-}
-
-static_assert(1024 + 3 * (16384 + 32768) + 65536 + 8 * 15 + 32 + 8 * 1025 <= 232448, "dh smem");
-static_assert(1024 + 4 * (16384 + 32768) + 16384 + 8 * 17 + 32 + 8 * 1025 <= 232448, "wgrad smem");
-
 }  // namespace gemm
 
 size_t ffn_backward_scratch(long long M, int I) {
@@ -2038,22 +1475,17 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   rc = launch_pair_wgrad<WGRAD_GU>(ta, tb0, tc0, tc1, p,
                                    static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
   if (rc) return rc;
-  // dWd = H^T dY: CTA pairs when d is a multiple of 256, else single-CTA 128 x 128 tiles
+  // dWd = H^T dY on CTA pairs (when d is an odd multiple of 128 the last n-tile's
+  // upper half reads the TMA fill value past column d and stores nothing)
   if (!make_map(&ta, h, I, M, 64, 64) || !make_map(&tb0, dy, d, M, 64, 64) ||
       !make_map(&tc0, dw_down, d, static_cast<uint64_t>(E) * I, 32, 32, true))
     return MOE_ERR_CUDA;
   p.outf0 = dw_down;
   p.outf1 = nullptr;
-  if (d % 256 == 0) {
-    p.m_tiles = (I + 2 * BM - 1) / (2 * BM);
-    p.n_tiles = d / 256;
-    return launch_pair_wgrad<WGRAD_D>(ta, tb0, tc0, tc0, p,
-                                      static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
-  }
-  p.m_tiles = I / BM;
-  p.n_tiles = d / 128;
-  return launch_bn<WGRAD_D>(128, ta, tb0, tb0, tc0, tc0, p,
-                            static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
+  p.m_tiles = (I + 2 * BM - 1) / (2 * BM);
+  p.n_tiles = (d + 255) / 256;
+  return launch_pair_wgrad<WGRAD_D>(ta, tb0, tc0, tc0, p,
+                                    static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
 }
 
 extern "C" int moe_debug_wait_timeout(void* ws, int timeout_us, void* stream) {

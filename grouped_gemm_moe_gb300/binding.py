@@ -53,6 +53,7 @@ SIGNATURES = {
     "moe_build_permutation_ep": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                       _SZ, _P]),
     "moe_dispatch": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_dispatch_scatter": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_ffn": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                       _P, _P, _P, _SZ, _P]),
@@ -317,6 +318,18 @@ def moe_dispatch(x: torch.Tensor, perm: torch.Tensor, K: int, out: Optional[torc
     xp = out if out is not None else torch.empty(T * K, d, dtype=torch.bfloat16, device=x.device)
     _check("moe_dispatch", load().moe_dispatch(_ptr(x), T, d, K, _ptr(perm), _ptr(xp),
                                                _stream(x.device)))
+    return xp
+
+
+def moe_dispatch_scatter(x: torch.Tensor, inv_perm: torch.Tensor, K: int,
+                         out: Optional[torch.Tensor] = None):
+    """The same xp as moe_dispatch, token-major through inv_perm."""
+    _need(x, torch.bfloat16, 2, "x")
+    _need(inv_perm, torch.int32, 1, "inv_perm")
+    T, d = x.shape
+    xp = out if out is not None else torch.empty(T * K, d, dtype=torch.bfloat16, device=x.device)
+    _check("moe_dispatch_scatter", load().moe_dispatch_scatter(_ptr(x), T, d, K, _ptr(inv_perm),
+                                                               _ptr(xp), _stream(x.device)))
     return xp
 
 

@@ -10,11 +10,12 @@
 // drafters on the FSDP2 backend", "What this adds" (shared expert added on
 // the local tokens).
 //
-// All four kernels are HBM-bound row moves: 16-byte vector loads and stores,
-// rows of d bf16 = d/8 vectors. Dispatch and the two token-major reductions
-// map one thread to one 16-byte vector of an output row, so a warp touches 512
-// contiguous bytes; each thread of the reductions issues its K independent
-// gathered loads before it accumulates (fp32, slot order, no atomics).
+// All kernels are HBM-bound row moves: 16-byte vector loads and stores, rows
+// of d bf16 = d/8 vectors. The token-major kernels (dispatch by inv_perm, the
+// two reductions) map one thread to one 16-byte vector of a token's row, so a
+// warp touches 512 contiguous bytes; each thread of the reductions issues its
+// K independent gathered loads before it accumulates (fp32, slot order, no
+// atomics). Dispatch by perm moves whole packed rows on the bulk-copy engine.
 #include <algorithm>
 
 #include "common.cuh"
@@ -24,9 +25,9 @@ namespace {
 
 constexpr int kThreads = 256;
 
-int grid_for(long long work, int per_block) {
+int grid_for(long long work, int per_block, int blocks_per_sm = 16) {
   long long b = (work + per_block - 1) / per_block;
-  const long long cap = static_cast<long long>(num_sms()) * 16;
+  const long long cap = static_cast<long long>(num_sms()) * blocks_per_sm;
   if (b > cap) b = cap;
   if (b < 1) b = 1;
   return static_cast<int>(b);
@@ -140,6 +141,35 @@ dispatch_bulk_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ 
     bulk_bar_wait(bar_addr + 8 * static_cast<int>(r % kBulkSlots),
                   static_cast<uint32_t>((r / kBulkSlots) & 1));
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// xp[inv_perm[a]] = x[a / K] for every assignment a = t*K + j: the rows of the
+// gather above, moved token-major. One thread per 16-byte vector of a token's
+// row loads it once (a warp reads 512 contiguous bytes of x) and stores it into
+// the token's K packed rows; the K positions are loaded first so the K stores
+// issue back to back. x is read from HBM once instead of once per assignment,
+// and within each expert's segment the stores advance row by row (a segment
+// lists its tokens in ascending order).
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads)
+dispatch_scatter_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_perm, int K,
+                        int nv, long long total, uint4* __restrict__ xp) {
+  pdl_enter();
+  const long long stride = static_cast<long long>(gridDim.x) * kThreads;
+  for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+       i += stride) {
+    const long long t = i / nv;
+    const int c = static_cast<int>(i - t * nv);
+    const int32_t* ip = inv_perm + t * K;
+    int32_t pos[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < K) pos[j] = __ldg(ip + j);
+    const uint4 v = ldg_nc_v4(x + i);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < K) stg_v4(xp + static_cast<long long>(pos[j]) * nv + c, v);
+  }
 }
 
 // out[t] = bf16( sum_j w[t,j] * rows[inv_perm[t*K+j]] + extra[t] ); w == nullptr means 1.
@@ -257,6 +287,26 @@ int launch_gather_sum(const void* rows, const float* w, const int32_t* inv_perm,
   return go(gather_sum_kernel<32>);
 }
 
+int launch_dispatch_scatter(const void* x, const int32_t* inv_perm, int T, int K, int d, void* xp,
+                            cudaStream_t st) {
+  const int nv = d / 8;
+  const long long total = static_cast<long long>(T) * nv;
+  // 32 blocks per SM of grid-stride work: measured ~5% faster than 8 or 16 on
+  // the qwen3 shape (more stores in flight per SM)
+  const int grid = grid_for(total, kThreads, 32);
+  auto xi = static_cast<const uint4*>(x);
+  auto o = static_cast<uint4*>(xp);
+  ProfScope prof("dispatch", st);
+  auto go = [&](auto kern) {
+    return launch_pdl(kern, grid, kThreads, 0, st, 1, xi, inv_perm, K, nv, total, o);
+  };
+  if (K <= 2) return go(dispatch_scatter_kernel<2>);
+  if (K <= 4) return go(dispatch_scatter_kernel<4>);
+  if (K <= 8) return go(dispatch_scatter_kernel<8>);
+  if (K <= 16) return go(dispatch_scatter_kernel<16>);
+  return go(dispatch_scatter_kernel<32>);
+}
+
 bool shape_ok(int T, int K, int d) { return T >= 0 && K >= 1 && K <= 32 && d > 0 && d % 8 == 0; }
 
 }  // namespace
@@ -296,6 +346,16 @@ extern "C" int moe_dispatch(const moe_bf16* x, int T, int d, int K, const int32_
   ProfScope prof("dispatch", st);
   return launch_pdl(dispatch_kernel, grid, kThreads, 0, st, 1, reinterpret_cast<const uint4*>(x),
                     perm, K, nv, rows, reinterpret_cast<uint4*>(xp));
+}
+
+extern "C" int moe_dispatch_scatter(const moe_bf16* x, int T, int d, int K,
+                                    const int32_t* inv_perm, moe_bf16* xp, void* stream) {
+  using namespace moe;
+  if (!shape_ok(T, K, d)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !inv_perm || !xp) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(inv_perm) || !aligned16(xp)) return MOE_ERR_MISALIGNED;
+  return launch_dispatch_scatter(x, inv_perm, T, K, d, xp, as_stream(stream));
 }
 
 extern "C" int moe_combine(const moe_bf16* y, const float* topk_w, const int32_t* inv_perm, int T,

@@ -3,7 +3,7 @@ library calls on the current CUDA stream with every buffer preallocated.
 
 Forward:  moe_route_topk -> moe_build_permutation_ep (the permutation and
           the simulated expert-parallel layout from one pass, with the one
-          device-to-host copy of the splits) -> moe_dispatch ->
+          device-to-host copy of the splits) -> moe_dispatch_scatter ->
           moe_grouped_ffn (routed experts; shared experts as E=1 on x) ->
           moe_combine.
 Backward: moe_combine_backward -> moe_grouped_ffn_backward (routed; shared)
@@ -122,7 +122,7 @@ class MoELayer:
         if self._mark_splits:   # the splits' device-to-host copy has been issued
             self.splits_issued = torch.cuda.Event()
             self.splits_issued.record(torch.cuda.current_stream(self.device))
-        self._run("dispatch", B.moe_dispatch, x, self.perm, K, out=self.xp)
+        self._run("dispatch", B.moe_dispatch_scatter, x, self.inv_perm, K, out=self.xp)
         self._run("grouped_ffn", B.moe_grouped_ffn, self.xp, self.offsets, w["w_gate"], w["w_up"],
                   w["w_down"], ws=self.ws_ffn, out=(self.y, self.h, self.gu))
         shared_y = None

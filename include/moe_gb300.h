@@ -220,6 +220,17 @@ int moe_build_permutation_ep(const int32_t* topk_idx, int T, int E, int K, int R
 int moe_dispatch(const moe_bf16* x, int T, int d, int K, const int32_t* perm,
                  moe_bf16* xp, void* stream);
 
+/* A5, token-major form: the same xp as moe_dispatch, written as
+ * xp[inv_perm[t*K + j]] = x[t] for every token t and slot j < K (inv_perm is
+ * the inverse of perm, as returned by moe_build_permutation). Each row of x is
+ * read once and stored K times, so the call moves 2*T*d*(1+K) bytes of rows
+ * with no re-reads of x.
+ *   x [T,d] bf16 in, inv_perm [TK] int32 in (a permutation of 0..TK-1;
+ *   other values are out of contract and write out of bounds), xp [TK,d]
+ *   bf16 out. d % 8 == 0, 1 <= K <= 32. Errors as moe_dispatch. */
+int moe_dispatch_scatter(const moe_bf16* x, int T, int d, int K, const int32_t* inv_perm,
+                         moe_bf16* xp, void* stream);
+
 /* A6. Grouped SwiGLU experts ([TAS] "Mapping experts to EP ranks": stacked
  * W_gate [E,d,I], W_val [E,d,I], W_out [E,I,d]; "Dispatch, expert
  * computation and combine": each expert is an independent MLP over its

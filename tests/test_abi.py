@@ -84,6 +84,12 @@ def test_argument_validation_permutation(lib):
 def test_argument_validation_rows_and_gemm(lib):
     assert lib.moe_dispatch(FAKE, 16, 12, 2, FAKE, FAKE, None) == B.MOE_ERR_INVALID_ARG   # d % 8
     assert lib.moe_dispatch(FAKE, 16, 16, 2, FAKE, MIS, None) == B.MOE_ERR_MISALIGNED
+    assert lib.moe_dispatch_scatter(FAKE, 16, 12, 2, FAKE, FAKE, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_scatter(FAKE, 16, 16, 0, FAKE, FAKE, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_scatter(FAKE, 16, 16, 33, FAKE, FAKE, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_scatter(FAKE, 16, 16, 2, None, FAKE, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_scatter(FAKE, 16, 16, 2, MIS, FAKE, None) == B.MOE_ERR_MISALIGNED
+    assert lib.moe_dispatch_scatter(FAKE, 0, 16, 2, None, None, None) == B.MOE_OK
     assert lib.moe_combine(FAKE, FAKE, FAKE, 16, 2, 16, MIS, FAKE, None) == B.MOE_ERR_MISALIGNED
     assert lib.moe_dispatch_backward(FAKE, FAKE, 16, 0, 16, None, FAKE, None) == B.MOE_ERR_INVALID_ARG
     f = lib.moe_grouped_ffn

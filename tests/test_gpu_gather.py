@@ -44,6 +44,16 @@ def test_dispatch_exact(T, d, E, K):
     assert np.array_equal(f64(xp), ref)
 
 
+@pytest.mark.parametrize("T,d,E,K", SHAPES + [(513, 136, 8, 1), (64, 8, 40, 32)])
+def test_dispatch_scatter_exact(T, d, E, K):
+    """Token-major dispatch through inv_perm: bit-identical to the oracle's gather."""
+    _, _, perm, inv = _routing(T, E, K, T + 2 * d)
+    x = _bf16((T, d), 4)
+    xp = B.moe_dispatch_scatter(to_dev(x, torch.bfloat16), to_dev(inv, torch.int32), K)
+    ref = O.dispatch(x.to(torch.float64).numpy(), perm, K)
+    assert np.array_equal(f64(xp), ref)
+
+
 @pytest.mark.parametrize("T,d,E,K", SHAPES)
 @pytest.mark.parametrize("shared", [False, True])
 def test_combine(T, d, E, K, shared):

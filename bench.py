@@ -60,7 +60,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
-    ap.add_argument("--profile-case", choices=["gemm", "gemm_l2", "layer"], default=None,
+    ap.add_argument("--profile-case", choices=["gemm", "gemm_l2", "layer", "hbm"], default=None,
                     help="run a small fixed case twice for an ncu capture and exit")
     return ap.parse_args()
 
@@ -74,10 +74,35 @@ def profile_case(which: str):
              and activations mostly resident in L2, which isolates the kernels' own
              pipeline from DRAM streaming.
     layer:   one qwen3-shaped layer at T=2048 tokens (forward + backward), run twice.
+    hbm:     HBM bandwidth by access pattern on 2 GiB fp32 buffers (torch's fill, sum and
+             copy; CUDA events, 20 launches after 3 warm-ups): the ceilings that write-only,
+             read-only and copy-like kernels are compared with.
     Prints each kernel's launch time (CUDA events on the launching stream) and rate for
     the last run.
     """
     import torch
+    if which == "hbm":
+        dev = torch.device("cuda:0")
+        n = 1 << 29
+        a = torch.full((n,), 1.0, device=dev)
+        b = torch.full((n,), 2.0, device=dev)
+
+        def rate(fn, nbytes, reps=20):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(reps):
+                fn()
+            e.record()
+            torch.cuda.synchronize()
+            return nbytes / (s.elapsed_time(e) / reps * 1e-3) / 1e9
+
+        print(json.dumps({"write_gbs": rate(lambda: a.fill_(3.0), 4 * n),
+                          "read_gbs": rate(lambda: torch.sum(a), 4 * n),
+                          "copy_gbs": rate(lambda: b.copy_(a), 8 * n)}))
+        return
     from grouped_gemm_moe_gb300 import binding as B
     from grouped_gemm_moe_gb300 import build as build_mod
     from grouped_gemm_moe_gb300 import layer as L

@@ -43,6 +43,11 @@ SMALL = [
     ([1000], 512, 128),
     ([63, 65, 200, 1, 0, 319], 384, 512),
     ([0, 0, 0, 5], 256, 256),
+    # every width of transposed tail tile (last pair of an expert with 1..128 rows),
+    # normal partial tiles (129, 255), exact multiples of 256, and a tail that ends the
+    # packed rows (its activation boxes reach past M)
+    ([1, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 257, 384, 552, 255, 256, 0, 40],
+     256, 256),
 ]
 
 

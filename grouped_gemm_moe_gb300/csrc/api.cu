@@ -8,7 +8,7 @@
 namespace moe {
 
 size_t permutation_workspace(long long TK, int E, int R);   // permute.cu
-size_t ffn_backward_scratch(long long M, int I);            // grouped_gemm.cu
+size_t ffn_backward_scratch(long long M, int E, int d, int I);   // grouped_gemm.cu
 size_t load_balance_workspace(int E);                       // route.cu
 
 namespace {
@@ -90,7 +90,7 @@ extern "C" size_t moe_workspace_size(int op, int T, int E, int K, int R, int d, 
       return kWorkspaceHeader;
     case MOE_OP_GROUPED_FFN_BACKWARD:
       if (I < 1 || d < 1) return 0;
-      return kWorkspaceHeader + ffn_backward_scratch(TK, I);
+      return kWorkspaceHeader + ffn_backward_scratch(TK, E, d, I);
     case MOE_OP_LOAD_BALANCE:
       return load_balance_workspace(E);
     default:

@@ -63,6 +63,15 @@ constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 
+// One zero-padded straddling step to prepare for the weight gradients: for each
+// expert whose row count is not a multiple of 16, the 16-row step that holds its
+// last rows, rows past the expert set to zero (a [M, C] bf16 -> pad [E, 16, C]).
+struct PadJob {
+  const __nv_bfloat16* a;
+  __nv_bfloat16* pad;
+  int C;
+};
+
 struct Params {
   const int32_t* offsets;  // [E+1] expert row offsets (device)
   int E;
@@ -79,6 +88,7 @@ struct Params {
   float* outf1;            // dWu
   int ld_out;              // row length of `out` in elements
   int* status;             // workspace status word
+  PadJob pad[2];           // BWD_DH: the weight gradients' pads of X and H (a == null: none)
 };
 
 // ----------------------------------------------------------------- PTX helpers
@@ -386,6 +396,35 @@ __device__ __forceinline__ void issue_pair(const PTile& tl, int kb, uint32_t ran
   }
 }
 
+// Fills pad[e] of one PadJob (see PadJob) with nthreads threads numbered tid,
+// each with up to kPadVec 16-byte loads in flight. s_off: the expert offsets.
+constexpr int kPadVec = 8;
+
+__device__ __forceinline__ void pad_straddle_step(const int* s_off, const PadJob& j, int e, int tid,
+                                                  int nthreads) {
+  const int r0 = s_off[e];
+  const int rows = s_off[e + 1] - r0;
+  const int v = rows & 15;
+  if (v == 0) return;
+  const int nv = j.C / 8;          // 16-byte vectors per row
+  const int total = 16 * nv;       // vectors of the 16-row step
+  const uint4* src = reinterpret_cast<const uint4*>(j.a + static_cast<size_t>(r0 + (rows & ~15)) * j.C);
+  uint4* dst = reinterpret_cast<uint4*>(j.pad + static_cast<size_t>(e) * 16 * j.C);
+  for (int base = tid; base < total; base += nthreads * kPadVec) {
+    uint4 x[kPadVec];
+#pragma unroll
+    for (int u = 0; u < kPadVec; ++u) {
+      const int i = base + u * nthreads;
+      x[u] = (i < total && i / nv < v) ? ldg_nc_v4(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kPadVec; ++u) {
+      const int i = base + u * nthreads;
+      if (i < total) dst[i] = x[u];
+    }
+  }
+}
+
 // Pair-kernel epilogue shared memory: bf16 output staging for bulk tensor stores,
 // per epilogue warp two alternating [32 rows x 64 columns] 128-byte-swizzled
 // boxes (gate/up streams H, G and U through them in turn), and for dh the four
@@ -608,6 +647,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     const int q = warp & 3;
     const int ew = warp - 2;
     const int r = q * 32 + lane;
+    if constexpr (KIND == BWD_DH) {
+      // Until the first accumulator is ready these warps are idle: they prepare the
+      // weight gradients' zero-padded straddling steps of X and H meanwhile.
+      if (p.pad[0].a) {
+        for (int job = static_cast<int>(blockIdx.x); job < 2 * p.E; job += static_cast<int>(gridDim.x))
+          pad_straddle_step(s_off, p.pad[job & 1], job >> 1, threadIdx.x - 64, 128);
+      }
+    }
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -815,11 +862,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 // per k-block instead of the 48 KB of a single-CTA 128 x 256 tile.
 //
 // Both CTAs' boxes complete on the leader's full barrier, as in the forward
-// pair kernel. The ragged last k-block of an expert is handled by the leader's
-// MMA warp alone: it issues only the K16 steps that hold valid rows and zeroes,
-// in both CTAs' A (the follower's through distributed shared memory), the rows
-// of the one step that straddles the expert's end; a shared::cluster proxy
-// fence then orders those writes before its own MMA.
+// pair kernel. In the ragged last k-block of an expert the MMA issues only the
+// K16 steps that hold a valid row. The one step that straddles the expert's
+// end would bring in rows of the next expert, so that k-block's A comes in
+// 16-row boxes: its full steps from the activations (tmA16) and the straddling
+// step from a zero-padded copy of it (tmP, filled by the dH launch's epilogue
+// warps before their first tile); B's rows past the expert then meet zero rows
+// of A. Nothing
+// is zeroed in shared memory: zeroing the rows there from the MMA thread (both
+// CTAs' A, the follower's through distributed shared memory, then a
+// cluster-scope proxy fence) cost this kernel ~8%.
 //
 // Accumulator buffers: the leader's epilogue warps arrive on its
 // accumulator-empty barrier locally, the follower's remotely with a relaxed
@@ -872,7 +924,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
                                const __grid_constant__ CUtensorMap tmB,
                                const __grid_constant__ CUtensorMap tmC0,
-                               const __grid_constant__ CUtensorMap tmC1, const Params p) {
+                               const __grid_constant__ CUtensorMap tmC1,
+                               const __grid_constant__ CUtensorMap tmA16,
+                               const __grid_constant__ CUtensorMap tmP, const Params p) {
   static_assert(KIND == WGRAD_GU || KIND == WGRAD_D, "pair weight-gradient kernel");
   constexpr int BN = 256;
   constexpr uint32_t MN_ATOM = 64 * 128;
@@ -916,6 +970,8 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC1)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA16)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmP)) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -958,10 +1014,25 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const int ky = tl.row0 + kb * BK;
           const uint32_t fb = full_bar(stage);
-          if (leader) mbar_expect_tx(fb, 2 * STAGE_BYTES);   // both CTAs' boxes
           const uint32_t fr = map_to_rank(fb, 0);
-          tma_load_2d_pair(sa, &tmA, fr, tl.m0, ky);
-          tma_load_2d_pair(sa + MN_ATOM, &tmA, fr, tl.m0 + 64, ky);
+          const int kvalid = min(BK, tl.rows - kb * BK);
+          if ((kvalid & 15) == 0) {
+            if (leader) mbar_expect_tx(fb, 2 * STAGE_BYTES);   // both CTAs' boxes
+            tma_load_2d_pair(sa, &tmA, fr, tl.m0, ky);
+            tma_load_2d_pair(sa + MN_ATOM, &tmA, fr, tl.m0 + 64, ky);
+          } else {
+            // straddling k-block: A in 16-row boxes, the last one zero-padded; the
+            // K16 steps past it are neither loaded nor read
+            const int nfull = kvalid >> 4;
+            if (leader) mbar_expect_tx(fb, 2 * (static_cast<uint32_t>(nfull + 1) * 2 * 2048u + B_BYTES));
+#pragma unroll
+            for (int atom = 0; atom < 2; ++atom) {
+              const uint32_t da = sa + atom * MN_ATOM;
+              const int x = tl.m0 + 64 * atom;
+              for (int kk = 0; kk < nfull; ++kk) tma_load_2d_pair(da + kk * 2048, &tmA16, fr, x, ky + 16 * kk);
+              tma_load_2d_pair(da + nfull * 2048, &tmP, fr, x, tl.e * 16);
+            }
+          }
           tma_load_2d_pair(sa + A_BYTES, &tmB, fr, nb, ky);
           tma_load_2d_pair(sa + A_BYTES + MN_ATOM, &tmB, fr, nb + 64, ky);
           fpar ^= 1u << stage;
@@ -992,7 +1063,6 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      const uint32_t peer_smem = map_to_rank(smem_base, 1);
       for (int t = cid; t < total && ok; t += ncl) {
         const WTile tl = decode_wgrad_pair<KIND>(t, 0, p, s_off);
         if (tl.nkb == 0) continue;
@@ -1005,22 +1075,6 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t sb = sa + A_BYTES;
           const int kvalid = min(BK, tl.rows - kb * BK);
           const int nsteps = (kvalid + 15) >> 4;          // K16 steps with a valid row
-          const int zlo = kvalid, zhi = nsteps * 16;       // rows to zero in the last step
-          if (zlo < zhi) {
-            // rows [zlo, zhi) of both CTAs' A belong to the next expert
-            const uint32_t peer_a = peer_smem + stage * STAGE_BYTES;
-            const int nbytes = (zhi - zlo) * 128;
-            for (int i = lane; i < 2 * (nbytes >> 4); i += 32) {
-              const int atom = i / (nbytes >> 4);
-              const int off = zlo * 128 + ((i - atom * (nbytes >> 4)) << 4) + atom * MN_ATOM;
-              *reinterpret_cast<uint4*>(smem + stage * STAGE_BYTES + off) = make_uint4(0, 0, 0, 0);
-              asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(peer_a + off),
-                           "r"(0u)
-                           : "memory");
-            }
-            asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-            __syncwarp();
-          }
           if (lane == 0) {
             for (int kk = 0; kk < nsteps; ++kk) {
               const uint64_t ad = smem_desc(sa + kk * 2048, MN_ATOM, 1024);
@@ -1248,8 +1302,8 @@ static_assert(pair_wgrad_smem_bytes<5>(1024) <= 232448, "pair wgrad smem (5 stag
 
 template <int KIND, int STAGES>
 int launch_pair_wgrad_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c0,
-                             const CUtensorMap& c1, const Params& p, long long tiles,
-                             cudaStream_t st) {
+                             const CUtensorMap& c1, const CUtensorMap& a16, const CUtensorMap& pad,
+                             const Params& p, long long tiles, cudaStream_t st) {
   static thread_local int configured = -1;
   static thread_local int max_clusters = 0;
   return launch_cluster2(grouped_gemm_pair_wgrad_kernel<KIND, STAGES>,
@@ -1257,14 +1311,17 @@ int launch_pair_wgrad_stages(const CUtensorMap& a, const CUtensorMap& b, const C
                          pair_wgrad_smem_bytes<STAGES>(STAGES == 6 ? kWgradPair6MaxE : 1024),
                          &configured, &max_clusters, tiles,
                          KIND == WGRAD_GU ? "gemm_wgrad_gate_up" : "gemm_wgrad_down", st, a, b,
-                         c0, c1, p);
+                         c0, c1, a16, pad, p);
 }
 
+// a16: A again with 16-row boxes; pad: the zero-padded straddling steps of A.
 template <int KIND>
 int launch_pair_wgrad(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c0,
-                      const CUtensorMap& c1, const Params& p, long long tiles, cudaStream_t st) {
-  if (p.E <= kWgradPair6MaxE) return launch_pair_wgrad_stages<KIND, 6>(a, b, c0, c1, p, tiles, st);
-  return launch_pair_wgrad_stages<KIND, 5>(a, b, c0, c1, p, tiles, st);
+                      const CUtensorMap& c1, const CUtensorMap& a16, const CUtensorMap& pad,
+                      const Params& p, long long tiles, cudaStream_t st) {
+  if (p.E <= kWgradPair6MaxE)
+    return launch_pair_wgrad_stages<KIND, 6>(a, b, c0, c1, a16, pad, p, tiles, st);
+  return launch_pair_wgrad_stages<KIND, 5>(a, b, c0, c1, a16, pad, p, tiles, st);
 }
 
 constexpr long long kSmemOptIn = 232448;   // shared memory a CTA may opt into
@@ -1323,8 +1380,10 @@ inline int pair_bn(int n) { return (n % 256 == 0 && MOE_PAIR_BN_MAX >= 256) ? 25
 
 }  // namespace gemm
 
-size_t ffn_backward_scratch(long long M, int I) {
-  return static_cast<size_t>(M) * 2 * I * sizeof(uint16_t);
+// [dG | dU] as bf16 [M, 2I], then the zero-padded straddling steps of X and H
+// for the weight gradients: bf16 [E, 16, d] and [E, 16, I].
+size_t ffn_backward_scratch(long long M, int E, int d, int I) {
+  return (static_cast<size_t>(M) * 2 * I + static_cast<size_t>(E) * 16 * (d + I)) * sizeof(uint16_t);
 }
 
 }  // namespace moe
@@ -1412,7 +1471,7 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
       !aligned16(offsets) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
       !aligned16(dw_gate) || !aligned16(dw_up) || !aligned16(dw_down))
     return MOE_ERR_MISALIGNED;
-  if (!ws || !aligned16(ws) || ws_bytes < kWorkspaceHeader + ffn_backward_scratch(M, I))
+  if (!ws || !aligned16(ws) || ws_bytes < kWorkspaceHeader + ffn_backward_scratch(M, E, d, I))
     return MOE_ERR_WORKSPACE;
   if (cc_major() < 10) return MOE_ERR_UNSUPPORTED;
   cudaStream_t st = as_stream(stream);
@@ -1424,6 +1483,9 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
     return check_launch();
   }
   auto dgu = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + kWorkspaceHeader);
+  auto pad_x = dgu + static_cast<size_t>(M) * 2 * I;          // [E, 16, d]
+  auto pad_h = pad_x + static_cast<size_t>(E) * 16 * d;       // [E, 16, I]
+
   Params p{};
   p.offsets = offsets;
   p.E = E;
@@ -1445,6 +1507,9 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   p.out = dgu;
   p.aux = reinterpret_cast<const __nv_bfloat16*>(gu);
   p.ld_out = 2 * I;
+  // the dH launch also fills the weight gradients' padded straddling steps
+  p.pad[0] = PadJob{reinterpret_cast<const __nv_bfloat16*>(xp), pad_x, d};
+  p.pad[1] = PadJob{reinterpret_cast<const __nv_bfloat16*>(h), pad_h, I};
   int rc = launch_pair_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc1, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // dX = dG Wg^T + dU Wu^T
@@ -1459,10 +1524,13 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   p.out = reinterpret_cast<__nv_bfloat16*>(dxp);
   p.aux = nullptr;
   p.ld_out = d;
+  p.pad[0] = p.pad[1] = PadJob{nullptr, nullptr, 0};
   rc = launch_pair_bn<BWD_DX>(bn_x, ta, tb0, tb1, tc0, tc0, p, mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // [dWg | dWu] = X^T [dG | dU]
+  CUtensorMap ta16, tpad;
   if (!make_map(&ta, xp, d, M, 64, 64) || !make_map(&tb0, dgu, 2 * static_cast<uint64_t>(I), M, 64, 64) ||
+      !make_map(&ta16, xp, d, M, 64, 16) || !make_map(&tpad, pad_x, d, static_cast<uint64_t>(E) * 16, 64, 16) ||
       !make_map(&tc0, dw_gate, I, static_cast<uint64_t>(E) * d, 32, 32, true) ||
       !make_map(&tc1, dw_up, I, static_cast<uint64_t>(E) * d, 32, 32, true))
     return MOE_ERR_CUDA;
@@ -1472,19 +1540,20 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   p.outf0 = dw_gate;
   p.outf1 = dw_up;
   p.out = nullptr;
-  rc = launch_pair_wgrad<WGRAD_GU>(ta, tb0, tc0, tc1, p,
+  rc = launch_pair_wgrad<WGRAD_GU>(ta, tb0, tc0, tc1, ta16, tpad, p,
                                    static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
   if (rc) return rc;
   // dWd = H^T dY on CTA pairs (when d is an odd multiple of 128 the last n-tile's
   // upper half reads the TMA fill value past column d and stores nothing)
   if (!make_map(&ta, h, I, M, 64, 64) || !make_map(&tb0, dy, d, M, 64, 64) ||
-      !make_map(&tc0, dw_down, d, static_cast<uint64_t>(E) * I, 32, 32, true))
+      !make_map(&tc0, dw_down, d, static_cast<uint64_t>(E) * I, 32, 32, true) ||
+      !make_map(&ta16, h, I, M, 64, 16) || !make_map(&tpad, pad_h, I, static_cast<uint64_t>(E) * 16, 64, 16))
     return MOE_ERR_CUDA;
   p.outf0 = dw_down;
   p.outf1 = nullptr;
   p.m_tiles = (I + 2 * BM - 1) / (2 * BM);
   p.n_tiles = (d + 255) / 256;
-  return launch_pair_wgrad<WGRAD_D>(ta, tb0, tc0, tc0, p,
+  return launch_pair_wgrad<WGRAD_D>(ta, tb0, tc0, tc0, ta16, tpad, p,
                                     static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
 }
 

@@ -261,7 +261,9 @@ int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E, int M, in
  *   moe_grouped_ffn. dxp [M,d] bf16 out; dw_gate, dw_up [E,d,I] fp32 out;
  *   dw_down [E,I,d] fp32 out.
  *   ws: moe_workspace_size(MOE_OP_GROUPED_FFN_BACKWARD, T,E,K,R,d,I) with
- *   T*K = M; holds [dG | dU] as bf16 [M,2I]. */
+ *   T*K = M; holds [dG | dU] as bf16 [M,2I] and, per expert, the 16-row step
+ *   of X and of H that holds the expert's last rows, zero-padded (bf16
+ *   [E,16,d] and [E,16,I]). */
 int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
                              const moe_bf16* h, const int32_t* offsets, int E, int M, int d,
                              int I, const moe_bf16* w_gate, const moe_bf16* w_up,

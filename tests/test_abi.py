@@ -130,7 +130,7 @@ def test_workspace_sizes(lib):
     hdr = B.WORKSPACE_HEADER
     assert B.workspace_size(B.MOE_OP_GROUPED_FFN, 8192, 128, 8, 1, 2048, 768) == hdr
     assert B.workspace_size(B.MOE_OP_GROUPED_FFN_BACKWARD, 8192, 128, 8, 1, 2048, 768) == \
-        hdr + 8192 * 8 * 2 * 768 * 2
+        hdr + 8192 * 8 * 2 * 768 * 2 + 128 * 16 * (2048 + 768) * 2
     n = B.workspace_size(B.MOE_OP_BUILD_PERMUTATION, 8192, 128, 8)
     assert n >= hdr + 16 * 128 * 4
     assert B.workspace_size(B.MOE_OP_EP_LAYOUT, 8192, 128, 8, 3) == 0

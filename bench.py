@@ -60,7 +60,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
-    ap.add_argument("--profile-case", choices=["gemm", "gemm_l2", "layer", "hbm"], default=None,
+    ap.add_argument("--profile-case", choices=["gemm", "gemm_ragged", "gemm_l2", "layer", "hbm"],
+                    default=None,
                     help="run a small fixed case twice for an ncu capture and exit")
     return ap.parse_args()
 
@@ -70,6 +71,8 @@ def profile_case(which: str):
 
     gemm:    the grouped-GEMM entry points, forward and backward, on E=64 experts x 512 rows
              (d=2048, I=768; the qwen3 workload's rows per expert), run twice.
+    gemm_ragged: as gemm, with seeded expert sizes 512 + round(N(0, 21)) (the spread of the
+             qwen3 workload's routed rows; most experts end inside a K16 step), run twice.
     gemm_l2: the same entry points on one expert of 16384 rows (d=2048, I=768): weights
              and activations mostly resident in L2, which isolates the kernels' own
              pipeline from DRAM streaming.
@@ -112,15 +115,20 @@ def profile_case(which: str):
     dev = torch.device("cuda:0")
     g = torch.Generator(device=dev).manual_seed(0)
     flops = {}
-    if which in ("gemm", "gemm_l2"):
-        E, d, I, rows = (64, 2048, 768, 512) if which == "gemm" else (1, 2048, 768, 16384)
-        M = E * rows
+    if which in ("gemm", "gemm_ragged", "gemm_l2"):
+        E, d, I, rows = (1, 2048, 768, 16384) if which == "gemm_l2" else (64, 2048, 768, 512)
+        if which == "gemm_ragged":
+            gc = torch.Generator().manual_seed(3)
+            sizes = (rows + torch.randn(E, generator=gc) * 21).round().clamp(min=1).to(torch.int64)
+        else:
+            sizes = torch.full((E,), rows, dtype=torch.int64)
+        M = int(sizes.sum())
         flops = {"gemm_gate_up": 4 * M * d * I, "gemm_down": 2 * M * d * I, "gemm_dh": 2 * M * d * I,
                  "gemm_dx": 4 * M * d * I, "gemm_wgrad_gate_up": 4 * M * d * I,
                  "gemm_wgrad_down": 2 * M * d * I}
         bf = torch.bfloat16
         rnd = lambda *s, sc=1.0: (torch.randn(*s, device=dev, generator=g) * sc).to(bf)  # noqa: E731
-        off = torch.arange(0, M + 1, rows, dtype=torch.int32, device=dev)
+        off = torch.cat([torch.zeros(1, dtype=torch.int64), sizes.cumsum(0)]).to(torch.int32).to(dev)
         xp, dy, gu, h = rnd(M, d), rnd(M, d, sc=0.1), rnd(M, 2 * I), rnd(M, I, sc=0.5)
         wg, wu, wd = rnd(E, d, I, sc=0.02), rnd(E, d, I, sc=0.02), rnd(E, I, d, sc=0.02)
         for it in range(2):

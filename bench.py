@@ -234,13 +234,38 @@ KERNEL_SOURCE = {"route": "route.cu", "perm": "permute.cu", "ep_": "permute.cu",
                  "dispatch": "gather.cu", "combine": "gather.cu", "gemm": "grouped_gemm.cu"}
 
 
+def code_digest(path: str) -> str:
+    """sha256 of a C++/CUDA source with its comments and blank lines removed
+    (line comments outside string literals, block comments), so that an edit
+    of the comments keeps a measured figure while any change of code drops it."""
+    import hashlib
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = []
+    for line in text.splitlines():
+        code, in_str, i = [], False, 0
+        while i < len(line):
+            ch = line[i]
+            if ch == '"' and (i == 0 or line[i - 1] != "\\"):
+                in_str = not in_str
+            if not in_str and line.startswith("//", i):
+                break
+            code.append(ch)
+            i += 1
+        stripped = "".join(code).rstrip()
+        if stripped.strip():
+            out.append(stripped)
+    return hashlib.sha256("\n".join(out).encode()).hexdigest()
+
+
 def measured_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from a committed ncu summary under
     profiles/: a line 'traffic-record: kernel=<name> bytes_per_launch=<B>
-    source=<file> sha256=<hex>'. The figure counts only while the kernel's
-    source file still hashes to the recorded value (None otherwise)."""
+    source=<file> code-sha256=<hex>'. The figure counts only while the
+    kernel's source file still has the recorded code digest (code_digest;
+    None otherwise)."""
     import glob
-    import hashlib
     here = os.path.dirname(os.path.abspath(__file__))
     src = next((f for pre, f in KERNEL_SOURCE.items() if kernel.startswith(pre)), None)
     if src is None:
@@ -248,13 +273,13 @@ def measured_traffic(kernel: str):
     path = os.path.join(here, "grouped_gemm_moe_gb300", "csrc", src)
     if not os.path.exists(path):
         return None
-    digest = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    digest = code_digest(path)
     for md in sorted(glob.glob(os.path.join(here, "profiles", "*.md"))):
         for line in open(md):
             if not line.startswith("traffic-record:"):
                 continue
             kv = dict(f.split("=", 1) for f in line.split()[1:] if "=" in f)
-            if kv.get("kernel") == kernel and kv.get("source") == src and kv.get("sha256") == digest:
+            if kv.get("kernel") == kernel and kv.get("source") == src and kv.get("code-sha256") == digest:
                 return float(kv["bytes_per_launch"])
     return None
 

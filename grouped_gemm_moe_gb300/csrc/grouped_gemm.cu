@@ -34,8 +34,9 @@
 //   * ragged segments: forward / input-gradient tiles start at an expert's
 //     first row and mask stores past its last row; the weight gradients run a
 //     ragged K loop over the expert's rows, issue only the K16 steps that hold
-//     valid rows and zero the rows of the one step that straddles the
-//     expert's end before the MMA reads them;
+//     valid rows and take the one step that straddles the expert's end from a
+//     zero-padded copy (written by the dH launch), so rows of the next expert
+//     never enter the product;
 //   * each GEMM waits on its producer through programmatic dependent launch
 //     before it reads the expert offsets;
 //   * every mbarrier wait is bounded (a few seconds of %globaltimer); on

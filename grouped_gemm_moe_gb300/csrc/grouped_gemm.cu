@@ -426,13 +426,13 @@ __device__ __forceinline__ void pad_straddle_step(const int* s_off, const PadJob
   }
 }
 
-// Pair-kernel epilogue shared memory: bf16 output staging for bulk tensor stores,
-// per epilogue warp two alternating [32 rows x 64 columns] 128-byte-swizzled
-// boxes (gate/up streams H, G and U through them in turn), and for dh the four
-// G/U prefetch boxes, which the dG/dU results overwrite before their store.
+// Pair-kernel epilogue shared memory: per epilogue warp two [32 rows x 64
+// columns] 128-byte-swizzled bf16 boxes: alternating bulk-store staging
+// (gate/up streams H, G and U through them in turn), and for dh the G and U
+// prefetch boxes, which the dG/dU results overwrite before their store.
 template <int KIND>
 __host__ __device__ constexpr uint32_t pair_epi_bytes() {
-  return KIND == BWD_DH ? 4u * 16384u : 4u * 2u * 4096u;
+  return 4u * 2u * 4096u;
 }
 
 // Writes 32 consecutive columns (values v) of this lane's row into a
@@ -669,17 +669,19 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       const int growq = tl.row0 + q * 32;          // first row of this warp's slice
       const bool full = (tl.rows - q * 32) >= 32;  // every row of the slice is valid
       if constexpr (KIND == BWD_DH) {
-        uint8_t* aux = epi + ew * 16384;   // boxes: G[c0,+64) G[c0+64,+64) U[c0,+64) U[c0+64,+64)
+        // The warp's 32 rows go 64 columns at a time: G[c0,+64) and U[c0,+64) are
+        // TMA-loaded into two boxes, dG and dU overwrite them in place and leave
+        // through bulk stores. Four such steps per tile take well under the next
+        // tile's MMA time, and the 8 KB per warp leaves room for a sixth stage.
+        uint8_t* aux = epi + ew * 8192;   // boxes: G[c0,+64) then U[c0,+64)
         const uint32_t aux_addr = smem_u32(aux);
         const uint32_t ab = aux_bar(ew);
         auto request = [&](int c0) {
           if (lane == 0) {
             bulk_wait_read_all();          // earlier dG/dU stores from these boxes are done
-            mbar_expect_tx(ab, 16384);
+            mbar_expect_tx(ab, 8192);
             tma_load_2d(aux_addr, &tmC0, ab, tl.n0 + c0, growq);
-            tma_load_2d(aux_addr + 4096, &tmC0, ab, tl.n0 + c0 + 64, growq);
-            tma_load_2d(aux_addr + 8192, &tmC0, ab, p.I + tl.n0 + c0, growq);
-            tma_load_2d(aux_addr + 12288, &tmC0, ab, p.I + tl.n0 + c0 + 64, growq);
+            tma_load_2d(aux_addr + 4096, &tmC0, ab, p.I + tl.n0 + c0, growq);
           }
           aux_pending = true;
         };
@@ -688,26 +690,25 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         tc_fence_after();
         const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
         bool ok = true;
-        for (int c0 = 0; c0 < BN; c0 += 128) {
+        for (int c0 = 0; c0 < BN; c0 += 64) {
           if (c0) request(c0);
           if (!mbar_wait(ab, aux_phase, abort_flag, p.status)) { ok = false; break; }
           aux_phase ^= 1u;
           aux_pending = false;
-          for (int c = 0; c < 128; c += 16) {
+          for (int c = 0; c < 64; c += 16) {
             float dh[16];
             tmem_ld16(tacc + c0 + c, dh);
             tmem_wait_ld();
-            const int box = c >> 6;
-            const int j0 = (c & 63) >> 3;
+            const int j0 = c >> 3;
             float g[16], u[16];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               const int off = lane * 128 + (((j0 + hh) ^ (lane & 7)) << 4);
               float f[8];
-              unpack8(*reinterpret_cast<const uint4*>(aux + box * 4096 + off), f);
+              unpack8(*reinterpret_cast<const uint4*>(aux + off), f);
 #pragma unroll
               for (int i = 0; i < 8; ++i) g[8 * hh + i] = f[i];
-              unpack8(*reinterpret_cast<const uint4*>(aux + 8192 + box * 4096 + off), f);
+              unpack8(*reinterpret_cast<const uint4*>(aux + 4096 + off), f);
 #pragma unroll
               for (int i = 0; i < 8; ++i) u[8 * hh + i] = f[i];
             }
@@ -722,8 +723,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 const int off = lane * 128 + (((j0 + hh) ^ (lane & 7)) << 4);
-                *reinterpret_cast<uint4*>(aux + box * 4096 + off) = pack8(&dg[8 * hh]);
-                *reinterpret_cast<uint4*>(aux + 8192 + box * 4096 + off) = pack8(&du[8 * hh]);
+                *reinterpret_cast<uint4*>(aux + off) = pack8(&dg[8 * hh]);
+                *reinterpret_cast<uint4*>(aux + 4096 + off) = pack8(&du[8 * hh]);
               }
             } else if (valid) {
               __nv_bfloat16* orow = p.out + grow * (2 * p.I);
@@ -735,9 +736,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           __syncwarp();
           if (full && lane == 0) {
             tma_store_2d(&tmC1, aux_addr, tl.n0 + c0, growq);
-            tma_store_2d(&tmC1, aux_addr + 4096, tl.n0 + c0 + 64, growq);
-            tma_store_2d(&tmC1, aux_addr + 8192, p.I + tl.n0 + c0, growq);
-            tma_store_2d(&tmC1, aux_addr + 12288, p.I + tl.n0 + c0 + 64, growq);
+            tma_store_2d(&tmC1, aux_addr + 4096, p.I + tl.n0 + c0, growq);
             bulk_commit();
           }
         }
@@ -1342,11 +1341,11 @@ constexpr int pair_max_e() {
 // latency.
 template <int KIND, int BN>
 constexpr int pair_stages() {
-  return KIND == BWD_DH ? (BN == 256 ? 4 : 5) : (BN == 256 ? 5 : 7);
+  return BN == 256 ? 5 : 7;
 }
 template <int KIND, int BN>
 constexpr int pair_stages_deep() {
-  return KIND == BWD_DH ? (BN == 256 ? 5 : 6) : (BN == 256 ? 6 : 8);
+  return BN == 256 ? 6 : 8;
 }
 
 template <int KIND, int BN>

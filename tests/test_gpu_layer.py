@@ -214,3 +214,45 @@ def test_run_from_host_pipelined_steps_match_device_path():
     for (_, _, _, oh, dxh), b in zip(steps, order):
         assert torch.equal(oh, want[b][0])
         assert torch.equal(dxh, want[b][1])
+
+
+@pytest.mark.parametrize("name", ["qwen3", "dsv2lite"])
+def test_layer_full_size_sampled_tokens(name):
+    """The benchmarked launch sequence at the workload's full size. Every output
+    row of a token (out, dx, dlogits, its top-k) depends only on that token's
+    inputs and on the experts it selects, so the oracle runs the layer on a
+    sample of 8 tokens restricted to the experts they select (relabelled in
+    ascending order: with renormalised weights the top-k and its weights are the
+    same among those experts as among all E, and the router gradient is zero
+    elsewhere), and those rows are compared."""
+    cfg = W.CONFIGS[name]
+    assert cfg.renorm == 1
+    inp = W.make_inputs(cfg, with_backward=True)
+    layer = L.layer_from_config(cfg, inp, dev())
+    out = layer.forward(inp["logits"].to(dev()), inp["x"].to(dev())).clone()
+    dx = layer.backward(inp["dout"].to(dev())).clone()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    toks = np.sort(np.random.default_rng(7).choice(cfg.T, size=8, replace=False))
+    tt = torch.from_numpy(toks)
+    idx, _ = O.route_topk(W.to_f64(inp["logits"][tt]), cfg.K, cfg.renorm)
+    used = np.unique(idx)
+    ut = torch.from_numpy(used)
+    sub = {"logits": W.to_f64(inp["logits"][tt][:, ut]), "x": W.to_f64(inp["x"][tt]),
+           "dout": W.to_f64(inp["dout"][tt])}
+    for k in ("w_gate", "w_up", "w_down"):
+        sub[k] = W.to_f64(inp[k][ut])
+    for k in ("ws_gate", "ws_up", "ws_down"):
+        if k in inp:
+            sub[k] = W.to_f64(inp[k])
+    ref = O.layer_forward(sub, cfg.K, 1, cfg.renorm, pre=True)
+    rb = O.layer_backward(sub, ref, sub["dout"], cfg.K, cfg.renorm, pre=True)
+    assert np.array_equal(i64(layer.topk_idx)[toks], used[ref["topk_idx"]])
+    assert_rel_close(f64(layer.topk_w)[toks], ref["topk_w"], name="topk_w")
+    assert_out_close(f64(out)[toks], ref["out_pre"], name="out")
+    assert_out_close(f64(dx)[toks], rb["dx_pre"], name="dx")
+    dl = f64(layer.dlogits)[toks]
+    assert_rms_close(dl[:, used], rb["dlogits"], name="dlogits")
+    rest = np.ones(cfg.E, bool)
+    rest[used] = False
+    assert (dl[:, rest] == 0).all()

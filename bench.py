@@ -60,7 +60,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
-    ap.add_argument("--profile-case", choices=["gemm", "gemm_ragged", "gemm_l2", "layer", "hbm"],
+    ap.add_argument("--profile-case", choices=["gemm", "gemm_ragged", "gemm_l2", "layer", "hbm",
+                                               "routing"],
                     default=None,
                     help="run a small fixed case twice for an ncu capture and exit")
     return ap.parse_args()
@@ -77,6 +78,9 @@ def profile_case(which: str):
              and activations mostly resident in L2, which isolates the kernels' own
              pipeline from DRAM streaming.
     layer:   one qwen3-shaped layer at T=2048 tokens (forward + backward), run twice.
+    routing: the forward's front on the qwen3 workload at full size (route top-k, the fused
+             permutation + EP layout with its host copy, token-major dispatch), run twice;
+             ~0.4 GB on the device.
     hbm:     HBM bandwidth by access pattern on 2 GiB fp32 buffers (torch's fill, sum and
              copy; CUDA events, 20 launches after 3 warm-ups): the ceilings that write-only,
              read-only and copy-like kernels are compared with.
@@ -137,6 +141,21 @@ def profile_case(which: str):
                 B.moe_profile_start(64)
             B.moe_grouped_ffn_backward(dy, xp, gu, h, off, wg, wu, wd)
             B.moe_grouped_ffn(xp, off, wg, wu, wd)
+    elif which == "routing":
+        cfg = W.CONFIGS["qwen3"]
+        inp = W.make_inputs(cfg, with_backward=False)
+        logits, x = inp["logits"].to(dev), inp["x"].to(dev)
+        host = torch.empty(cfg.R * cfg.E + cfg.R * cfg.R, dtype=torch.int32).pin_memory()
+        for it in range(2):
+            if it == 1:
+                torch.cuda.synchronize()
+                B.moe_profile_start(64)
+            idx, w = B.moe_route_topk(logits, cfg.K, cfg.renorm)
+            res = B.moe_build_permutation_ep(idx, cfg.E, cfg.R, host_splits=host)
+            B.moe_dispatch_scatter(x, res[3], cfg.K)
+        torch.cuda.synchronize()
+        for name, ms in B.moe_profile_stop():
+            print(f"  {name:22s} {ms * 1e3:9.1f} us")
     else:
         cfg = W.MoEConfig("qwen3-2k", T=2048, d=2048, E=128, K=8, I=768, R=8)
         inp = W.make_inputs(cfg)

@@ -47,17 +47,26 @@ __device__ __forceinline__ void chunk_range(const ChunkGeom& g, int c, long long
   end = min(start + kChunk, static_cast<long long>(s + 1) * g.seg_len);
 }
 
-// Counts this warp's assignments of the chunk into wh[e] (warp-private row).
-__device__ __forceinline__ void warp_count(const int32_t* __restrict__ idx, long long wstart,
-                                           long long end, int* wh) {
+// This warp's experts of the chunk, one per lane and step (-1 past the chunk),
+// loaded up front so that their latency overlaps whatever the block does next.
+__device__ __forceinline__ void load_warp_ids(const int32_t* __restrict__ idx, long long wstart,
+                                              long long end, int (&ev)[kSteps]) {
   const int lane = threadIdx.x & 31;
-#pragma unroll 1
+#pragma unroll
   for (int st = 0; st < kSteps; ++st) {
     const long long a = wstart + st * 32 + lane;
-    const bool valid = a < end;
-    const int e = valid ? __ldg(idx + a) : -1;
+    ev[st] = (a < end) ? __ldg(idx + a) : -1;
+  }
+}
+
+// Counts this warp's assignments of the chunk into wh[e] (warp-private row).
+__device__ __forceinline__ void warp_count(const int (&ev)[kSteps], int* wh) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int st = 0; st < kSteps; ++st) {
+    const int e = ev[st];
     const unsigned grp = __match_any_sync(0xffffffffu, e);
-    if (valid && lane == __ffs(grp) - 1) wh[e] += __popc(grp);
+    if (e >= 0 && lane == __ffs(grp) - 1) wh[e] += __popc(grp);
     __syncwarp();
   }
 }
@@ -91,7 +100,9 @@ hist_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int32_t* __rest
   int s;
   chunk_range(g, blockIdx.x, start, end, s);
   const int w = threadIdx.x >> 5;
-  warp_count(idx, start + static_cast<long long>(w) * kPerWarp, end, wh + w * E);
+  int ev[kSteps];
+  load_warp_ids(idx, start + static_cast<long long>(w) * kPerWarp, end, ev);
+  warp_count(ev, wh + w * E);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kThreads) {
     int sum = 0;
@@ -130,17 +141,27 @@ scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
   int* cs = bs + E;                  // [E+1] C[s][e] -> exclusive scan (send prefix)
   int* craw = cs + (E + 1);          // [E]   C[s][e]
   int* csb = craw + E;               // [E+1] sum of C[s'][e] for s' < s -> exclusive scan
+  int* part = csb + (E + 1);         // [5][kThreads] partial sums of the table pass
 
   const int c = blockIdx.x;
   long long start, end;
   int s;
   chunk_range(g, c, start, end, s);
+  const int w = threadIdx.x >> 5;
+  const long long wstart = start + static_cast<long long>(w) * kPerWarp;
+  int ev[kSteps];
+  load_warp_ids(idx, wstart, end, ev);
 
   for (int i = threadIdx.x; i < kWarps * E; i += kThreads) wh[i] = 0;
-  for (int e = threadIdx.x; e < E; e += kThreads) {
+  // Table pass: per expert, sums of hist over all chunks, the chunks before this
+  // one, and (EP) this sender's chunks, those before this chunk, earlier senders'.
+  // With E <= 128 the chunks are split over P = 2 or 4 threads per expert.
+  const int P = (4 * E <= kThreads) ? 4 : ((2 * E <= kThreads) ? 2 : 1);
+  for (int t = threadIdx.x; t < P * E; t += kThreads) {
+    const int e = t % E, q = t / E;
     int tot = 0, b_all = 0, b_s = 0, c_s = 0, c_sb = 0;
 #pragma unroll 16
-    for (int k = 0; k < NC; ++k) {
+    for (int k = q * NC / P; k < (q + 1) * NC / P; ++k) {
       const int h = __ldg(hist + static_cast<size_t>(k) * E + e);
       tot += h;
       if (k < c) b_all += h;
@@ -150,19 +171,37 @@ scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
         if (sk < s) c_sb += h;
       }
     }
-    off[e] = tot;
-    ball[e] = b_all;
-    if (EP) { bs[e] = b_s; cs[e] = c_s; craw[e] = c_s; csb[e] = c_sb; }
+    if (P == 1) {
+      off[e] = tot;
+      ball[e] = b_all;
+      if (EP) { bs[e] = b_s; cs[e] = c_s; craw[e] = c_s; csb[e] = c_sb; }
+    } else {
+      part[t] = tot;
+      part[kThreads + t] = b_all;
+      part[2 * kThreads + t] = b_s;
+      part[3 * kThreads + t] = c_s;
+      part[4 * kThreads + t] = c_sb;
+    }
+  }
+  if (P > 1) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+      int v[5] = {0, 0, 0, 0, 0};
+      for (int q = 0; q < P; ++q)
+#pragma unroll
+        for (int i = 0; i < 5; ++i) v[i] += part[i * kThreads + q * E + e];
+      off[e] = v[0];
+      ball[e] = v[1];
+      if (EP) { bs[e] = v[2]; cs[e] = v[3]; craw[e] = v[3]; csb[e] = v[4]; }
+    }
   }
   if (threadIdx.x == 0) { off[E] = 0; if (EP) { cs[E] = 0; csb[E] = 0; } }
   __syncthreads();
-  const int w = threadIdx.x >> 5;
   if (w == 0) warp_exscan(off, E + 1);
   if (EP && w == 1) warp_exscan(cs, E + 1);
   if (EP && w == 2) warp_exscan(csb, E + 1);
   // per-warp counts of this chunk
-  const long long wstart = start + static_cast<long long>(w) * kPerWarp;
-  warp_count(idx, wstart, end, wh + w * E);
+  warp_count(ev, wh + w * E);
   __syncthreads();
 
   if (c == 0 && (!EP || po.counts)) {   // counts and offsets (the EP pass writes them on request)
@@ -191,11 +230,11 @@ scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
 
   const int lane = threadIdx.x & 31;
   int* mine = wh + w * E;
-#pragma unroll 1
+#pragma unroll
   for (int st = 0; st < kSteps; ++st) {
     const long long a = wstart + st * 32 + lane;
     const bool valid = a < end;
-    const int e = valid ? __ldg(idx + a) : -1;
+    const int e = ev[st];
     const unsigned grp = __match_any_sync(0xffffffffu, e);
     const int before = valid ? mine[e] : 0;
     __syncwarp();
@@ -224,6 +263,12 @@ scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
   }
 }
 
+// Dynamic shared memory of scatter_kernel: the warp counts, the offset and
+// prefix tables (6E + 3 ints) and the table pass's partial sums (5 x kThreads).
+size_t scatter_smem_bytes(int E) {
+  return (static_cast<size_t>(kWarps) * E + 6 * E + 3 + 5 * kThreads) * sizeof(int);
+}
+
 size_t hist_bytes(long long TK, int E, int R) {
   const long long seg = TK / R;
   const long long cps = (seg + kChunk - 1) / kChunk;
@@ -238,7 +283,7 @@ int launch_counting_sort(bool ep, const int32_t* idx, long long TK, int E, int R
   const int NC = g.cps * R;
   int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kWorkspaceHeader);
   const size_t sh_hist = static_cast<size_t>(kWarps) * E * sizeof(int);
-  const size_t sh_scatter = sh_hist + static_cast<size_t>(6 * E + 3) * sizeof(int);
+  const size_t sh_scatter = scatter_smem_bytes(E);
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -442,7 +487,7 @@ extern "C" int moe_build_permutation_static(const int32_t* topk_idx, int T, int 
     g_static_smem_set[dev] = true;
   }
   const size_t sh_hist = static_cast<size_t>(kWarps) * E * sizeof(int);
-  const size_t sh_scatter = sh_hist + static_cast<size_t>(6 * E + 3) * sizeof(int);
+  const size_t sh_scatter = scatter_smem_bytes(E);
   PermOut po{counts, offsets, perm, inv_perm};
   EpOut eo{};
   {

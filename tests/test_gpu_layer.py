@@ -216,12 +216,12 @@ def test_run_from_host_pipelined_steps_match_device_path():
         assert torch.equal(dxh, want[b][1])
 
 
-@pytest.mark.parametrize("name", ["qwen3", "dsv2lite"])
-def test_layer_full_size_sampled_tokens(name):
+@pytest.mark.parametrize("name,n_tok", [("qwen3", 8), ("dsv2lite", 8), ("skew", 8), ("drafter", 3)])
+def test_layer_full_size_sampled_tokens(name, n_tok):
     """The benchmarked launch sequence at the workload's full size. Every output
     row of a token (out, dx, dlogits, its top-k) depends only on that token's
     inputs and on the experts it selects, so the oracle runs the layer on a
-    sample of 8 tokens restricted to the experts they select (relabelled in
+    sample of tokens restricted to the experts they select (relabelled in
     ascending order: with renormalised weights the top-k and its weights are the
     same among those experts as among all E, and the router gradient is zero
     elsewhere), and those rows are compared."""
@@ -233,7 +233,7 @@ def test_layer_full_size_sampled_tokens(name):
     dx = layer.backward(inp["dout"].to(dev())).clone()
     torch.cuda.synchronize()
     assert layer.device_status() == 0
-    toks = np.sort(np.random.default_rng(7).choice(cfg.T, size=8, replace=False))
+    toks = np.sort(np.random.default_rng(7).choice(cfg.T, size=n_tok, replace=False))
     tt = torch.from_numpy(toks)
     idx, _ = O.route_topk(W.to_f64(inp["logits"][tt]), cfg.K, cfg.renorm)
     used = np.unique(idx)

@@ -207,3 +207,40 @@ def test_grouped_ffn_backward_full_sampled(name):
     empty = np.nonzero(counts == 0)[0]
     for e in empty[:4]:
         assert float(dwg[int(e)].abs().max()) == 0.0 and float(dwd[int(e)].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("E", [600, 1024])
+def test_grouped_ffn_many_experts(E):
+    """Expert counts past the deep rings' shared-memory budget (the GEMMs fall back
+    to their shallower rings; the weight gradients use five stages above 440
+    experts), up to the largest supported E: sparse ragged sizes, many experts
+    empty, every row compared, forward and backward."""
+    rng = np.random.default_rng(E)
+    counts = np.where(rng.random(E) < 0.4, 0, rng.integers(1, 40, E))
+    d, I = 128, 128
+    off, xp, wg, wu, wd = _problem(counts.tolist(), d, I, E)
+    args = [to_dev(t, torch.bfloat16) for t in (xp,)] + [to_dev(off, torch.int32)] + \
+        [to_dev(t, torch.bfloat16) for t in (wg, wu, wd)]
+    y, h, gu = B.moe_grouped_ffn(*args)
+    ry, rgu, rh = O.grouped_ffn(xp.double().numpy(), off, wg.double().numpy(), wu.double().numpy(),
+                                wd.double().numpy(), pre=True)
+    assert_bf16_close(f64(h), rh, name="h")
+    assert_bf16_close(f64(gu), rgu, name="gu")
+    assert_out_close(f64(y), ry, name="y")
+    g = torch.Generator().manual_seed(E + 1)
+    M = int(off[-1])
+    dy = _bf16((M, d), g, 0.1)
+    gu_in = _bf16((M, 2 * I), g, 1.0)
+    h_in = _bf16((M, I), g, 0.5)
+    dxp, dwg, dwu, dwd = B.moe_grouped_ffn_backward(
+        to_dev(dy, torch.bfloat16), args[0], to_dev(gu_in, torch.bfloat16),
+        to_dev(h_in, torch.bfloat16), args[1], args[2], args[3], args[4])
+    r = O.grouped_ffn_backward(dy.double().numpy(), xp.double().numpy(), gu_in.double().numpy(),
+                               h_in.double().numpy(), off, wg.double().numpy(), wu.double().numpy(),
+                               wd.double().numpy(), pre=True)
+    assert_out_close(f64(dxp), r[0], name="dxp")
+    assert_rms_close(f64(dwg), r[1], name="dw_gate")
+    assert_rms_close(f64(dwu), r[2], name="dw_up")
+    assert_rms_close(f64(dwd), r[3], name="dw_down")
+    empty = counts == 0
+    assert (f64(dwg)[empty] == 0).all() and (f64(dwd)[empty] == 0).all()

@@ -32,7 +32,10 @@ def _bf16(shape, seed, scale=1.0):
 
 
 SHAPES = [(256, 128, 8, 2), (1000, 64, 16, 3), (777, 520, 32, 6), (8192, 2048, 128, 8),
-          (1, 8, 4, 4), (3000, 4096, 64, 8)]
+          (1, 8, 4, 4), (3000, 4096, 64, 8),
+          # K = 16 and 32 instances of the K-slot kernels; d = 8192 takes the
+          # per-row dispatch by perm (rows too long for the bulk-copy ring)
+          (100, 136, 64, 16), (50, 8192, 64, 32)]
 
 
 @pytest.mark.parametrize("T,d,E,K", SHAPES)

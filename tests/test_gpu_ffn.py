@@ -244,3 +244,27 @@ def test_grouped_ffn_many_experts(E):
     assert_rms_close(f64(dwd), r[3], name="dw_down")
     empty = counts == 0
     assert (f64(dwg)[empty] == 0).all() and (f64(dwd)[empty] == 0).all()
+
+
+def test_grouped_ffn_no_rows():
+    """A batch that routes no row to any expert (M = 0): the forward writes
+    nothing and returns, the backward writes zero weight gradients everywhere
+    (over whatever the output buffers held)."""
+    E, d, I = 4, 128, 128
+    off, xp, wg, wu, wd = _problem([0] * E, d, I, 3)
+    dv = [to_dev(t, torch.bfloat16) for t in (xp, wg, wu, wd)]
+    offd = to_dev(off, torch.int32)
+    y, h, gu = B.moe_grouped_ffn(dv[0], offd, dv[1], dv[2], dv[3])
+    assert y.shape[0] == 0 and h.shape[0] == 0
+    empty_rows = torch.empty(0, d, dtype=torch.bfloat16, device=dv[0].device)
+    out = (torch.empty(0, d, dtype=torch.bfloat16, device=dv[0].device),
+           torch.full((E, d, I), 7.0, device=dv[0].device),
+           torch.full((E, d, I), 7.0, device=dv[0].device),
+           torch.full((E, I, d), 7.0, device=dv[0].device))
+    dxp, dwg, dwu, dwd = B.moe_grouped_ffn_backward(
+        empty_rows, dv[0], torch.empty(0, 2 * I, dtype=torch.bfloat16, device=dv[0].device),
+        torch.empty(0, I, dtype=torch.bfloat16, device=dv[0].device), offd, dv[1], dv[2], dv[3],
+        out=out)
+    torch.cuda.synchronize()
+    assert dxp.shape[0] == 0
+    assert (dwg == 0).all() and (dwu == 0).all() and (dwd == 0).all()

@@ -174,4 +174,4 @@ extern "C" int moe_profile_record(int i, const char** name, float* ms) {
 
 extern "C" int moe_last_cuda_error(void) { return moe::g_last_cuda_error; }
 
-extern "C" int moe_version(void) { return 100; }
+extern "C" int moe_version(void) { return 200; }

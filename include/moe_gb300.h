@@ -330,7 +330,9 @@ const char* moe_status_string(int status);
 /* cudaError_t of the most recent MOE_ERR_CUDA on this host thread (0 if none). */
 int moe_last_cuda_error(void);
 
-/* Library version as major*10000 + minor*100 + patch. */
+/* Library version as major*10000 + minor*100 + patch. 0.2.0 added
+ * moe_dispatch_scatter and enlarged the MOE_OP_GROUPED_FFN_BACKWARD workspace
+ * (size it with moe_workspace_size). */
 int moe_version(void);
 
 #ifdef __cplusplus

@@ -50,7 +50,7 @@ def test_library_has_no_cpu_compute_symbols(lib):
 def test_status_strings_and_version(lib):
     assert lib.moe_status_string(0) == b"ok"
     assert b"workspace" in lib.moe_status_string(3)
-    assert lib.moe_version() >= 100
+    assert lib.moe_version() >= 200
 
 
 FAKE = ctypes.c_void_p(0x10000)          # aligned, never dereferenced

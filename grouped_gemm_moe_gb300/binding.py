@@ -57,6 +57,10 @@ SIGNATURES = {
     "moe_grouped_ffn": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_grouped_ffn_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                       _P, _P, _P, _SZ, _P]),
+    "moe_grouped_ffn_backward_data": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
+                                           _P, _SZ, _P]),
+    "moe_grouped_ffn_backward_weights": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
+                                              _SZ, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_combine_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_dispatch_backward": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
@@ -381,6 +385,42 @@ def moe_grouped_ffn_backward(dy, xp, gu, h, offsets, w_gate, w_up, w_down,
         _ptr(w_down), _ptr(dxp), _ptr(dwg), _ptr(dwu), _ptr(dwd), _ptr(ws), ws.numel(),
         _stream(dev)))
     return dxp, dwg, dwu, dwd
+
+
+def moe_grouped_ffn_backward_data(dy, xp, gu, h, offsets, w_gate, w_up, w_down,
+                                  ws: torch.Tensor, out: Optional[torch.Tensor] = None):
+    """The data part of moe_grouped_ffn_backward: returns dxp [M,d] bf16 and leaves
+    [dG | dU] and the padded straddling steps in ws for the weight part."""
+    for n, t in (("dy", dy), ("xp", xp), ("gu", gu), ("h", h)):
+        _need(t, torch.bfloat16, 2, n)
+    _need(offsets, torch.int32, 1, "offsets")
+    M, d = xp.shape
+    E, _, I = w_gate.shape
+    dxp = out if out is not None else torch.empty(M, d, dtype=torch.bfloat16, device=xp.device)
+    _check("moe_grouped_ffn_backward_data", load().moe_grouped_ffn_backward_data(
+        _ptr(dy), _ptr(xp), _ptr(gu), _ptr(h), _ptr(offsets), E, M, d, I, _ptr(w_gate), _ptr(w_up),
+        _ptr(w_down), _ptr(dxp), _ptr(ws), ws.numel(), _stream(xp.device)))
+    return dxp
+
+
+def moe_grouped_ffn_backward_weights(dy, xp, h, offsets, E: int, I: int, ws: torch.Tensor,
+                                     out=None):
+    """The weight part of moe_grouped_ffn_backward, after the data part on the same
+    stream with the same ws: returns (dw_gate, dw_up [E,d,I], dw_down [E,I,d]) fp32."""
+    for n, t in (("dy", dy), ("xp", xp), ("h", h)):
+        _need(t, torch.bfloat16, 2, n)
+    _need(offsets, torch.int32, 1, "offsets")
+    M, d = xp.shape
+    dev = xp.device
+    if out is None:
+        out = (torch.empty(E, d, I, dtype=torch.float32, device=dev),
+               torch.empty(E, d, I, dtype=torch.float32, device=dev),
+               torch.empty(E, I, d, dtype=torch.float32, device=dev))
+    dwg, dwu, dwd = out
+    _check("moe_grouped_ffn_backward_weights", load().moe_grouped_ffn_backward_weights(
+        _ptr(dy), _ptr(xp), _ptr(h), _ptr(offsets), E, M, d, I, _ptr(dwg), _ptr(dwu), _ptr(dwd),
+        _ptr(ws), ws.numel(), _stream(dev)))
+    return dwg, dwu, dwd
 
 
 def moe_combine(y: torch.Tensor, topk_w: torch.Tensor, inv_perm: torch.Tensor,

@@ -1451,25 +1451,35 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
   return launch_pair_bn<FWD_DOWN>(bn, ta, tb0, tb0, tc0, tc0, p, mt_upper * p.n_tiles, st);
 }
 
-extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
-                                        const moe_bf16* h, const int32_t* offsets, int E, int M,
-                                        int d, int I, const moe_bf16* w_gate, const moe_bf16* w_up,
-                                        const moe_bf16* w_down, moe_bf16* dxp, float* dw_gate,
-                                        float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
-                                        void* stream) {
+namespace {
+
+constexpr int kBwdData = 1;      // dH (with the weight gradients' padded steps) and dX
+constexpr int kBwdWeights = 2;   // the weight gradients
+
+// The backward GEMMs, in two parts that share the workspace: the data part
+// writes [dG | dU] and the padded straddling steps into it, the weight part
+// reads them. Arguments a part does not use may be null.
+int ffn_backward_parts(int parts, const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
+                       const moe_bf16* h, const int32_t* offsets, int E, int M, int d, int I,
+                       const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                       moe_bf16* dxp, float* dw_gate, float* dw_up, float* dw_down, void* ws,
+                       size_t ws_bytes, void* stream) {
   using namespace moe;
   using namespace moe::gemm;
+  const bool data = parts & kBwdData, weights = parts & kBwdWeights;
   if (!ffn_shape_ok(E, M, d, I) || d % 128 != 0) {
     if (E >= 1 && M >= 0 && d > 0 && I > 0 && d % 8 == 0 && I % 8 == 0) return MOE_ERR_UNSUPPORTED;
     return MOE_ERR_INVALID_ARG;
   }
-  if (!offsets || !w_gate || !w_up || !w_down || !dw_gate || !dw_up || !dw_down)
-    return MOE_ERR_INVALID_ARG;
-  if (M > 0 && (!dy || !xp || !gu || !h || !dxp)) return MOE_ERR_INVALID_ARG;
-  if ((M > 0 && (!aligned16(dy) || !aligned16(xp) || !aligned16(gu) || !aligned16(h) ||
-                 !aligned16(dxp))) ||
-      !aligned16(offsets) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
-      !aligned16(dw_gate) || !aligned16(dw_up) || !aligned16(dw_down))
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  if (data && (!w_gate || !w_up || !w_down)) return MOE_ERR_INVALID_ARG;
+  if (weights && (!dw_gate || !dw_up || !dw_down)) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!dy || !xp || !h || (data && (!gu || !dxp)))) return MOE_ERR_INVALID_ARG;
+  if ((M > 0 && (!aligned16(dy) || !aligned16(xp) || !aligned16(h) ||
+                 (data && (!aligned16(gu) || !aligned16(dxp))))) ||
+      !aligned16(offsets) ||
+      (data && (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down))) ||
+      (weights && (!aligned16(dw_gate) || !aligned16(dw_up) || !aligned16(dw_down))))
     return MOE_ERR_MISALIGNED;
   if (!ws || !aligned16(ws) || ws_bytes < kWorkspaceHeader + ffn_backward_scratch(M, E, d, I))
     return MOE_ERR_WORKSPACE;
@@ -1477,9 +1487,11 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   cudaStream_t st = as_stream(stream);
   const size_t wbytes = static_cast<size_t>(E) * d * I * sizeof(float);
   if (M == 0) {
-    cudaMemsetAsync(dw_gate, 0, wbytes, st);
-    cudaMemsetAsync(dw_up, 0, wbytes, st);
-    cudaMemsetAsync(dw_down, 0, wbytes, st);
+    if (weights) {
+      cudaMemsetAsync(dw_gate, 0, wbytes, st);
+      cudaMemsetAsync(dw_up, 0, wbytes, st);
+      cudaMemsetAsync(dw_down, 0, wbytes, st);
+    }
     return check_launch();
   }
   auto dgu = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + kWorkspaceHeader);
@@ -1495,38 +1507,42 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   p.status = static_cast<int*>(ws);
   const long long mt_upper = (M + BM - 1) / BM + E;
   CUtensorMap ta, tb0, tb1, tc0, tc1;
-  // dH = dY Wd^T with the SwiGLU backward epilogue -> [dG | dU]
-  const int bn_h = pair_bn(I);
-  if (!make_map(&ta, dy, d, M, 64, BM) ||
-      !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h / 2) ||
-      !make_map(&tc0, gu, 2 * static_cast<uint64_t>(I), M, 64, 32) ||
-      !make_map(&tc1, dgu, 2 * static_cast<uint64_t>(I), M, 64, 32))
-    return MOE_ERR_CUDA;
-  p.n_tiles = I / bn_h;
-  p.k_blocks = d / BK;
-  p.out = dgu;
-  p.aux = reinterpret_cast<const __nv_bfloat16*>(gu);
-  p.ld_out = 2 * I;
-  // the dH launch also fills the weight gradients' padded straddling steps
-  p.pad[0] = PadJob{reinterpret_cast<const __nv_bfloat16*>(xp), pad_x, d};
-  p.pad[1] = PadJob{reinterpret_cast<const __nv_bfloat16*>(h), pad_h, I};
-  int rc = launch_pair_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc1, p, mt_upper * p.n_tiles, st);
-  if (rc) return rc;
-  // dX = dG Wg^T + dU Wu^T
-  const int bn_x = pair_bn(d);
-  if (!make_map(&ta, dgu, 2 * static_cast<uint64_t>(I), M, 64, BM) ||
-      !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2) ||
-      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2) ||
-      !make_map(&tc0, dxp, d, M, 64, 32))
-    return MOE_ERR_CUDA;
-  p.n_tiles = d / bn_x;
-  p.k_blocks = 2 * I / BK;
-  p.out = reinterpret_cast<__nv_bfloat16*>(dxp);
-  p.aux = nullptr;
-  p.ld_out = d;
-  p.pad[0] = p.pad[1] = PadJob{nullptr, nullptr, 0};
-  rc = launch_pair_bn<BWD_DX>(bn_x, ta, tb0, tb1, tc0, tc0, p, mt_upper * p.n_tiles, st);
-  if (rc) return rc;
+  int rc = MOE_OK;
+  if (data) {
+    // dH = dY Wd^T with the SwiGLU backward epilogue -> [dG | dU]
+    const int bn_h = pair_bn(I);
+    if (!make_map(&ta, dy, d, M, 64, BM) ||
+        !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h / 2) ||
+        !make_map(&tc0, gu, 2 * static_cast<uint64_t>(I), M, 64, 32) ||
+        !make_map(&tc1, dgu, 2 * static_cast<uint64_t>(I), M, 64, 32))
+      return MOE_ERR_CUDA;
+    p.n_tiles = I / bn_h;
+    p.k_blocks = d / BK;
+    p.out = dgu;
+    p.aux = reinterpret_cast<const __nv_bfloat16*>(gu);
+    p.ld_out = 2 * I;
+    // the dH launch also fills the weight gradients' padded straddling steps
+    p.pad[0] = PadJob{reinterpret_cast<const __nv_bfloat16*>(xp), pad_x, d};
+    p.pad[1] = PadJob{reinterpret_cast<const __nv_bfloat16*>(h), pad_h, I};
+    rc = launch_pair_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc1, p, mt_upper * p.n_tiles, st);
+    if (rc) return rc;
+    // dX = dG Wg^T + dU Wu^T
+    const int bn_x = pair_bn(d);
+    if (!make_map(&ta, dgu, 2 * static_cast<uint64_t>(I), M, 64, BM) ||
+        !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2) ||
+        !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2) ||
+        !make_map(&tc0, dxp, d, M, 64, 32))
+      return MOE_ERR_CUDA;
+    p.n_tiles = d / bn_x;
+    p.k_blocks = 2 * I / BK;
+    p.out = reinterpret_cast<__nv_bfloat16*>(dxp);
+    p.aux = nullptr;
+    p.ld_out = d;
+    p.pad[0] = p.pad[1] = PadJob{nullptr, nullptr, 0};
+    rc = launch_pair_bn<BWD_DX>(bn_x, ta, tb0, tb1, tc0, tc0, p, mt_upper * p.n_tiles, st);
+    if (rc) return rc;
+  }
+  if (!weights) return MOE_OK;
   // [dWg | dWu] = X^T [dG | dU]
   CUtensorMap ta16, tpad;
   if (!make_map(&ta, xp, d, M, 64, 64) || !make_map(&tb0, dgu, 2 * static_cast<uint64_t>(I), M, 64, 64) ||
@@ -1555,6 +1571,40 @@ extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, 
   p.n_tiles = (d + 255) / 256;
   return launch_pair_wgrad<WGRAD_D>(ta, tb0, tc0, tc0, ta16, tpad, p,
                                     static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
+}
+
+}  // namespace
+
+extern "C" int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
+                                        const moe_bf16* h, const int32_t* offsets, int E, int M,
+                                        int d, int I, const moe_bf16* w_gate, const moe_bf16* w_up,
+                                        const moe_bf16* w_down, moe_bf16* dxp, float* dw_gate,
+                                        float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  if (!w_gate || !w_up || !w_down || !dw_gate || !dw_up || !dw_down) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && !gu) return MOE_ERR_INVALID_ARG;
+  return ffn_backward_parts(kBwdData | kBwdWeights, dy, xp, gu, h, offsets, E, M, d, I, w_gate,
+                            w_up, w_down, dxp, dw_gate, dw_up, dw_down, ws, ws_bytes, stream);
+}
+
+extern "C" int moe_grouped_ffn_backward_data(const moe_bf16* dy, const moe_bf16* xp,
+                                             const moe_bf16* gu, const moe_bf16* h,
+                                             const int32_t* offsets, int E, int M, int d, int I,
+                                             const moe_bf16* w_gate, const moe_bf16* w_up,
+                                             const moe_bf16* w_down, moe_bf16* dxp, void* ws,
+                                             size_t ws_bytes, void* stream) {
+  return ffn_backward_parts(kBwdData, dy, xp, gu, h, offsets, E, M, d, I, w_gate, w_up, w_down,
+                            dxp, nullptr, nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+extern "C" int moe_grouped_ffn_backward_weights(const moe_bf16* dy, const moe_bf16* xp,
+                                                const moe_bf16* h, const int32_t* offsets, int E,
+                                                int M, int d, int I, float* dw_gate, float* dw_up,
+                                                float* dw_down, void* ws, size_t ws_bytes,
+                                                void* stream) {
+  return ffn_backward_parts(kBwdWeights, dy, xp, nullptr, h, offsets, E, M, d, I, nullptr,
+                            nullptr, nullptr, nullptr, dw_gate, dw_up, dw_down, ws, ws_bytes,
+                            stream);
 }
 
 extern "C" int moe_debug_wait_timeout(void* ws, int timeout_us, void* stream) {

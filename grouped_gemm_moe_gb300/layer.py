@@ -6,8 +6,9 @@ Forward:  moe_route_topk -> moe_build_permutation_ep (the permutation and
           device-to-host copy of the splits) -> moe_dispatch_scatter ->
           moe_grouped_ffn (routed experts; shared experts as E=1 on x) ->
           moe_combine.
-Backward: moe_combine_backward -> moe_grouped_ffn_backward (routed; shared)
-          -> moe_dispatch_backward -> moe_route_topk_backward.
+Backward: moe_combine_backward -> moe_grouped_ffn_backward_data (routed; shared)
+          -> moe_dispatch_backward -> moe_grouped_ffn_backward_weights (routed;
+          shared) -> moe_route_topk_backward.
 
 With aux_loss_coef > 0 the forward also runs moe_load_balance (per-expert load
 fractions, mean router probabilities, the load-balance loss and load metrics,
@@ -138,17 +139,26 @@ class MoELayer:
         w = self.w
         self._run("combine_backward", B.moe_combine_backward, dout, self.y, self.topk_w,
                   self.inv_perm, out=(self.dy, self.dtopk_w))
-        self._run("grouped_ffn_backward", B.moe_grouped_ffn_backward, self.dy, self.xp, self.gu,
-                  self.h, self.offsets, w["w_gate"], w["w_up"], w["w_down"], ws=self.ws_bwd,
-                  out=(self.dxp, self.dw_gate, self.dw_up, self.dw_down))
+        # data parts first, then the gather of dx while the GEMMs' dX rows are still
+        # in L2, then the weight gradients
+        self._run("grouped_ffn_backward_data", B.moe_grouped_ffn_backward_data, self.dy, self.xp,
+                  self.gu, self.h, self.offsets, w["w_gate"], w["w_up"], w["w_down"],
+                  ws=self.ws_bwd, out=self.dxp)
         dxs = None
         if self.shared:
-            self._run("shared_ffn_backward", B.moe_grouped_ffn_backward, dout, self.x, self.gus,
-                      self.hs, self.s_offsets, self.ws_g, self.ws_u, self.ws_d, ws=self.ws_sbwd,
-                      out=(self.dxs, self.dws_gate, self.dws_up, self.dws_down))
+            self._run("shared_ffn_backward_data", B.moe_grouped_ffn_backward_data, dout, self.x,
+                      self.gus, self.hs, self.s_offsets, self.ws_g, self.ws_u, self.ws_d,
+                      ws=self.ws_sbwd, out=self.dxs)
             dxs = self.dxs
         self._run("dispatch_backward", B.moe_dispatch_backward, self.dxp, self.inv_perm, self.T,
                   self.K, dxs, out=self.dx)
+        self._run("grouped_ffn_backward_weights", B.moe_grouped_ffn_backward_weights, self.dy,
+                  self.xp, self.h, self.offsets, self.E, self.I, ws=self.ws_bwd,
+                  out=(self.dw_gate, self.dw_up, self.dw_down))
+        if self.shared:
+            self._run("shared_ffn_backward_weights", B.moe_grouped_ffn_backward_weights, dout,
+                      self.x, self.hs, self.s_offsets, 1, self.Is, ws=self.ws_sbwd,
+                      out=(self.dws_gate, self.dws_up, self.dws_down))
         self._run("route_topk_backward", B.moe_route_topk_backward,
                   None if self.renorm else self.logits, self.topk_idx, self.topk_w, self.dtopk_w,
                   self.E, self.renorm, out=self.dlogits)

@@ -271,6 +271,24 @@ int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_b
                              float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
                              void* stream);
 
+/* B2 in two parts, the same work as moe_grouped_ffn_backward: the data part
+ * computes dH, [dG | dU] (kept in ws) and dX, and prepares in ws the padded
+ * straddling steps the weight part reads; the weight part computes dWg, dWu,
+ * dWd from ws. Issue the weight part after the data part on the same stream,
+ * with the same ws, dy, xp, h, offsets and sizes; work may run in between
+ * (a caller can consume dxp while its rows are still in L2). Arguments,
+ * layouts, limits and errors as moe_grouped_ffn_backward, for the arguments
+ * each part takes. */
+int moe_grouped_ffn_backward_data(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
+                                  const moe_bf16* h, const int32_t* offsets, int E, int M, int d,
+                                  int I, const moe_bf16* w_gate, const moe_bf16* w_up,
+                                  const moe_bf16* w_down, moe_bf16* dxp, void* ws,
+                                  size_t ws_bytes, void* stream);
+int moe_grouped_ffn_backward_weights(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* h,
+                                     const int32_t* offsets, int E, int M, int d, int I,
+                                     float* dw_gate, float* dw_up, float* dw_down, void* ws,
+                                     size_t ws_bytes, void* stream);
+
 /* A7. Combine ([TAS] "Dispatch, expert computation and combine", last
  * paragraph: undo the packing with the saved indices, weight each expert
  * output by its router weight, sum the K outputs; [SF] "What this adds": the

@@ -104,6 +104,20 @@ def test_argument_validation_rows_and_gemm(lib):
     g = lib.moe_grouped_ffn_backward
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
              FAKE, FAKE, 256, None) == B.MOE_ERR_WORKSPACE
+    gd = lib.moe_grouped_ffn_backward_data
+    assert gd(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, FAKE, FAKE, FAKE, FAKE, FAKE, 256,
+              None) == B.MOE_ERR_WORKSPACE
+    assert gd(FAKE, FAKE, None, FAKE, FAKE, 4, 256, 128, 256, FAKE, FAKE, FAKE, FAKE, FAKE, 256,
+              None) == B.MOE_ERR_INVALID_ARG                                          # gu
+    assert gd(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, None, FAKE, FAKE, FAKE, FAKE, 256,
+              None) == B.MOE_ERR_INVALID_ARG                                          # w_gate
+    gw = lib.moe_grouped_ffn_backward_weights
+    assert gw(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, FAKE, FAKE, FAKE, FAKE, 256,
+              None) == B.MOE_ERR_WORKSPACE
+    assert gw(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, FAKE, None, FAKE, FAKE, 256,
+              None) == B.MOE_ERR_INVALID_ARG                                          # dw_up
+    assert gw(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, FAKE, MIS, FAKE, FAKE, 1 << 30,
+              None) == B.MOE_ERR_MISALIGNED
 
 
 def test_debug_wait_argument_checks(lib):

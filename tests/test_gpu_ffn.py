@@ -268,3 +268,30 @@ def test_grouped_ffn_no_rows():
     torch.cuda.synchronize()
     assert dxp.shape[0] == 0
     assert (dwg == 0).all() and (dwu == 0).all() and (dwd == 0).all()
+
+
+@pytest.mark.parametrize("counts,d,I", [SMALL[0], SMALL[-1]])
+def test_grouped_ffn_backward_split_matches_whole(counts, d, I):
+    """The data part then the weight part (with another kernel in between on the
+    same stream) give bit-identical results to the single backward call."""
+    off, xp, wg, wu, wd = _problem(counts, d, I, 5 * sum(counts) + I)
+    g = torch.Generator().manual_seed(13)
+    M = int(off[-1])
+    dy, gu, h = _bf16((M, d), g, 0.1), _bf16((M, 2 * I), g, 1.0), _bf16((M, I), g, 0.5)
+    dv = {k: to_dev(t, torch.bfloat16) for k, t in
+          (("dy", dy), ("xp", xp), ("gu", gu), ("h", h), ("wg", wg), ("wu", wu), ("wd", wd))}
+    offd = to_dev(off, torch.int32)
+    whole = B.moe_grouped_ffn_backward(dv["dy"], dv["xp"], dv["gu"], dv["h"], offd, dv["wg"],
+                                       dv["wu"], dv["wd"])
+    E = len(counts)
+    ws = B.new_workspace(B.workspace_size(B.MOE_OP_GROUPED_FFN_BACKWARD, M, E, 1, 1, d, I),
+                         dv["xp"].device)
+    dxp = B.moe_grouped_ffn_backward_data(dv["dy"], dv["xp"], dv["gu"], dv["h"], offd, dv["wg"],
+                                          dv["wu"], dv["wd"], ws=ws)
+    between = B.moe_grouped_ffn(dv["xp"], offd, dv["wg"], dv["wu"], dv["wd"])   # other work
+    dws = B.moe_grouped_ffn_backward_weights(dv["dy"], dv["xp"], dv["h"], offd, E, I, ws=ws)
+    torch.cuda.synchronize()
+    del between
+    assert torch.equal(dxp, whole[0])
+    for got, want in zip(dws, whole[1:]):
+        assert torch.equal(got, want)

@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--config", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-side-configs", action="store_true",
+                    help="report only the headline workload (no configs sub-object)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--profile-case", choices=["gemm", "gemm_ragged", "gemm_l2", "layer", "hbm",
                                                "routing"],
@@ -278,12 +280,12 @@ def code_digest(path: str) -> str:
     return hashlib.sha256("\n".join(out).encode()).hexdigest()
 
 
-def measured_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from a committed ncu summary under
-    profiles/: a line 'traffic-record: kernel=<name> bytes_per_launch=<B>
-    source=<file> code-sha256=<hex>'. The figure counts only while the
-    kernel's source file still has the recorded code digest (code_digest;
-    None otherwise)."""
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu
+    summary under profiles/: a line 'traffic-record: kernel=<name>
+    workload=<name> bytes_per_launch=<B> source=<file> code-sha256=<hex>'. The
+    figure counts only while the kernel's source file still has the recorded
+    code digest (code_digest; None otherwise)."""
     import glob
     here = os.path.dirname(os.path.abspath(__file__))
     src = next((f for pre, f in KERNEL_SOURCE.items() if kernel.startswith(pre)), None)
@@ -298,7 +300,8 @@ def measured_traffic(kernel: str):
             if not line.startswith("traffic-record:"):
                 continue
             kv = dict(f.split("=", 1) for f in line.split()[1:] if "=" in f)
-            if kv.get("kernel") == kernel and kv.get("source") == src and kv.get("code-sha256") == digest:
+            if (kv.get("kernel") == kernel and kv.get("workload") == workload
+                    and kv.get("source") == src and kv.get("code-sha256") == digest):
                 return float(kv["bytes_per_launch"])
     return None
 
@@ -382,27 +385,56 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle
 class OracleSample:
-    """The CPU oracle on a bounded token sample of a workload. Inputs are drawn
-    once (full-size expert weights, up to ``t_max`` tokens) and converted to
-    float64 once; a step runs the oracle's forward and backward on the first T
-    tokens, and only that is timed."""
+    """The CPU oracle on a bounded token sample of a workload. A step runs the
+    oracle's forward and backward on the first T tokens, restricted to the
+    experts those tokens select (relabelled in ascending order; with
+    renormalised weights the selection and its weights are the same among them
+    as among all E, and every other expert's work is zero); only that is timed.
+    Token inputs are converted to float64 once; expert weights stay as
+    bf16-exact float32 arrays, which the oracle converts one expert at a time,
+    so a large workload's weights are never held in float64 all at once."""
 
-    def __init__(self, cfg, t_max: int = 512):
+    WEIGHTS = ("w_gate", "w_up", "w_down")
+    SHARED = ("ws_gate", "ws_up", "ws_down")
+
+    def __init__(self, cfg, inputs=None, t_max: int = 512):
         from grouped_gemm_moe_gb300 import workloads as W
         self.cfg = cfg
         t_max -= t_max % cfg.R
-        inp = W.make_inputs(cfg, T=t_max, with_backward=True)
-        self.np = {k: W.to_f64(v) for k, v in inp.items()}
+        if inputs is None:
+            inputs = W.make_inputs(cfg, T=t_max, with_backward=True)
+        t_max = min(t_max, inputs["logits"].shape[0])
+        self.tok = {k: W.to_f64(inputs[k][:t_max]) for k in ("logits", "x", "dout")}
+        self.wts = {k: inputs[k].float().numpy() for k in self.WEIGHTS + self.SHARED
+                    if k in inputs}
         self.t_max = t_max
+        self._cached = (None, None)
+
+    def inputs(self, T: int):
+        if self._cached[0] == T:
+            return self._cached[1]
+        import numpy as np
+        from oracle import moe_oracle as O
+        lg = self.tok["logits"][:T]
+        idx, _ = O.route_topk(lg, self.cfg.K, self.cfg.renorm)
+        used = np.unique(idx)
+        whole = len(used) == self.cfg.E
+        sub = {"logits": lg if whole else lg[:, used], "x": self.tok["x"][:T],
+               "dout": self.tok["dout"][:T]}
+        for k in self.WEIGHTS:
+            sub[k] = self.wts[k] if whole else self.wts[k][used]
+        for k in self.SHARED:
+            if k in self.wts:
+                sub[k] = self.wts[k]
+        self._cached = (T, sub)
+        return sub
 
     def step(self, T: int) -> float:
         from oracle import moe_oracle as O
         cfg = self.cfg
-        inp = dict(self.np)
-        for k in ("logits", "x", "dout"):
-            inp[k] = self.np[k][:T]
+        inp = self.inputs(T)
         t0 = time.perf_counter()
-        fwd = O.layer_forward(inp, cfg.K, cfg.R, cfg.renorm)
+        fwd = O.layer_forward(inp, cfg.K, 1, cfg.renorm)
         O.layer_backward(inp, fwd, inp["dout"], cfg.K, cfg.renorm)
         return time.perf_counter() - t0
 
@@ -427,14 +459,15 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(cfg, tokens):
-    smp = OracleSample(cfg)
+def cpu_baseline(cfg, tokens, inputs=None):
+    smp = OracleSample(cfg, inputs)
     if tokens <= 0:
         tokens = smp.tokens_for(15.0)
     dt = smp.step(tokens)
     return {"value": tokens / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{tokens} of {cfg.T} tokens of the same workload (full expert weights), "
-                      f"fwd+bwd, float64 NumPy, one run of {dt:.2f} s"}
+            "sample": f"the first {tokens} of {cfg.T} tokens of the same workload, fwd+bwd, "
+                      f"restricted to the experts they select (full-size expert weights), "
+                      f"float64 NumPy, one run of {dt:.2f} s"}
 
 
 def run_reference(args, cfg, world, rank):
@@ -457,7 +490,8 @@ def run_reference(args, cfg, world, rank):
         "config": {"workload": f"{cfg.name}: {W.describe(cfg)}, fwd+bwd",
                    "sample_tokens_per_step": tokens},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"{tokens} of {cfg.T} tokens per step (full expert weights), "
+                         "sample": f"the first {tokens} of {cfg.T} tokens per step, restricted to "
+                                   f"the experts they select (full-size expert weights), "
                                    f"float64 NumPy oracle"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -465,6 +499,166 @@ def run_reference(args, cfg, world, rank):
 
 
 # ------------------------------------------------------------------ GPU arm
+class Runner:
+    """Times one workload's layer forward + backward on one GPU: K steps with
+    per-step events (L2 flushed before each, outside the events), the same K
+    steps again (A/A), and a third pass with the library's per-launch events
+    for the per-kernel table."""
+
+    def __init__(self, cfg, inputs, dev, flush_l2, world):
+        import torch
+        from grouped_gemm_moe_gb300 import layer as L
+        self.cfg, self.dev, self.flush_l2, self.world = cfg, dev, flush_l2, world
+        self.layer = L.layer_from_config(cfg, inputs, dev)
+        self.logits, self.x, self.dout = (inputs[k].to(dev) for k in ("logits", "x", "dout"))
+        self.stream = torch.cuda.current_stream(dev)
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def step(self):
+        self.layer.forward(self.logits, self.x)
+        self.layer.backward(self.dout)
+
+    def warm(self, n: int, min_seconds: float = 0.0):
+        import torch
+        t0 = time.time()
+        for _ in range(max(n, 3)):
+            self.flush_l2()
+            self.step()
+        torch.cuda.synchronize()
+        # keep the GPU busy long enough for the clock sampler to see it under load
+        while time.time() - t0 < min_seconds:
+            self.step()
+            torch.cuda.synchronize()
+        if self.layer.device_status() != 0:
+            raise SystemExit("device status word reports an error")
+
+    def timed(self, steps: int):
+        import torch
+        self.barrier()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(steps):
+            self.flush_l2()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(self.stream)
+            self.step()
+            e.record(self.stream)
+            evs.append((s, e))
+        torch.cuda.synchronize()
+        self.barrier()
+        return [s.elapsed_time(e) for s, e in evs]
+
+    def per_launch(self, steps: int):
+        import torch
+        from grouped_gemm_moe_gb300 import binding as B
+        B.moe_profile_start(64 * steps + 64)
+        for _ in range(steps):
+            self.flush_l2()
+            self.step()
+        torch.cuda.synchronize()
+        self.barrier()
+        return B.moe_profile_stop()
+
+
+def kernel_table(cfg, records, steps, pk):
+    """Per-kernel launches, average duration, share and roofline, and the
+    per-step algorithmic totals."""
+    per = {}
+    for n, kms, sh in label_records(records, steps):
+        key = n + ("[shared]" if sh else "")
+        c = per.setdefault(key, {"launches": 0, "total_ms": 0.0, "shared": sh, "name": n})
+        c["launches"] += 1
+        c["total_ms"] += kms
+    tot = sum(c["total_ms"] for c in per.values()) or 1.0
+    kernels = {}
+    for k, c in per.items():
+        fl, nb = kernel_work(c["name"], cfg, c["shared"])
+        avg = c["total_ms"] / c["launches"]
+        rf = roofline_of(fl, nb, avg, pk)
+        kernels[k] = {"launches": c["launches"], "avg_ms": round(avg, 5),
+                      "share": round(c["total_ms"] / tot, 4), "bound": rf["bound"],
+                      "achieved": round(rf["achieved"], 1), "unit": rf["unit"],
+                      "frac": round(rf["frac"], 4), "roofline_ms": round(rf["roofline_ms"], 5)}
+    flops_step = sum(kernel_work(c["name"], cfg, c["shared"])[0] * c["launches"]
+                     for c in per.values()) / steps
+    bytes_step = sum(kernel_work(c["name"], cfg, c["shared"])[1] * c["launches"]
+                     for c in per.values()) / steps
+    layer_roof_ms = max(flops_step / (pk["bf16_tflops_sustained"] * 1e12),
+                        bytes_step / (pk["hbm_gbs"] * 1e9)) * 1e3
+    sum_roof_ms = sum(v["roofline_ms"] * v["launches"] for v in kernels.values()) / steps
+    return per, kernels, flops_step, bytes_step, layer_roof_ms, sum_roof_ms
+
+
+def side_config(name, args, dev, flush_l2, world, rank, pk):
+    """One of the other forward + backward workloads: its step time, tokens/s,
+    layer fraction of roofline and kernel table (fewer steps than the headline)."""
+    import torch
+    from grouped_gemm_moe_gb300 import workloads as W
+    cfg = W.CONFIGS[name]
+    inp = W.make_inputs(cfg, seed=cfg.seed + rank)
+    run = Runner(cfg, inp, dev, flush_l2, world)
+    steps = max(5, min(args.steps, 10))
+    run.warm(3)
+    step_ms = run.timed(steps)
+    records = run.per_launch(steps)
+    _, kernels, fl, nb, roof_ms, sum_ms = kernel_table(cfg, records, steps, pk)
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
+    out = {"workload": f"{cfg.name}: {W.describe(cfg)}, fwd+bwd", "steps": steps,
+           "ms_per_step": ms, "step_ms_median": statistics.median(step_ms),
+           "tokens_per_s": aggregate_value(ms, cfg.T, world),
+           "step_tflop": fl / 1e12, "step_gbytes_algorithmic": nb / 1e9,
+           "layer_roofline_ms": roof_ms, "layer_frac_of_roofline": roof_ms / ms,
+           "sum_of_kernel_rooflines_ms": sum_ms, "gpu_launches": len(records),
+           "kernels": kernels}
+    del run, inp
+    torch.cuda.empty_cache()
+    return out
+
+
+def load_balance_block(cfg, layer, logits, dev, flush_l2, steps, pk):
+    """Load-balance metrics, loss and gradient on the headline routing (not part
+    of the headline step): K timed iterations with per-launch events, L2
+    flushed before each."""
+    import torch
+    from grouped_gemm_moe_gb300 import binding as B
+    from grouped_gemm_moe_gb300 import workloads as W
+    lb_frac, lb_pmean, lb_stats = (torch.empty(cfg.E, device=dev), torch.empty(cfg.E, device=dev),
+                                   torch.empty(4, device=dev))
+    lb_ws = B.new_workspace(B.workspace_size(B.MOE_OP_LOAD_BALANCE, cfg.T, cfg.E, cfg.K), dev)
+    lb_dl = torch.zeros(cfg.T, cfg.E, device=dev)
+    for _ in range(3):
+        B.moe_load_balance(logits, layer.counts, cfg.K, ws=lb_ws, out=(lb_frac, lb_pmean, lb_stats))
+        B.moe_load_balance_backward(logits, lb_frac, 0.01, dlogits=lb_dl, accumulate=True)
+    torch.cuda.synchronize()
+    B.moe_profile_start(16 * steps + 16)
+    for _ in range(steps):
+        flush_l2()
+        B.moe_load_balance(logits, layer.counts, cfg.K, ws=lb_ws, out=(lb_frac, lb_pmean, lb_stats))
+        B.moe_load_balance_backward(logits, lb_frac, 0.01, dlogits=lb_dl, accumulate=True)
+    torch.cuda.synchronize()
+    lb_rec = {}
+    for n, kms in B.moe_profile_stop():
+        lb_rec.setdefault(n, []).append(kms)
+    TE = cfg.T * cfg.E
+    lb_bytes = {"load_balance": 4 * TE, "load_balance_final": 4 * 256 * cfg.E + 12 * cfg.E,
+                "load_balance_backward": 12 * TE + 4 * cfg.E}
+    out = {"workload": f"{cfg.name} routing, logits [{cfg.T},{cfg.E}] fp32", "kernels": {}}
+    for n, v in lb_rec.items():
+        avg = statistics.mean(v)
+        bw = lb_bytes.get(n, 0) / (avg * 1e-3) / 1e9
+        out["kernels"][n] = {"launches": len(v), "avg_us": round(avg * 1e3, 2),
+                             "bytes": lb_bytes.get(n, 0), "achieved_gbs": round(bw, 1),
+                             "frac_hbm": round(bw / pk["hbm_gbs"], 4)}
+    out["loss"] = float(lb_stats[0])
+    out["max_over_uniform"] = float(lb_stats[1])
+    del lb_dl
+    return out
+
+
 def main():
     args = parse()
     if args.profile_case:
@@ -480,7 +674,6 @@ def main():
     import torch.distributed as dist
     from grouped_gemm_moe_gb300 import binding as B
     from grouped_gemm_moe_gb300 import build as build_mod
-    from grouped_gemm_moe_gb300 import layer as L
 
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -493,8 +686,6 @@ def main():
         raise SystemExit("the benchmark workload must include the backward pass")
 
     inp = W.make_inputs(cfg, seed=cfg.seed + rank)
-    layer = L.layer_from_config(cfg, inp, dev)
-    logits, x, dout = (inp[k].to(dev) for k in ("logits", "x", "dout"))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -503,7 +694,9 @@ def main():
         # L2 holding none of its data and no dirty lines left to write back
         flush.zero_()
         flush_rd.sum()
-    stream = torch.cuda.current_stream(dev)
+
+    run = Runner(cfg, inp, dev, flush_l2, world)
+    layer, stream = run.layer, run.stream
 
     props = torch.cuda.get_device_properties(dev)
     gpu_id = str(getattr(props, "uuid", local))
@@ -511,83 +704,22 @@ def main():
         gpu_id = "GPU-" + gpu_id
     sampler = ClockSampler(gpu_id) if rank == 0 else None
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    t_warm = time.time()
-    for i in range(max(args.warmup, 3)):
-        flush_l2()
-        layer.forward(logits, x)
-        layer.backward(dout)
-    torch.cuda.synchronize()
-    # keep the GPU busy long enough for the clock sampler to see it under load
-    while time.time() - t_warm < 1.5:
-        layer.forward(logits, x)
-        layer.backward(dout)
-        torch.cuda.synchronize()
-    if layer.device_status() != 0:
-        raise SystemExit("device status word reports an error")
-
-    barrier()
-    torch.cuda.synchronize()
-    evs = []
-    for i in range(args.steps):
-        flush_l2()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        layer.forward(logits, x)
-        layer.backward(dout)
-        e.record(stream)
-        evs.append((s, e))
-    torch.cuda.synchronize()
-    barrier()
-    step_ms = [s.elapsed_time(e) for s, e in evs]
+    run.warm(args.warmup, min_seconds=1.5)
+    step_ms = run.timed(args.steps)
     # A/A: the same K steps again, back to back, for the run-to-run noise floor
-    evs2 = []
-    for i in range(args.steps):
-        flush_l2()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        layer.forward(logits, x)
-        layer.backward(dout)
-        e.record(stream)
-        evs2.append((s, e))
-    torch.cuda.synchronize()
-    barrier()
-    step_ms_aa = [s.elapsed_time(e) for s, e in evs2]
+    step_ms_aa = run.timed(args.steps)
     # per-kernel durations: the same K steps again, each library launch bracketed by
-    # events on its stream (kept out of the pass above, where events between launches
+    # events on its stream (kept out of the passes above, where events between launches
     # would hold back each kernel's early launch behind its predecessor)
-    B.moe_profile_start(64 * args.steps + 64)
-    for i in range(args.steps):
-        flush_l2()
-        layer.forward(logits, x)
-        layer.backward(dout)
-    torch.cuda.synchronize()
-    barrier()
-    records = B.moe_profile_stop()
+    records = run.per_launch(args.steps)
+    clocks = sampler.stop() if sampler else None
     ms = max_over_ranks(statistics.mean(step_ms), world, dev)
     value = aggregate_value(ms, cfg.T, world)
 
     # per-kernel table and the dominant kernel's roofline
     pk = peaks()
-    per = {}
-    for n, kms, sh in label_records(records, args.steps):
-        key = n + ("[shared]" if sh else "")
-        c = per.setdefault(key, {"launches": 0, "total_ms": 0.0, "shared": sh, "name": n})
-        c["launches"] += 1
-        c["total_ms"] += kms
-    tot = sum(c["total_ms"] for c in per.values()) or 1.0
-    kernels = {}
-    for k, c in per.items():
-        fl, nb = kernel_work(c["name"], cfg, c["shared"])
-        avg = c["total_ms"] / c["launches"]
-        rf = roofline_of(fl, nb, avg, pk)
-        kernels[k] = {"launches": c["launches"], "avg_ms": round(avg, 5),
-                      "share": round(c["total_ms"] / tot, 4), "bound": rf["bound"],
-                      "achieved": round(rf["achieved"], 1), "unit": rf["unit"],
-                      "frac": round(rf["frac"], 4), "roofline_ms": round(rf["roofline_ms"], 5)}
+    per, kernels, flops_step, bytes_step, layer_roof_ms, sum_roof_ms = kernel_table(
+        cfg, records, args.steps, pk)
     dom = max(per, key=lambda k: per[k]["total_ms"])
     dfl, dnb = kernel_work(per[dom]["name"], cfg, per[dom]["shared"])
     davg = per[dom]["total_ms"] / per[dom]["launches"]
@@ -596,51 +728,13 @@ def main():
             "unit": rf["unit"], "frac": rf["frac"],
             "peak_source": pk["source"] + (" bf16 sustained" if rf["bound"] == "tensor"
                                            else " HBM copy (read+write)"),
-            "traffic": measured_traffic(dom),
+            "traffic": measured_traffic(dom, cfg.name),
             "frac_of_nominal": rf["achieved"] / (NOMINAL_TFLOPS if rf["bound"] == "tensor"
                                                  else NOMINAL_GBS),
             "work_per_launch": {"flop": dfl, "bytes": dnb},
             "avg_launch_ms": davg}
-    flops_step = sum(kernel_work(c["name"], cfg, c["shared"])[0] * c["launches"]
-                     for c in per.values()) / args.steps
-    bytes_step = sum(kernel_work(c["name"], cfg, c["shared"])[1] * c["launches"]
-                     for c in per.values()) / args.steps
-    layer_roof_ms = max(flops_step / (pk["bf16_tflops_sustained"] * 1e12),
-                        bytes_step / (pk["hbm_gbs"] * 1e9)) * 1e3
-    sum_roof_ms = sum(v["roofline_ms"] * v["launches"] for v in kernels.values()) / args.steps
 
-    # load-balance metrics, loss and gradient on the same routing (not part of the
-    # headline step): K timed iterations with per-launch events, L2 flushed before each
-    lb_frac, lb_pmean, lb_stats = (torch.empty(cfg.E, device=dev), torch.empty(cfg.E, device=dev),
-                                   torch.empty(4, device=dev))
-    lb_ws = B.new_workspace(B.workspace_size(B.MOE_OP_LOAD_BALANCE, cfg.T, cfg.E, cfg.K), dev)
-    lb_dl = torch.zeros(cfg.T, cfg.E, device=dev)
-    for _ in range(3):
-        B.moe_load_balance(logits, layer.counts, cfg.K, ws=lb_ws, out=(lb_frac, lb_pmean, lb_stats))
-        B.moe_load_balance_backward(logits, lb_frac, 0.01, dlogits=lb_dl, accumulate=True)
-    torch.cuda.synchronize()
-    B.moe_profile_start(16 * args.steps + 16)
-    for _ in range(args.steps):
-        flush_l2()
-        B.moe_load_balance(logits, layer.counts, cfg.K, ws=lb_ws, out=(lb_frac, lb_pmean, lb_stats))
-        B.moe_load_balance_backward(logits, lb_frac, 0.01, dlogits=lb_dl, accumulate=True)
-    torch.cuda.synchronize()
-    lb_rec = {}
-    for n, kms in B.moe_profile_stop():
-        lb_rec.setdefault(n, []).append(kms)
-    TE = cfg.T * cfg.E
-    lb_bytes = {"load_balance": 4 * TE, "load_balance_final": 4 * 256 * cfg.E + 12 * cfg.E,
-                "load_balance_backward": 12 * TE + 4 * cfg.E}
-    load_balance = {"workload": "qwen3 routing, logits [8192,128] fp32", "kernels": {}}
-    for n, v in lb_rec.items():
-        avg = statistics.mean(v)
-        bw = lb_bytes.get(n, 0) / (avg * 1e-3) / 1e9
-        load_balance["kernels"][n] = {"launches": len(v), "avg_us": round(avg * 1e3, 2),
-                                      "bytes": lb_bytes.get(n, 0), "achieved_gbs": round(bw, 1),
-                                      "frac_hbm": round(bw / pk["hbm_gbs"], 4)}
-    load_balance["loss"] = float(lb_stats[0])
-    load_balance["max_over_uniform"] = float(lb_stats[1])
-    clocks = sampler.stop() if sampler else None
+    load_balance = load_balance_block(cfg, layer, run.logits, dev, flush_l2, args.steps, pk)
 
     # end to end through the layer API with pinned host buffers
     e2e = None
@@ -651,20 +745,33 @@ def main():
         dx_h = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
         layer.run_from_host([(lh, xh, dh, out_h, dx_h)] * 2)
         torch.cuda.synchronize()
-        barrier()
+        run.barrier()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
         h2d, d2h = layer.run_from_host([(lh, xh, dh, out_h, dx_h)] * args.steps)
         e.record(stream)
         torch.cuda.synchronize()
-        barrier()
+        run.barrier()
         ems = max_over_ranks(s.elapsed_time(e) / args.steps, world, dev)
         e2e = {"value": aggregate_value(ems, cfg.T, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems,
+               "l2": (f"not flushed between steps: the steps run back to back, each step's "
+                      f"uploads and downloads overlapping its neighbours' compute; one step "
+                      f"moves {bytes_step / 1e9:.1f} GB of algorithmic traffic, "
+                      f"{bytes_step / (129 << 20):.0f}x the 129 MB L2")}
+        del lh, xh, dh, out_h, dx_h
+
+    # the other forward + backward workloads (shorter runs), after the headline
+    del run, layer
+    torch.cuda.empty_cache()
+    configs = {}
+    if not args.no_side_configs and args.config is None:
+        for name in W.SIDE_CONFIGS:
+            configs[name] = side_config(name, args, dev, flush_l2, world, rank, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(cfg, args.cpu_sample_tokens)
+        cpu = cpu_baseline(cfg, args.cpu_sample_tokens, inp)
 
     if rank == 0:
         line = {
@@ -682,13 +789,14 @@ def main():
                        "layer_frac_of_roofline": layer_roof_ms / ms,
                        "sum_of_kernel_rooflines_ms": sum_roof_ms},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": len(records), "clocks": clocks, "load_balance": load_balance,
+            "gpu_launches": len(records), "clocks": clocks,
             "step_ms_min_max": [min(step_ms), max(step_ms)],
             "step_ms_median": statistics.median(step_ms),
             "aa": {"ms_per_step": statistics.mean(step_ms_aa),
                    "rel_diff": abs(statistics.mean(step_ms_aa) - statistics.mean(step_ms))
                    / statistics.mean(step_ms)},
-            "kernels": kernels, "device": torch.cuda.get_device_name(dev),
+            "kernels": kernels, "configs": configs, "load_balance": load_balance,
+            "device": torch.cuda.get_device_name(dev),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -44,9 +44,25 @@ def _stale(src: str, obj: str) -> bool:
     return any(os.path.getmtime(p) > t for p in deps)
 
 
+def _flags_digest(cc: str, flags) -> str:
+    """The compiler and flags the objects were built with: a change of either
+    rebuilds every object (objects built with other flags are never reused)."""
+    import hashlib
+    return hashlib.sha256(("\0".join([cc, *flags])).encode()).hexdigest()
+
+
+STAMP = os.path.join(BUILD, "flags.sha256")
+
+
 def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
+    digest = _flags_digest(cc, _flags(extra_flags))
+    try:
+        with open(STAMP) as f:
+            force = force or f.read().strip() != digest
+    except OSError:
+        force = True
     jobs = []
     for s in SOURCES:
         src = os.path.join(CSRC, s)
@@ -68,6 +84,8 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
     if force or jobs or not os.path.exists(LIB):
         run([cc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
              "-o", LIB, *objs])
+    with open(STAMP, "w") as f:
+        f.write(digest + "\n")
     return LIB
 
 

@@ -73,6 +73,17 @@ struct PadJob {
   int C;
 };
 
+// The backward's data part leaves [dG | dU] and the padded straddling steps in
+// the workspace for the weight part. It records what they were computed for in
+// the workspace header (words kTagFirst.. after the status word); the weight
+// part's kernels compare that record with their own arguments and, on a
+// mismatch (no data part on this workspace, other sizes or other offsets),
+// report MOE_ERR_DEVICE_CHECK and compute nothing.
+constexpr int kTagNone = 0, kTagWrite = 1, kTagCheck = 2;
+constexpr int kTagWords = 6;
+constexpr int kTagFirst = 4;                  // int32 index in the workspace header
+constexpr uint32_t kTagMagic = 0x4D6F4542u;
+
 struct Params {
   const int32_t* offsets;  // [E+1] expert row offsets (device)
   int E;
@@ -90,6 +101,8 @@ struct Params {
   int ld_out;              // row length of `out` in elements
   int* status;             // workspace status word
   PadJob pad[2];           // BWD_DH: the weight gradients' pads of X and H (a == null: none)
+  int tag_mode;            // kTagNone, kTagWrite (data part's dH) or kTagCheck (weight part)
+  uint32_t tag[kTagWords]; // the backward's scratch tag: magic, M, E, d, I, offsets (low 32 bits)
 };
 
 // ----------------------------------------------------------------- PTX helpers
@@ -523,6 +536,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   }
   pdl_wait();   // offsets and operands come from earlier launches
   pdl_launch_dependents();
+  if (p.tag_mode == kTagWrite && blockIdx.x == 0 && threadIdx.x < kTagWords)
+    reinterpret_cast<uint32_t*>(p.status)[kTagFirst + threadIdx.x] = p.tag[threadIdx.x];
   for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
   __syncthreads();
   if (warp == 0) {   // exclusive prefix of per-expert m-tile pairs
@@ -995,7 +1010,15 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
                : "memory");
   const bool tmem_ok = (peer_base == tmem_base);
   if (!tmem_ok && threadIdx.x == 0) report_status(p.status, MOE_ERR_DEVICE_CHECK);
-  const int total = tmem_ok ? p.E * p.m_tiles * p.n_tiles : 0;
+  // the data part's record of the scratch this launch reads (every CTA reads it)
+  bool tag_ok = true;
+  if (p.tag_mode == kTagCheck) {
+    const volatile uint32_t* rec = reinterpret_cast<const volatile uint32_t*>(p.status) + kTagFirst;
+#pragma unroll
+    for (int i = 0; i < kTagWords; ++i) tag_ok = tag_ok && rec[i] == p.tag[i];
+    if (!tag_ok && blockIdx.x == 0 && threadIdx.x == 0) report_status(p.status, MOE_ERR_DEVICE_CHECK);
+  }
+  const int total = (tmem_ok && tag_ok) ? p.E * p.m_tiles * p.n_tiles : 0;
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(n_clusters_x());
 
@@ -1421,6 +1444,12 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
   p.d = d;
   p.I = I;
   p.status = static_cast<int*>(ws);
+  p.tag[0] = kTagMagic;
+  p.tag[1] = static_cast<uint32_t>(M);
+  p.tag[2] = static_cast<uint32_t>(E);
+  p.tag[3] = static_cast<uint32_t>(d);
+  p.tag[4] = static_cast<uint32_t>(I);
+  p.tag[5] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(offsets));
   const long long mt_upper = (M + BM - 1) / BM + E;
   CUtensorMap ta, tb0, tb1, tc0, tc1;
   // gate/up projection with the SwiGLU epilogue (H and [G|U] leave through bulk stores)
@@ -1505,6 +1534,12 @@ int ffn_backward_parts(int parts, const moe_bf16* dy, const moe_bf16* xp, const 
   p.d = d;
   p.I = I;
   p.status = static_cast<int*>(ws);
+  p.tag[0] = kTagMagic;
+  p.tag[1] = static_cast<uint32_t>(M);
+  p.tag[2] = static_cast<uint32_t>(E);
+  p.tag[3] = static_cast<uint32_t>(d);
+  p.tag[4] = static_cast<uint32_t>(I);
+  p.tag[5] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(offsets));
   const long long mt_upper = (M + BM - 1) / BM + E;
   CUtensorMap ta, tb0, tb1, tc0, tc1;
   int rc = MOE_OK;
@@ -1524,7 +1559,9 @@ int ffn_backward_parts(int parts, const moe_bf16* dy, const moe_bf16* xp, const 
     // the dH launch also fills the weight gradients' padded straddling steps
     p.pad[0] = PadJob{reinterpret_cast<const __nv_bfloat16*>(xp), pad_x, d};
     p.pad[1] = PadJob{reinterpret_cast<const __nv_bfloat16*>(h), pad_h, I};
+    p.tag_mode = kTagWrite;
     rc = launch_pair_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc1, p, mt_upper * p.n_tiles, st);
+    p.tag_mode = kTagNone;
     if (rc) return rc;
     // dX = dG Wg^T + dU Wu^T
     const int bn_x = pair_bn(d);
@@ -1556,6 +1593,7 @@ int ffn_backward_parts(int parts, const moe_bf16* dy, const moe_bf16* xp, const 
   p.outf0 = dw_gate;
   p.outf1 = dw_up;
   p.out = nullptr;
+  p.tag_mode = kTagCheck;
   rc = launch_pair_wgrad<WGRAD_GU>(ta, tb0, tc0, tc1, ta16, tpad, p,
                                    static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
   if (rc) return rc;

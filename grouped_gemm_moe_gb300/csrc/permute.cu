@@ -23,6 +23,8 @@
 //              its assignments again so each one gets
 //              rank = earlier chunks + earlier warps + earlier steps + earlier
 //              lanes with the same expert. Positions follow in closed form.
+#include <atomic>
+#include <mutex>
 #include "common.cuh"
 
 namespace moe {
@@ -430,23 +432,44 @@ static __device__ __align__(256) int32_t g_static_hist[MOE_STATIC_HIST_INTS];
 namespace {
 
 constexpr int kMaxStaticDevices = 64;
-int32_t* g_static_hist_dev[kMaxStaticDevices] = {nullptr};
-bool g_static_smem_set[kMaxStaticDevices] = {false};
 
-// Device address of g_static_hist on the current device (looked up once per device).
-int static_hist_on_current_device(int32_t** out, int* dev_out) {
+// Per-device set-up of the static entry point, done once per device under a
+// lock (host threads may make their first call on a device concurrently):
+// the device address of g_static_hist and the kernels' shared-memory limits.
+// A failed set-up is not recorded, so the next call retries it.
+struct StaticDeviceState {
+  std::atomic<int32_t*> hist{nullptr};
+};
+StaticDeviceState g_static_state[kMaxStaticDevices];
+std::mutex g_static_mutex;
+
+int static_setup_current_device(int32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
   if (dev < 0 || dev >= kMaxStaticDevices) return MOE_ERR_UNSUPPORTED;
-  if (!g_static_hist_dev[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_static_hist);
-    if (e != cudaSuccess || !ptr) { set_last_cuda_error(e); return MOE_ERR_CUDA; }
-    g_static_hist_dev[dev] = static_cast<int32_t*>(ptr);
+  StaticDeviceState& s = g_static_state[dev];
+  int32_t* p = s.hist.load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    p = s.hist.load(std::memory_order_relaxed);
+    if (!p) {
+      e = cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               160 * 1024);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(scatter_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+      void* ptr = nullptr;
+      if (e == cudaSuccess) e = cudaGetSymbolAddress(&ptr, g_static_hist);
+      if (e != cudaSuccess || !ptr) {
+        set_last_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+        return MOE_ERR_CUDA;
+      }
+      p = static_cast<int32_t*>(ptr);
+      s.hist.store(p, std::memory_order_release);
+    }
   }
-  *out = g_static_hist_dev[dev];
-  *dev_out = dev;
+  *out = p;
   return MOE_OK;
 }
 
@@ -477,15 +500,8 @@ extern "C" int moe_build_permutation_static(const int32_t* topk_idx, int T, int 
   const int NC = g.cps;
   if (static_cast<long long>(NC) * E > MOE_STATIC_HIST_INTS) return MOE_ERR_WORKSPACE;
   int32_t* hist = nullptr;
-  int dev = 0;
-  int rc = static_hist_on_current_device(&hist, &dev);
+  int rc = static_setup_current_device(&hist);
   if (rc) return rc;
-  if (!g_static_smem_set[dev]) {
-    cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    cudaFuncSetAttribute(scatter_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         160 * 1024);
-    g_static_smem_set[dev] = true;
-  }
   const size_t sh_hist = static_cast<size_t>(kWarps) * E * sizeof(int);
   const size_t sh_scatter = scatter_smem_bytes(E);
   PermOut po{counts, offsets, perm, inv_perm};

@@ -64,8 +64,11 @@ CONFIGS: Dict[str, MoEConfig] = {
     "drafter": MoEConfig("drafter", T=32768, d=4096, E=64, K=8, I=2048, R=4),
 }
 
-# The configuration the throughput metric is quoted on (one GPU, fwd+bwd).
-BENCH_CONFIG = "qwen3"
+# The configuration the throughput metric is quoted on: the largest workload
+# that runs forward and backward on one GPU.
+BENCH_CONFIG = "drafter"
+# The other forward + backward workloads, reported beside it.
+SIDE_CONFIGS = ("qwen3", "dsv2lite", "skew")
 
 
 def zipf_bias(E: int) -> torch.Tensor:
@@ -138,5 +141,5 @@ def describe(cfg: MoEConfig) -> str:
     return s
 
 
-__all__ = ["MoEConfig", "CONFIGS", "BENCH_CONFIG", "make_inputs", "small_config",
+__all__ = ["MoEConfig", "CONFIGS", "BENCH_CONFIG", "SIDE_CONFIGS", "make_inputs", "small_config",
            "zipf_bias", "to_f64", "describe", "flops_per_assignment_fwd"]

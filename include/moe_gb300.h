@@ -161,9 +161,15 @@ int moe_build_permutation(const int32_t* topk_idx, int T, int E, int K,
  *   Limit: ceil(T*K / 1024) * E <= MOE_STATIC_HIST_INTS (for example E = 128
  *   up to T*K = 2,097,152); larger problems return MOE_ERR_WORKSPACE before
  *   anything is enqueued. Other limits as moe_build_permutation.
- *   The first call on a device looks up that device's address of the array
- *   (cudaGetSymbolAddress, with the device current) and caches it; make that
- *   first call before any stream capture on that device.
+ *   The first call on a device sets that device up once: it raises the two
+ *   kernels' shared-memory limits and looks up that device's address of the
+ *   array (cudaGetSymbolAddress, with the device current), and caches the
+ *   address. The set-up runs under a lock, so host threads may make their
+ *   first calls concurrently; a failed set-up returns MOE_ERR_CUDA and is
+ *   retried by the next call. Make that first call before any stream capture
+ *   on that device. The cached address belongs to the device's primary
+ *   context: after cudaDeviceReset on that device this entry point must not
+ *   be called again in the same process.
  *   All calls share the array and it keeps the last call's contents; every
  *   entry a call reads is written earlier in the same call, so nothing needs
  *   clearing. Calls that overlap on the GPU (other streams, other host
@@ -278,7 +284,14 @@ int moe_grouped_ffn_backward(const moe_bf16* dy, const moe_bf16* xp, const moe_b
  * with the same ws, dy, xp, h, offsets and sizes; work may run in between
  * (a caller can consume dxp while its rows are still in L2). Arguments,
  * layouts, limits and errors as moe_grouped_ffn_backward, for the arguments
- * each part takes. */
+ * each part takes.
+ *   The data part records M, E, d, I and the offsets pointer in the
+ *   workspace header (after the status word); the weight part's kernels
+ *   compare that record with their own arguments and, if it differs (no data
+ *   part ran on this workspace, or it ran for other sizes or offsets), write
+ *   nothing and set the status word to MOE_ERR_DEVICE_CHECK (read it with
+ *   moe_read_device_status). The record does not see a change of the
+ *   contents of offsets, dy, xp or h between the parts. */
 int moe_grouped_ffn_backward_data(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* gu,
                                   const moe_bf16* h, const int32_t* offsets, int E, int M, int d,
                                   int I, const moe_bf16* w_gate, const moe_bf16* w_up,

@@ -295,3 +295,41 @@ def test_grouped_ffn_backward_split_matches_whole(counts, d, I):
     assert torch.equal(dxp, whole[0])
     for got, want in zip(dws, whole[1:]):
         assert torch.equal(got, want)
+
+
+def test_grouped_ffn_backward_weights_without_data_part_reports_check():
+    """The weight part on a workspace no data part has filled (or filled for
+    other offsets) writes nothing and reports MOE_ERR_DEVICE_CHECK; after a
+    matching data part it runs normally."""
+    counts, d, I = SMALL[0]
+    off, xp, wg, wu, wd = _problem(counts, d, I, 7 * sum(counts) + I)
+    g = torch.Generator().manual_seed(17)
+    M = int(off[-1])
+    dy, gu, h = _bf16((M, d), g, 0.1), _bf16((M, 2 * I), g, 1.0), _bf16((M, I), g, 0.5)
+    dv = {k: to_dev(t, torch.bfloat16) for k, t in
+          (("dy", dy), ("xp", xp), ("gu", gu), ("h", h), ("wg", wg), ("wu", wu), ("wd", wd))}
+    offd = to_dev(off, torch.int32)
+    E = len(counts)
+    dev_ = dv["xp"].device
+    ws = B.new_workspace(B.workspace_size(B.MOE_OP_GROUPED_FFN_BACKWARD, M, E, 1, 1, d, I), dev_)
+    sentinel = lambda *s: torch.full(s, 7.0, device=dev_)  # noqa: E731
+    out = (sentinel(E, d, I), sentinel(E, d, I), sentinel(E, I, d))
+    B.moe_grouped_ffn_backward_weights(dv["dy"], dv["xp"], dv["h"], offd, E, I, ws=ws, out=out)
+    assert B.moe_read_device_status(ws) == B.MOE_ERR_DEVICE_CHECK
+    assert all((t == 7.0).all() for t in out)
+    # a data part for another offsets tensor (same values) does not vouch for this one
+    off_other = offd.clone()
+    B.moe_grouped_ffn_backward_data(dv["dy"], dv["xp"], dv["gu"], dv["h"], off_other, dv["wg"],
+                                    dv["wu"], dv["wd"], ws=ws)
+    B.moe_grouped_ffn_backward_weights(dv["dy"], dv["xp"], dv["h"], offd, E, I, ws=ws, out=out)
+    assert B.moe_read_device_status(ws) == B.MOE_ERR_DEVICE_CHECK
+    assert all((t == 7.0).all() for t in out)
+    # the matching pair runs and agrees with the single call
+    whole = B.moe_grouped_ffn_backward(dv["dy"], dv["xp"], dv["gu"], dv["h"], offd, dv["wg"],
+                                       dv["wu"], dv["wd"])
+    B.moe_grouped_ffn_backward_data(dv["dy"], dv["xp"], dv["gu"], dv["h"], offd, dv["wg"],
+                                    dv["wu"], dv["wd"], ws=ws)
+    B.moe_grouped_ffn_backward_weights(dv["dy"], dv["xp"], dv["h"], offd, E, I, ws=ws, out=out)
+    assert B.moe_read_device_status(ws) == B.MOE_OK
+    for got, want in zip(out, whole[1:]):
+        assert torch.equal(got, want)

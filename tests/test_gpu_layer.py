@@ -256,3 +256,51 @@ def test_layer_full_size_sampled_tokens(name, n_tok):
     rest = np.ones(cfg.E, bool)
     rest[used] = False
     assert (dl[:, rest] == 0).all()
+
+
+def test_layer_full_size_every_element_qwen3():
+    """The benchmarked launch sequence on the whole Qwen3-shaped workload
+    (T=8192, d=2048, E=128, K=8, I=768, R=8), forward and backward, against the
+    oracle's layer on the same inputs, compared element by element on every
+    output: the routing, permutation and expert-parallel indices bit-exact; the
+    fp32 router weights within 1e-5 relative; every bf16 activation and gradient
+    (xp exact; h, gu, dy element-wise within half an ulp of the stored value
+    plus 1e-3 RMS; y, out, dxp, dx with the error beyond half an ulp within
+    2e-2 RMS); the fp32 weight gradients, dtopk_w and dlogits within 2e-2 RMS
+    (the end-to-end layer bound)."""
+    cfg = W.CONFIGS["qwen3"]
+    inp = W.make_inputs(cfg, with_backward=True)
+    layer = L.layer_from_config(cfg, inp, dev())
+    out = layer.forward(inp["logits"].to(dev()), inp["x"].to(dev())).clone()
+    dx = layer.backward(inp["dout"].to(dev())).clone()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    np_inp = {k: W.to_f64(v) for k, v in inp.items()}
+    ref = O.layer_forward(np_inp, cfg.K, cfg.R, cfg.renorm, pre=True)
+    assert np.array_equal(i64(layer.topk_idx), ref["topk_idx"])
+    assert_rel_close(f64(layer.topk_w), ref["topk_w"], name="topk_w")
+    for k in ("counts", "offsets", "perm", "inv_perm", "send_index", "a2a_index",
+              "regroup_index"):
+        assert np.array_equal(i64(getattr(layer, k)), ref[k]), k
+    R, E = cfg.R, cfg.E
+    s = i64(layer.ep_splits)
+    assert np.array_equal(s[:R * E].reshape(R, E), ref["ep_counts"])
+    assert np.array_equal(s[R * E:].reshape(R, R), ref["send_splits"])
+    assert np.array_equal(f64(layer.xp), ref["xp"])
+    assert_bf16_close(f64(layer.h), ref["h_pre"], name="h")
+    assert_bf16_close(f64(layer.gu), ref["gu_pre"], name="gu")
+    assert_out_close(f64(layer.y), ref["y_pre"], name="y")
+    assert_out_close(f64(out), ref["out_pre"], name="out")
+    rb = O.layer_backward(np_inp, ref, np_inp["dout"], cfg.K, cfg.renorm, pre=True)
+    # dy = bf16(w * dout) against the exact product with the oracle's weights
+    T, K = cfg.T, cfg.K
+    dy_pre = np.empty((T * K, cfg.d))
+    dy_pre[ref["inv_perm"]] = (ref["topk_w"][:, :, None] * np_inp["dout"][:, None, :]).reshape(T * K, -1)
+    assert_bf16_close(f64(layer.dy), dy_pre, name="dy")
+    del dy_pre
+    assert_rms_close(f64(layer.dtopk_w), rb["dtopk_w"], name="dtopk_w")
+    assert_out_close(f64(layer.dxp), rb["dxp_pre"], name="dxp")
+    assert_out_close(f64(dx), rb["dx_pre"], name="dx")
+    assert_rms_close(f64(layer.dlogits), rb["dlogits"], name="dlogits")
+    for k in ("dw_gate", "dw_up", "dw_down"):
+        assert_rms_close(f64(getattr(layer, k)), rb[k], name=k)

@@ -63,7 +63,7 @@ def parse():
                     help="report only the headline workload (no configs sub-object)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--profile-case", choices=["gemm", "gemm_ragged", "gemm_l2", "layer", "hbm",
-                                               "routing"],
+                                               "routing", "combine_side"],
                     default=None,
                     help="run a small fixed case twice for an ncu capture and exit")
     return ap.parse_args()
@@ -83,6 +83,10 @@ def profile_case(which: str):
     routing: the forward's front on the qwen3 workload at full size (route top-k, the fused
              permutation + EP layout with its host copy, token-major dispatch), run twice;
              ~0.4 GB on the device.
+    combine_side: the combine, its backward and the dispatch backward at the qwen3 workload's
+             full size (T=8192, d=2048, K=8; the routing of the qwen3 inputs), on synthetic
+             expert outputs and gradients (~1.1 GB on the device), run twice, with 256 MiB
+             of L2-flushing writes before each kernel.
     hbm:     HBM bandwidth by access pattern on 2 GiB fp32 buffers (torch's fill, sum and
              copy; CUDA events, 20 launches after 3 warm-ups): the ceilings that write-only,
              read-only and copy-like kernels are compared with.
@@ -143,6 +147,29 @@ def profile_case(which: str):
                 B.moe_profile_start(64)
             B.moe_grouped_ffn_backward(dy, xp, gu, h, off, wg, wu, wd)
             B.moe_grouped_ffn(xp, off, wg, wu, wd)
+    elif which == "combine_side":
+        cfg = W.CONFIGS["qwen3"]
+        inp = W.make_inputs(cfg, with_backward=False)
+        idx, w = B.moe_route_topk(inp["logits"].to(dev), cfg.K, cfg.renorm)
+        _, _, _, inv = B.moe_build_permutation(idx, cfg.E)
+        TK, d = cfg.T * cfg.K, cfg.d
+        y = (torch.randn(TK, d, device=dev, generator=g) * 0.1).to(torch.bfloat16)
+        dxp = (torch.randn(TK, d, device=dev, generator=g) * 0.1).to(torch.bfloat16)
+        dout = torch.randn(cfg.T, d, device=dev, generator=g).to(torch.bfloat16)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for it in range(2):
+            if it == 1:
+                torch.cuda.synchronize()
+                B.moe_profile_start(64)
+            flush.zero_()
+            B.moe_combine(y, w, inv)
+            flush.zero_()
+            B.moe_combine_backward(dout, y, w, inv)
+            flush.zero_()
+            B.moe_dispatch_backward(dxp, inv, cfg.T, cfg.K)
+        torch.cuda.synchronize()
+        for name, ms in B.moe_profile_stop():
+            print(f"  {name:22s} {ms * 1e3:9.1f} us")
     elif which == "routing":
         cfg = W.CONFIGS["qwen3"]
         inp = W.make_inputs(cfg, with_backward=False)

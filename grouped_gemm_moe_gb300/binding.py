@@ -33,6 +33,7 @@ MOE_OP_EP_LAYOUT = 2
 MOE_OP_GROUPED_FFN = 3
 MOE_OP_GROUPED_FFN_BACKWARD = 4
 MOE_OP_LOAD_BALANCE = 5
+MOE_OP_EP_RECV_LAYOUT = 6
 
 WORKSPACE_HEADER = 256
 
@@ -64,6 +65,12 @@ SIGNATURES = {
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_combine_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_dispatch_backward": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "moe_ep_recv_layout": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_dispatch_slice": (_I, [_P, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "moe_combine_slice": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_combine_backward_slice": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_dispatch_backward_slice": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_reduce_finish": (_I, [_P, _P, _I, _I, _P, _P]),
     "moe_read_device_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
     "moe_debug_wait_timeout": (_I, [_P, _I, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -465,6 +472,120 @@ def moe_dispatch_backward(dxp: torch.Tensor, inv_perm: torch.Tensor, T: int, K: 
     _check("moe_dispatch_backward", load().moe_dispatch_backward(
         _ptr(dxp), _ptr(inv_perm), T, K, d, _ptr(dx_shared), _ptr(dx), _stream(dxp.device)))
     return dx
+
+
+# ---------------------------------------------------------------- expert parallelism over ranks
+def moe_ep_recv_layout(counts_local: torch.Tensor, recv_counts: torch.Tensor, R: int,
+                       capacity: int, host_splits: Optional[torch.Tensor] = None,
+                       ws: Optional[torch.Tensor] = None, out=None):
+    """Receive-side layout of the all-to-all dispatch from this rank's counts
+    [E] and the exchanged counts [R*El]. Returns (splits [2R] = send then
+    receive rows per peer, local_offsets [El+1], regroup_index [capacity],
+    host_splits); ``host_splits`` (pinned CPU int32 [2R]) receives the one
+    device-to-host copy (``False`` skips it)."""
+    _need(counts_local, torch.int32, 1, "counts_local")
+    _need(recv_counts, torch.int32, 1, "recv_counts")
+    E = counts_local.numel()
+    dev = counts_local.device
+    if E % R or recv_counts.numel() != E:
+        raise ValueError("R must divide E and recv_counts must hold R * (E / R) counts")
+    El = E // R
+    if host_splits is None:
+        host_splits = torch.empty(2 * R, dtype=torch.int32, pin_memory=True)
+    elif host_splits is False:
+        host_splits = None
+    if ws is None:
+        ws = new_workspace(workspace_size(MOE_OP_EP_RECV_LAYOUT, 1, E, 1, R), dev)
+    if out is None:
+        out = (torch.empty(2 * R, dtype=torch.int32, device=dev),
+               torch.empty(El + 1, dtype=torch.int32, device=dev),
+               torch.empty(max(int(capacity), 1), dtype=torch.int32, device=dev))
+    splits, loff, reg = out
+    _check("moe_ep_recv_layout", load().moe_ep_recv_layout(
+        _ptr(counts_local), _ptr(recv_counts), E, R, int(capacity), _ptr(splits), _ptr(loff),
+        _ptr(reg), _ptr(host_splits), _ptr(ws), ws.numel(), _stream(dev)))
+    return splits, loff, reg, host_splits
+
+
+def moe_dispatch_slice(x: torch.Tensor, inv_perm: torch.Tensor, offsets: torch.Tensor, K: int,
+                       e_lo: int, e_hi: int, out: Tuple[torch.Tensor, torch.Tensor]):
+    """Local rows of the dispatch for experts [e_lo, e_hi): out = (xs [rows, d] bf16,
+    local_offsets [e_hi - e_lo + 1] int32); returns out."""
+    _need(x, torch.bfloat16, 2, "x")
+    _need(inv_perm, torch.int32, 1, "inv_perm")
+    _need(offsets, torch.int32, 1, "offsets")
+    T, d = x.shape
+    xs, loff = out
+    _need(xs, torch.bfloat16, 2, "xs")
+    _need(loff, torch.int32, 1, "local_offsets")
+    _check("moe_dispatch_slice", load().moe_dispatch_slice(
+        _ptr(x), T, d, K, _ptr(inv_perm), _ptr(offsets), offsets.numel() - 1, int(e_lo), int(e_hi),
+        _ptr(xs), _ptr(loff), _stream(x.device)))
+    return xs, loff
+
+
+def moe_combine_slice(y_local: torch.Tensor, topk_w: torch.Tensor, inv_perm: torch.Tensor,
+                      offsets: torch.Tensor, e_lo: int, e_hi: int,
+                      out: Optional[torch.Tensor] = None):
+    """fp32 partial combine [T, d] of the local experts' rows."""
+    _need(y_local, torch.bfloat16, 2, "y_local")
+    _need(topk_w, torch.float32, 2, "topk_w")
+    _need(inv_perm, torch.int32, 1, "inv_perm")
+    _need(offsets, torch.int32, 1, "offsets")
+    T, K = topk_w.shape
+    d = y_local.shape[1]
+    o = out if out is not None else torch.empty(T, d, dtype=torch.float32, device=y_local.device)
+    _check("moe_combine_slice", load().moe_combine_slice(
+        _ptr(y_local), _ptr(topk_w), _ptr(inv_perm), _ptr(offsets), offsets.numel() - 1,
+        int(e_lo), int(e_hi), T, K, d, _ptr(o), _stream(y_local.device)))
+    return o
+
+
+def moe_combine_backward_slice(dout: torch.Tensor, y_local: torch.Tensor, topk_w: torch.Tensor,
+                               inv_perm: torch.Tensor, offsets: torch.Tensor, e_lo: int,
+                               e_hi: int, out: Tuple[torch.Tensor, torch.Tensor]):
+    """(dy_local [rows, d] bf16, dtopk_w [T, K] fp32, zero on other ranks' slots)."""
+    _need(dout, torch.bfloat16, 2, "dout")
+    _need(y_local, torch.bfloat16, 2, "y_local")
+    _need(topk_w, torch.float32, 2, "topk_w")
+    _need(inv_perm, torch.int32, 1, "inv_perm")
+    _need(offsets, torch.int32, 1, "offsets")
+    T, K = topk_w.shape
+    d = dout.shape[1]
+    dy, dw = out
+    _check("moe_combine_backward_slice", load().moe_combine_backward_slice(
+        _ptr(dout), _ptr(y_local), _ptr(topk_w), _ptr(inv_perm), _ptr(offsets),
+        offsets.numel() - 1, int(e_lo), int(e_hi), T, K, d, _ptr(dy), _ptr(dw),
+        _stream(dout.device)))
+    return dy, dw
+
+
+def moe_dispatch_backward_slice(dxs: torch.Tensor, inv_perm: torch.Tensor, offsets: torch.Tensor,
+                                T: int, K: int, e_lo: int, e_hi: int,
+                                out: Optional[torch.Tensor] = None):
+    """fp32 partial input gradient [T, d] from the local experts' rows."""
+    _need(dxs, torch.bfloat16, 2, "dxs")
+    _need(inv_perm, torch.int32, 1, "inv_perm")
+    _need(offsets, torch.int32, 1, "offsets")
+    d = dxs.shape[1]
+    o = out if out is not None else torch.empty(T, d, dtype=torch.float32, device=dxs.device)
+    _check("moe_dispatch_backward_slice", load().moe_dispatch_backward_slice(
+        _ptr(dxs), _ptr(inv_perm), _ptr(offsets), offsets.numel() - 1, int(e_lo), int(e_hi), T, K,
+        d, _ptr(o), _stream(dxs.device)))
+    return o
+
+
+def moe_reduce_finish(partial: torch.Tensor, extra: Optional[torch.Tensor] = None,
+                      out: Optional[torch.Tensor] = None):
+    """bf16(partial + extra) for fp32 partial [T, d] and bf16 extra [T, d] (or None)."""
+    _need(partial, torch.float32, 2, "partial")
+    if extra is not None:
+        _need(extra, torch.bfloat16, 2, "extra")
+    T, d = partial.shape
+    o = out if out is not None else torch.empty(T, d, dtype=torch.bfloat16, device=partial.device)
+    _check("moe_reduce_finish", load().moe_reduce_finish(_ptr(partial), _ptr(extra), T, d, _ptr(o),
+                                                         _stream(partial.device)))
+    return o
 
 
 def moe_profile_start(capacity: int = 4096):

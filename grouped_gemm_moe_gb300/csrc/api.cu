@@ -93,6 +93,8 @@ extern "C" size_t moe_workspace_size(int op, int T, int E, int K, int R, int d, 
       return kWorkspaceHeader + ffn_backward_scratch(TK, E, d, I);
     case MOE_OP_LOAD_BALANCE:
       return load_balance_workspace(E);
+    case MOE_OP_EP_RECV_LAYOUT:
+      return kWorkspaceHeader;
     default:
       return 0;
   }

@@ -69,7 +69,8 @@ enum moe_op {
   MOE_OP_EP_LAYOUT = 2,
   MOE_OP_GROUPED_FFN = 3,
   MOE_OP_GROUPED_FFN_BACKWARD = 4,
-  MOE_OP_LOAD_BALANCE = 5
+  MOE_OP_LOAD_BALANCE = 5,
+  MOE_OP_EP_RECV_LAYOUT = 6
 };
 
 /* Bytes of device workspace the operation needs for these sizes (0 on bad
@@ -341,6 +342,98 @@ int moe_dispatch_backward(const moe_bf16* dxp, const int32_t* inv_perm, int T, i
 int moe_profile_start(int capacity);
 int moe_profile_stop(void);
 int moe_profile_record(int i, const char** name, float* ms);
+
+/* ------------------------------------------------------------------------
+ * Expert parallelism over real ranks. One process per GPU; the collectives
+ * (all-to-all, all-gather, reduce-scatter) are the caller's (for example
+ * torch.distributed over NCCL). These calls are the per-rank steps on either
+ * side of them; every other step reuses the entry points above.
+ * ------------------------------------------------------------------------ */
+
+/* All-to-all EP, receive side ([TAS] "Dispatch, expert computation and
+ * combine": counts are exchanged, each destination receives a source-major
+ * buffer and regroups it by local expert; [MOD] "Design" items 1-2: the
+ * regroup index is built on device and both split lists reach the host in one
+ * device-to-host copy).
+ *   R ranks, E experts, El = E / R; rank r owns experts [r*El, (r+1)*El).
+ *   A rank's send buffer is its own expert-major permutation of its
+ *   assignments (moe_build_permutation + moe_dispatch_scatter), so its rows
+ *   for destination q are contiguous and number
+ *   send[q] = sum_{e in q's experts} counts_local[e].
+ *   counts_local [E] int32: this rank's per-expert counts (from
+ *   moe_build_permutation). recv_counts [R*El] int32: row s holds source s's
+ *   counts for this rank's El experts (the count exchange: an all-to-all of
+ *   counts_local with El elements per peer).
+ *   Outputs: splits [2R] int32 = send splits then receive splits (rows per
+ *   peer); local_offsets [El+1] int32 = offsets of the regrouped rows, ordered
+ *   by (local expert, source, the source's order), so that they are the
+ *   offsets moe_grouped_ffn takes for this rank's experts; regroup_index
+ *   [capacity] int32: regroup_index[p] = the receive-buffer row of regrouped
+ *   row p for p < sum(receive splits) (entries past that are not written).
+ *   host_splits (pinned host int32 [2R] or NULL) receives the one
+ *   device-to-host copy of splits on `stream`; synchronise before reading it.
+ *   capacity >= sum of receive splits; at most R * (T/R) * min(K, El) rows
+ *   arrive when every rank has T/R tokens. If the counts need more rows than
+ *   capacity, nothing past capacity is written and the status word of ws
+ *   (moe_workspace_size(MOE_OP_EP_RECV_LAYOUT, ...) = header only) reads
+ *   MOE_ERR_DEVICE_CHECK. E <= 1024, R divides E. */
+int moe_ep_recv_layout(const int32_t* counts_local, const int32_t* recv_counts, int E, int R,
+                       int capacity, int32_t* splits, int32_t* local_offsets,
+                       int32_t* regroup_index, int32_t* host_splits, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/* All-gather / reduce-scatter EP ([SF] "What this adds", the MoELayer.forward
+ * under EP bullet: the group's tokens are all-gathered, the replicated router
+ * runs on them, each rank computes only its own experts for all tokens, the
+ * partial outputs are reduce-scattered and the shared expert is added on the
+ * local tokens). Every rank holds route / permutation results for all T
+ * gathered tokens (offsets [E+1], inv_perm [T*K]); its experts [e_lo, e_hi)
+ * own the packed rows [offsets[e_lo], offsets[e_hi)), which the kernels read
+ * on the device. The local rows are compact: local row i is packed row
+ * offsets[e_lo] + i. Arguments as the single-GPU calls otherwise; d % 8 == 0,
+ * 1 <= K <= 32, 0 <= e_lo < e_hi <= E.
+ *
+ * moe_dispatch_slice: xs[p - offsets[e_lo]] = x[t] for every assignment
+ *   a = t*K + j whose row p = inv_perm[a] is local; writes local_offsets
+ *   [e_hi - e_lo + 1] = offsets[e_lo + i] - offsets[e_lo] (the offsets
+ *   moe_grouped_ffn takes for the local rows). xs holds at least
+ *   offsets[e_hi] - offsets[e_lo] rows (T * min(K, e_hi - e_lo) always
+ *   suffices). */
+int moe_dispatch_slice(const moe_bf16* x, int T, int d, int K, const int32_t* inv_perm,
+                       const int32_t* offsets, int E, int e_lo, int e_hi, moe_bf16* xs,
+                       int32_t* local_offsets, void* stream);
+
+/* moe_combine_slice: out_partial[t] (fp32 [T,d]) = sum over the slots j of
+ *   token t whose row p = inv_perm[t*K+j] is local, in slot order, of
+ *   topk_w[t,j] * y_local[p - offsets[e_lo]]; zero rows for tokens with no
+ *   local slot. The reduce-scatter (sum) of these partials over the ranks is
+ *   the combine of every rank's tokens before the shared expert and the bf16
+ *   rounding (moe_reduce_finish). */
+int moe_combine_slice(const moe_bf16* y_local, const float* topk_w, const int32_t* inv_perm,
+                      const int32_t* offsets, int E, int e_lo, int e_hi, int T, int K, int d,
+                      float* out_partial, void* stream);
+
+/* moe_combine_backward_slice: moe_combine_backward on the local slots: for
+ *   a = t*K + j with local row p, dy_local[p - offsets[e_lo]] =
+ *   bf16(topk_w[a] * dout[t]) and dtopk_w[a] = <dout[t], y_local[p - lo]>;
+ *   dtopk_w[a] = 0 for the other slots (the sum over ranks is the full
+ *   dtopk_w). dout is the gathered [T,d] upstream gradient. */
+int moe_combine_backward_slice(const moe_bf16* dout, const moe_bf16* y_local,
+                               const float* topk_w, const int32_t* inv_perm,
+                               const int32_t* offsets, int E, int e_lo, int e_hi, int T, int K,
+                               int d, moe_bf16* dy_local, float* dtopk_w, void* stream);
+
+/* moe_dispatch_backward_slice: dx_partial[t] (fp32 [T,d]) = sum over the
+ *   local slots of token t, in slot order, of dxs[p - offsets[e_lo]]. */
+int moe_dispatch_backward_slice(const moe_bf16* dxs, const int32_t* inv_perm,
+                                const int32_t* offsets, int E, int e_lo, int e_hi, int T, int K,
+                                int d, float* dx_partial, void* stream);
+
+/* moe_reduce_finish: out = bf16(partial + extra) element-wise, partial fp32
+ *   [T,d] (the reduce-scattered sum), extra bf16 [T,d] or NULL (the shared
+ *   expert's output or input gradient on the local tokens). */
+int moe_reduce_finish(const float* partial, const moe_bf16* extra, int T, int d, moe_bf16* out,
+                      void* stream);
 
 /* Diagnostics: runs the bounded device-side wait that every mbarrier wait of
  * the GEMM kernels uses, on an mbarrier that nothing completes, with a limit of

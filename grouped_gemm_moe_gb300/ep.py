@@ -70,8 +70,11 @@ class CudaKernels:
     reduce_finish = staticmethod(B.moe_reduce_finish)
 
     @staticmethod
-    def workspace(op, T, E, K, R, d, I, device):
-        return B.new_workspace(B.workspace_size(op, T, E, K, R, d, I), device)
+    def workspace(op, T, E, K, R, d, I, device, zero: bool = False):
+        ws = B.new_workspace(B.workspace_size(op, T, E, K, R, d, I), device)
+        if zero:
+            ws.zero_()
+        return ws
 
 
 # --------------------------------------------------------------------- exchanges
@@ -387,20 +390,28 @@ class AGRSRank:
         cap = max(self.cap, 1)
         bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
         e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        # The local rows fill only the first offsets[e_hi] - offsets[e_lo] of the
+        # capacity-sized row buffers, and the GEMMs see the whole capacity (the
+        # count is known on the device only). The weight gradients multiply the
+        # rows past the last local expert by zero rows in their straddling step,
+        # so those rows must hold finite values: the row buffers and the backward
+        # workspace start zeroed, and later steps leave only finite results there.
+        z = lambda *s, dt: torch.zeros(*s, dtype=dt, device=dev)  # noqa: E731
         self.logits_all, self.x_all = e(Tg, E, dt=f32), e(Tg, d, dt=bf)
         self.topk_idx, self.topk_w = e(Tg, K, dt=i32), e(Tg, K, dt=f32)
         self.counts, self.offsets = e(E, dt=i32), e(E + 1, dt=i32)
         self.perm, self.inv_perm = e(TK, dt=i32), e(TK, dt=i32)
-        self.xs, self.local_offsets = e(cap, d, dt=bf), e(self.El + 1, dt=i32)
-        self.y, self.h, self.gu = e(cap, d, dt=bf), e(cap, I, dt=bf), e(cap, 2 * I, dt=bf)
+        self.xs, self.local_offsets = z(cap, d, dt=bf), e(self.El + 1, dt=i32)
+        self.y, self.h, self.gu = z(cap, d, dt=bf), z(cap, I, dt=bf), z(cap, 2 * I, dt=bf)
         self.partial = e(Tg, d, dt=f32)
         self.out_partial = e(T_local, d, dt=f32)
         self.out = e(T_local, d, dt=bf)
         self.ws_perm = self.k.workspace(B.MOE_OP_BUILD_PERMUTATION, Tg, E, K, 1, 0, 0, dev)
         self.ws_ffn = self.k.workspace(B.MOE_OP_GROUPED_FFN, cap, self.El, 1, 1, d, I, dev)
-        self.ws_bwd = self.k.workspace(B.MOE_OP_GROUPED_FFN_BACKWARD, cap, self.El, 1, 1, d, I, dev)
+        self.ws_bwd = self.k.workspace(B.MOE_OP_GROUPED_FFN_BACKWARD, cap, self.El, 1, 1, d, I, dev,
+                                       zero=True)
         self.dout_all = e(Tg, d, dt=bf)
-        self.dy, self.dxs = e(cap, d, dt=bf), e(cap, d, dt=bf)
+        self.dy, self.dxs = z(cap, d, dt=bf), z(cap, d, dt=bf)
         self.dtopk_w_partial, self.dtopk_w = e(Tg, K, dt=f32), e(T_local, K, dt=f32)
         self.dx_partial, self.dx_local_partial = e(Tg, d, dt=f32), e(T_local, d, dt=f32)
         self.dx, self.dlogits = e(T_local, d, dt=bf), e(T_local, E, dt=f32)

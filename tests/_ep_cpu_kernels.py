@@ -23,7 +23,7 @@ class CpuKernels:
     def __init__(self):
         self._stash = {}
 
-    def workspace(self, op, T, E, K, R, d, I, device):
+    def workspace(self, op, T, E, K, R, d, I, device, zero=False):
         return torch.zeros(1, dtype=torch.uint8)
 
     def route_topk(self, logits, K, renorm=1, out=None):

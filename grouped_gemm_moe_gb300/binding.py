@@ -34,6 +34,7 @@ MOE_OP_GROUPED_FFN = 3
 MOE_OP_GROUPED_FFN_BACKWARD = 4
 MOE_OP_LOAD_BALANCE = 5
 MOE_OP_EP_RECV_LAYOUT = 6
+MOE_OP_GROUPED_FFN_FP8 = 7
 
 WORKSPACE_HEADER = 256
 
@@ -71,6 +72,9 @@ SIGNATURES = {
     "moe_combine_backward_slice": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_dispatch_backward_slice": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moe_reduce_finish": (_I, [_P, _P, _I, _I, _P, _P]),
+    "moe_mxfp8_quantize_rows": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "moe_mxfp8_quantize_weights": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "moe_grouped_ffn_fp8": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_read_device_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
     "moe_debug_wait_timeout": (_I, [_P, _I, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -586,6 +590,72 @@ def moe_reduce_finish(partial: torch.Tensor, extra: Optional[torch.Tensor] = Non
     _check("moe_reduce_finish", load().moe_reduce_finish(_ptr(partial), _ptr(extra), T, d, _ptr(o),
                                                          _stream(partial.device)))
     return o
+
+
+# ---------------------------------------------------------------- MXFP8 grouped experts
+def mxfp8_row_sf_bytes(M: int, E: int, K: int) -> int:
+    """Bytes of the scale atoms of M expert-ordered rows of K elements."""
+    return ((M + 127) // 128 + 2 * E) * (K // 128) * 512
+
+
+def moe_mxfp8_quantize_rows(x: torch.Tensor, offsets: torch.Tensor, out=None):
+    """(q [M, K] uint8 E4M3, sf uint8 scale atoms) of the expert-ordered rows x."""
+    _need(x, torch.bfloat16, 2, "x")
+    _need(offsets, torch.int32, 1, "offsets")
+    M, K = x.shape
+    E = offsets.numel() - 1
+    if out is None:
+        out = (torch.empty(M, K, dtype=torch.uint8, device=x.device),
+               torch.empty(mxfp8_row_sf_bytes(M, E, K), dtype=torch.uint8, device=x.device))
+    q, sf = out
+    _check("moe_mxfp8_quantize_rows", load().moe_mxfp8_quantize_rows(
+        _ptr(x), _ptr(offsets), E, M, K, _ptr(q), _ptr(sf), _stream(x.device)))
+    return q, sf
+
+
+def moe_mxfp8_quantize_weights(w_a: torch.Tensor, w_b: Optional[torch.Tensor] = None, out=None):
+    """(q [E, Nq, K] uint8, sf) of weights [E, K, N] (gate/up interleaved when w_b is given)."""
+    _need(w_a, torch.bfloat16, 3, "w_a")
+    if w_b is not None:
+        _need(w_b, torch.bfloat16, 3, "w_b")
+        if w_b.shape != w_a.shape:
+            raise ValueError("w_a and w_b must have the same shape")
+    E, K, N = w_a.shape
+    Nq = 2 * N if w_b is not None else N
+    if out is None:
+        out = (torch.empty(E, Nq, K, dtype=torch.uint8, device=w_a.device),
+               torch.empty(E * (Nq // 128) * (K // 128) * 512, dtype=torch.uint8, device=w_a.device))
+    q, sf = out
+    _check("moe_mxfp8_quantize_weights", load().moe_mxfp8_quantize_weights(
+        _ptr(w_a), _ptr(w_b), E, K, N, _ptr(q), _ptr(sf), _stream(w_a.device)))
+    return q, sf
+
+
+def moe_grouped_ffn_fp8(xp: torch.Tensor, offsets: torch.Tensor, wgu, wd, save_gu: bool = True,
+                        ws: Optional[torch.Tensor] = None, out=None):
+    """MXFP8 forward of the grouped SwiGLU experts. ``wgu`` = (q, sf) of
+    moe_mxfp8_quantize_weights(w_gate, w_up), ``wd`` = (q, sf) of
+    moe_mxfp8_quantize_weights(w_down). Returns (y [M,d], h [M,I], gu [M,2I] or None)."""
+    _need(xp, torch.bfloat16, 2, "xp")
+    _need(offsets, torch.int32, 1, "offsets")
+    (gq, gsf), (dq, dsf) = wgu, wd
+    for n, t in (("wgu_q", gq), ("wd_q", dq)):
+        _need(t, torch.uint8, 3, n)
+    M, d = xp.shape
+    E, two_i, _ = gq.shape
+    I = two_i // 2
+    dev = xp.device
+    if ws is None:
+        ws = new_workspace(workspace_size(MOE_OP_GROUPED_FFN_FP8, M, E, 1, 1, d, I), dev)
+    if out is None:
+        out = (torch.empty(M, d, dtype=torch.bfloat16, device=dev),
+               torch.empty(M, I, dtype=torch.bfloat16, device=dev),
+               torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dev) if save_gu else None)
+    y, h, gu = out
+    _check("moe_grouped_ffn_fp8", load().moe_grouped_ffn_fp8(
+        _ptr(xp), _ptr(offsets), E, M, d, I, _ptr(gq), _ptr(gsf), _ptr(dq), _ptr(dsf), _ptr(y),
+        _ptr(h), _ptr(gu), _ptr(ws), ws.numel(), _stream(dev)))
+    return y, h, gu
 
 
 def moe_profile_start(capacity: int = 4096):

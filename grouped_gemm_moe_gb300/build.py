@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["api.cu", "route.cu", "permute.cu", "gather.cu", "ep.cu", "grouped_gemm.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "gather.cu", "ep.cu", "fp8.cu", "grouped_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

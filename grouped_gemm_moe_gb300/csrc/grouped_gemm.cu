@@ -328,6 +328,51 @@ __host__ __device__ constexpr uint32_t make_idesc() {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: fp32 D, E4M3 A and
+// B (both K-major), UE8M0 scale factors, M rows (256 for a pair). The scale
+// factor ids (which byte of each 32-bit scale column a K32 step uses) are
+// or-ed in per step: bits 4-5 for B, 29-30 for A.
+template <int N, int M>
+__host__ __device__ constexpr uint32_t make_idesc_mxf8() {
+  return (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t mx_sf_ids(uint32_t a_id, uint32_t b_id) {
+  return (b_id << 4) | (a_id << 29);
+}
+
+// D[tmem of both CTAs] (+)= (A * 2^SFA) (B * 2^SFB)^T with E4M3 operands and one
+// UE8M0 scale per 32 K for every row of A and of B, M = 256 over the pair.
+__device__ __forceinline__ void tc_mma_pair_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t sfa_tmem,
+                                               uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4],"
+      " [%5], p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared memory -> TMEM of both CTAs of the pair (each from its own shared
+// memory): a 32 x 128-bit block (512 B, rows 16 B apart) to lanes 0-31 of four
+// consecutive columns, repeated in the other three lane quarters.
+__device__ __forceinline__ void tc_cp_pair_32x128(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled block of 16-byte rows (8-row core
+// matrices 128 B apart), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
 // silu(g) = g * sigmoid(g) with the fast exponential and reciprocal: a few
 // ulp of fp32, far below the bf16 rounding of H. For g < -87 the denominator
 // overflows and the quotient is 0, the limit of silu.
@@ -360,6 +405,7 @@ struct PTile {
   int row0;   // this CTA's first packed row
   int rows;   // this CTA's valid rows (<= 0: none)
   int n0;
+  int mg;     // the tile's pair index in the expert-ordered list of m-tile pairs
 };
 
 template <int KIND, int BN>
@@ -374,6 +420,7 @@ __device__ __forceinline__ PTile decode_pair(int t, int rank, const Params& p, c
     if (s_mp[mid] <= mg) lo = mid; else hi = mid - 1;
   }
   tl.e = lo;
+  tl.mg = mg;
   tl.row0 = s_off[lo] + (2 * (mg - s_mp[lo]) + rank) * BM;
   tl.rows = min(BM, s_off[lo + 1] - tl.row0);
   tl.n0 = nt * (KIND == FWD_GATEUP ? BN / 2 : BN);
@@ -472,21 +519,39 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float (&v
   }
 }
 
-template <int KIND, int BN, int STAGES>
+// FP8 = true: the forward kinds on MXFP8 operands (E4M3 elements, one UE8M0
+// scale per 32 K; tcgen05.mma kind::mxf8f6f4 with block scaling). A k-block is
+// then 128 K (the same 128-byte rows), B is K-major (the weights are quantized
+// into a transposed layout, gate and up interleaved in 64-row blocks), and each
+// stage also carries one 512-byte scale atom for the CTA's 128 A rows (tmB1)
+// and one for the pair's 128 B columns (tmS): 128 rows x 4 K32 scales, row r
+// at byte (r % 32) * 16 + (r / 32) * 4 + k. The MMA thread copies both atoms
+// into TMEM (tcgen05.cp, 32 x 128 bit repeated over the four lane quarters,
+// four columns each, a column ring per stage beside the accumulators) before
+// the stage's four K32 MMAs, which pick the scale byte by the descriptor's
+// scale ids. The A atoms follow the m-tiles of the tile list (pair index mg:
+// m-tiles 2 mg and 2 mg + 1), so the quantizer lays them out per expert.
+template <int KIND, int BN, int STAGES, bool FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB0,
                          const __grid_constant__ CUtensorMap tmB1,
                          const __grid_constant__ CUtensorMap tmC0,
-                         const __grid_constant__ CUtensorMap tmC1, const Params p) {
+                         const __grid_constant__ CUtensorMap tmC1,
+                         const __grid_constant__ CUtensorMap tmS, const Params p) {
   static_assert(KIND == FWD_GATEUP || KIND == FWD_DOWN || KIND == BWD_DH || KIND == BWD_DX,
                 "pair kernel: forward and input-gradient kinds");
-  constexpr bool B_MN = (KIND == FWD_GATEUP || KIND == FWD_DOWN);
-  constexpr uint32_t A_BYTES = BM * BK * 2;
+  static_assert(!FP8 || ((KIND == FWD_GATEUP || KIND == FWD_DOWN) && BN == 128),
+                "MXFP8: forward kinds on 256 x 128 pair tiles");
+  constexpr bool B_MN = !FP8 && (KIND == FWD_GATEUP || KIND == FWD_DOWN);
+  constexpr uint32_t A_BYTES = BM * BK * 2;          // 128 rows x 128 bytes (bf16 or fp8)
   constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
-  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr uint32_t TMEM_COLS = 2 * BN;
-  constexpr uint32_t IDESC = make_idesc<BN, false, B_MN, 2 * BM>();
+  constexpr uint32_t SF_BYTES = FP8 ? 1024u : 0u;    // scale atoms: A rows, then B columns
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+  constexpr uint32_t TMEM_COLS = FP8 ? 512u : 2u * BN;
+  constexpr uint32_t SF_COL0 = 2u * BN;              // scale columns: 8 per stage
+  static_assert(!FP8 || SF_COL0 + 8u * STAGES <= TMEM_COLS, "MXFP8 scale ring in TMEM");
+  constexpr uint32_t IDESC = FP8 ? make_idesc_mxf8<BN, 2 * BM>() : make_idesc<BN, false, B_MN, 2 * BM>();
   constexpr uint32_t MN_ATOM = 64 * 128;
 
   extern __shared__ uint8_t smem_raw[];
@@ -526,6 +591,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB1)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC1)) : "memory");
+    if constexpr (FP8)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmS)) : "memory");
   }
   if (warp == 1) {   // one warp in each CTA of the pair allocates collectively
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -588,8 +655,23 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t fb_local = full_bar(stage);
           if (leader) mbar_expect_tx(fb_local, 2 * STAGE_BYTES);   // both CTAs' boxes
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          issue_pair<KIND, BN>(tl, kb, rank, p, &tmA, &tmB0, &tmB1, sa, sa + A_BYTES,
-                               map_to_rank(fb_local, 0));
+          if constexpr (FP8) {
+            // A rows, the CTA's 64 B rows (gate or up for gate/up: interleaved rows),
+            // then the A rows' scale atom and the pair's B scale atom
+            const uint32_t fb = map_to_rank(fb_local, 0);
+            const int nq = (KIND == FWD_GATEUP) ? 2 * p.I : p.d;    // B rows per expert
+            const int nrow = (KIND == FWD_GATEUP) ? 2 * tl.n0 : tl.n0;
+            tma_load_2d_pair(sa, &tmA, fb, kb * 128, tl.row0);
+            tma_load_2d_pair(sa + A_BYTES, &tmB0, fb, kb * 128,
+                             tl.e * nq + nrow + static_cast<int>(rank) * (BN / 2));
+            tma_load_2d_pair(sa + A_BYTES + B_BYTES, &tmB1, fb, 0,
+                             (2 * tl.mg + static_cast<int>(rank)) * p.k_blocks + kb);
+            tma_load_2d_pair(sa + A_BYTES + B_BYTES + 512, &tmS, fb, 0,
+                             (tl.e * (nq / 128) + nrow / 128) * p.k_blocks + kb);
+          } else {
+            issue_pair<KIND, BN>(tl, kb, rank, p, &tmA, &tmB0, &tmB1, sa, sa + A_BYTES,
+                                 map_to_rank(fb_local, 0));
+          }
           issued[stage] += 1;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -627,13 +709,28 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
           if (lane == 0) {
+            if constexpr (FP8) {
+              const uint32_t t_sfa = tmem_base + SF_COL0 + 8u * static_cast<uint32_t>(stage);
+              const uint32_t t_sfb = t_sfa + 4u;
+              const uint32_t sf = sb + B_BYTES;
+              tc_cp_pair_32x128(t_sfa, smem_desc_rows16(sf));
+              tc_cp_pair_32x128(t_sfb, smem_desc_rows16(sf + 512));
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
-              uint64_t bd;
-              if constexpr (B_MN) bd = smem_desc(sb + kk * 2048, MN_ATOM, 1024);
-              else bd = smem_desc(sb + kk * 32, 16, 1024);
-              tc_mma_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) {   // K32 steps of 32 bytes
+                const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024);
+                tc_mma_pair_mx(d_tmem, ad, bd, IDESC | mx_sf_ids(kk, kk), t_sfa, t_sfb,
+                               (kb | kk) != 0 ? 1u : 0u);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+                uint64_t bd;
+                if constexpr (B_MN) bd = smem_desc(sb + kk * 2048, MN_ATOM, 1024);
+                else bd = smem_desc(sb + kk * 32, 16, 1024);
+                tc_mma_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+              }
             }
             tc_commit_pair_both(empty_bar(stage));
           }
@@ -1244,14 +1341,41 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D tensor map over a row-major [outer, inner] array of bytes (E4M3), 128-byte swizzle.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                 uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map over n_atoms 512-byte scale atoms (as [n_atoms, 128] uint32), one atom per box.
+bool make_map_atoms(CUtensorMap* m, const void* base, uint64_t n_atoms) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, n_atoms};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 #ifndef MOE_PAIR_BN_MAX
 #define MOE_PAIR_BN_MAX 256
 #endif
 
-template <int KIND, int BN, int STAGES>
+template <int KIND, int BN, int STAGES, bool FP8 = false>
 constexpr size_t pair_smem_bytes(int E) {
-  return 1024 + STAGES * (BM * BK * 2 + (BN / 2) * BK * 2) + pair_epi_bytes<KIND>() +
-         8 * (2 * STAGES + 9) + 16 + sizeof(int) * 2 * (E + 1) + 16;
+  return 1024 + STAGES * (BM * BK * 2 + (BN / 2) * BK * 2 + (FP8 ? 1024 : 0)) +
+         pair_epi_bytes<KIND>() + 8 * (2 * STAGES + 9) + 16 + sizeof(int) * 2 * (E + 1) + 16;
 }
 
 // Launches a cluster-of-two kernel on as many clusters as can be resident
@@ -1299,17 +1423,19 @@ int launch_cluster2(void (*kern)(KArgs...), size_t sm, size_t sm_max, int* confi
 
 // Launches the CTA-pair kernel of a forward or input-gradient kind with the
 // shared-memory opt-in sized for the largest expert count it is used with.
-template <int KIND, int BN, int STAGES>
+template <int KIND, int BN, int STAGES, bool FP8 = false>
 int launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
-                long long tiles_upper, int e_max, cudaStream_t st) {
+                const CUtensorMap& c0, const CUtensorMap& c1, const CUtensorMap& s,
+                const Params& p, long long tiles_upper, int e_max, cudaStream_t st) {
   static thread_local int configured = -1;
   static thread_local int max_clusters = 0;
   static const char* kNames[] = {"gemm_gate_up", "gemm_down", "gemm_dh", "gemm_dx", "", ""};
-  return launch_cluster2(grouped_gemm_pair_kernel<KIND, BN, STAGES>,
-                         pair_smem_bytes<KIND, BN, STAGES>(p.E),
-                         pair_smem_bytes<KIND, BN, STAGES>(e_max), &configured, &max_clusters,
-                         tiles_upper, kNames[KIND], st, a, b0, b1, c0, c1, p);
+  static const char* kNamesFp8[] = {"gemm_gate_up_fp8", "gemm_down_fp8", "", "", "", ""};
+  return launch_cluster2(grouped_gemm_pair_kernel<KIND, BN, STAGES, FP8>,
+                         pair_smem_bytes<KIND, BN, STAGES, FP8>(p.E),
+                         pair_smem_bytes<KIND, BN, STAGES, FP8>(e_max), &configured,
+                         &max_clusters, tiles_upper, FP8 ? kNamesFp8[KIND] : kNames[KIND], st, a,
+                         b0, b1, c0, c1, s, p);
 }
 
 // Weight gradients on CTA pairs: six 32 KB stages while the expert table fits
@@ -1350,10 +1476,11 @@ int launch_pair_wgrad(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
 constexpr long long kSmemOptIn = 232448;   // shared memory a CTA may opt into
 
 // Largest expert count whose offset tables fit beside STAGES pair stages (-1: none).
-template <int KIND, int BN, int STAGES>
+template <int KIND, int BN, int STAGES, bool FP8 = false>
 constexpr int pair_max_e() {
-  return static_cast<int>((kSmemOptIn - static_cast<long long>(pair_smem_bytes<KIND, BN, STAGES>(0))) /
-                          (2 * static_cast<long long>(sizeof(int))));
+  return static_cast<int>(
+      (kSmemOptIn - static_cast<long long>(pair_smem_bytes<KIND, BN, STAGES, FP8>(0))) /
+      (2 * static_cast<long long>(sizeof(int))));
 }
 
 // Pair pipeline depth. The shallow ring fits beside the expert tables of up to
@@ -1371,30 +1498,32 @@ constexpr int pair_stages_deep() {
   return BN == 256 ? 6 : 8;
 }
 
-template <int KIND, int BN>
+template <int KIND, int BN, bool FP8 = false>
 int launch_pair_depth(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                      const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
-                      long long tiles_upper, cudaStream_t st) {
+                      const CUtensorMap& c0, const CUtensorMap& c1, const CUtensorMap& s,
+                      const Params& p, long long tiles_upper, cudaStream_t st) {
   constexpr int kDeep = pair_stages_deep<KIND, BN>();
   constexpr int kShallow = pair_stages<KIND, BN>();
-  constexpr int kDeepMaxE = pair_max_e<KIND, BN, kDeep>();
-  static_assert(pair_max_e<KIND, BN, kShallow>() >= 1024, "shallow pair ring must fit 1024 experts");
+  constexpr int kDeepMaxE = pair_max_e<KIND, BN, kDeep, FP8>();
+  static_assert(pair_max_e<KIND, BN, kShallow, FP8>() >= 1024,
+                "shallow pair ring must fit 1024 experts");
   if constexpr (kDeepMaxE >= 1) {
     if (p.E <= kDeepMaxE)
-      return launch_pair<KIND, BN, kDeep>(a, b0, b1, c0, c1, p, tiles_upper,
-                                          kDeepMaxE < 1024 ? kDeepMaxE : 1024, st);
+      return launch_pair<KIND, BN, kDeep, FP8>(a, b0, b1, c0, c1, s, p, tiles_upper,
+                                               kDeepMaxE < 1024 ? kDeepMaxE : 1024, st);
   }
-  return launch_pair<KIND, BN, kShallow>(a, b0, b1, c0, c1, p, tiles_upper, 1024, st);
+  return launch_pair<KIND, BN, kShallow, FP8>(a, b0, b1, c0, c1, s, p, tiles_upper, 1024, st);
 }
 
 template <int KIND>
 int launch_pair_bn(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                    const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
                    long long tiles_upper, cudaStream_t st) {
+  // the scale-atom map is read by the MXFP8 instantiation only
 #if MOE_PAIR_BN_MAX >= 256
-  if (bn == 256) return launch_pair_depth<KIND, 256>(a, b0, b1, c0, c1, p, tiles_upper, st);
+  if (bn == 256) return launch_pair_depth<KIND, 256>(a, b0, b1, c0, c1, a, p, tiles_upper, st);
 #endif
-  return launch_pair_depth<KIND, 128>(a, b0, b1, c0, c1, p, tiles_upper, st);
+  return launch_pair_depth<KIND, 128>(a, b0, b1, c0, c1, a, p, tiles_upper, st);
 }
 
 // The N width a pair tile uses for an output of n columns (n % 128 == 0).
@@ -1408,6 +1537,28 @@ inline int pair_bn(int n) { return (n % 256 == 0 && MOE_PAIR_BN_MAX >= 256) ? 25
 size_t ffn_backward_scratch(long long M, int E, int d, int I) {
   return (static_cast<size_t>(M) * 2 * I + static_cast<size_t>(E) * 16 * (d + I)) * sizeof(uint16_t);
 }
+
+long long mxfp8_row_tiles(long long M, int E);                                     // fp8.cu
+int launch_quantize_rows(const void* x, const int32_t* offsets, int E, int M, int K, void* q,
+                         void* sf, cudaStream_t st);                               // fp8.cu
+
+// The MXFP8 forward's scratch: X and H quantized (E4M3 [M, d], [M, I]) with
+// their scale atoms, each region 1024-byte aligned.
+struct Fp8Scratch {
+  size_t xq, xsf, hq, hsf, total;
+};
+Fp8Scratch ffn_fp8_layout(long long M, int E, int d, int I) {
+  auto up = [](size_t b) { return (b + 1023) & ~static_cast<size_t>(1023); };
+  const long long tiles = mxfp8_row_tiles(M, E);
+  Fp8Scratch s;
+  s.xq = 0;
+  s.xsf = up(static_cast<size_t>(M) * d);
+  s.hq = s.xsf + up(static_cast<size_t>(tiles) * (d / 128) * 512);
+  s.hsf = s.hq + up(static_cast<size_t>(M) * I);
+  s.total = s.hsf + up(static_cast<size_t>(tiles) * (I / 128) * 512);
+  return s;
+}
+size_t ffn_fp8_scratch(long long M, int E, int d, int I) { return ffn_fp8_layout(M, E, d, I).total; }
 
 }  // namespace moe
 
@@ -1651,4 +1802,77 @@ extern "C" int moe_debug_wait_timeout(void* ws, int timeout_us, void* stream) {
   gemm::wait_timeout_kernel<<<1, 32, 0, as_stream(stream)>>>(
       static_cast<int*>(ws), static_cast<uint64_t>(timeout_us) * 1000ull);
   return check_launch();
+}
+
+extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, int E, int M, int d,
+                                   int I, const uint8_t* wgu_q, const uint8_t* wgu_sf,
+                                   const uint8_t* wd_q, const uint8_t* wd_sf, moe_bf16* y,
+                                   moe_bf16* h, moe_bf16* gu, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  using namespace moe;
+  using namespace moe::gemm;
+  if (!ffn_shape_ok(E, M, d, I)) {
+    if (E >= 1 && M >= 0 && d > 0 && I > 0 && d % 8 == 0 && I % 8 == 0) return MOE_ERR_UNSUPPORTED;
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (M == 0) return MOE_OK;
+  if (!xp || !offsets || !wgu_q || !wgu_sf || !wd_q || !wd_sf || !y || !h) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xp) || !aligned16(offsets) || !aligned16(wgu_q) || !aligned16(wgu_sf) ||
+      !aligned16(wd_q) || !aligned16(wd_sf) || !aligned16(y) || !aligned16(h) ||
+      (gu && !aligned16(gu)))
+    return MOE_ERR_MISALIGNED;
+  const Fp8Scratch lay = ffn_fp8_layout(M, E, d, I);
+  if (!ws || !aligned16(ws) || ws_bytes < kWorkspaceHeader + lay.total) return MOE_ERR_WORKSPACE;
+  if (cc_major() < 10) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  uint8_t* scratch = static_cast<uint8_t*>(ws) + kWorkspaceHeader;
+  uint8_t* xq = scratch + lay.xq;
+  uint8_t* xsf = scratch + lay.xsf;
+  uint8_t* hq = scratch + lay.hq;
+  uint8_t* hsf = scratch + lay.hsf;
+  const long long tiles = mxfp8_row_tiles(M, E);
+  Params p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.M = M;
+  p.d = d;
+  p.I = I;
+  p.status = static_cast<int*>(ws);
+  const long long mt_upper = (M + BM - 1) / BM + E;
+  int rc = launch_quantize_rows(xp, offsets, E, M, d, xq, xsf, st);
+  if (rc) return rc;
+  CUtensorMap ta, tb0, tb1, tc0, tc1, ts;
+  // gate/up on 256 x 128 pair tiles (64 gate + 64 up columns), SwiGLU epilogue
+  if (!make_map_u8(&ta, xq, d, M, 128, BM) ||
+      !make_map_u8(&tb0, wgu_q, d, static_cast<uint64_t>(E) * 2 * I, 128, 64) ||
+      !make_map_atoms(&tb1, xsf, static_cast<uint64_t>(tiles) * (d / 128)) ||
+      !make_map_atoms(&ts, wgu_sf, static_cast<uint64_t>(E) * (2 * I / 128) * (d / 128)) ||
+      !make_map(&tc0, h, I, M, 64, 32) ||
+      !make_map(&tc1, gu ? static_cast<const void*>(gu) : static_cast<const void*>(h),
+                gu ? 2 * static_cast<uint64_t>(I) : I, M, 64, 32))
+    return MOE_ERR_CUDA;
+  p.n_tiles = I / 64;
+  p.k_blocks = d / 128;
+  p.out = reinterpret_cast<__nv_bfloat16*>(h);
+  p.out2 = reinterpret_cast<__nv_bfloat16*>(gu);
+  p.ld_out = I;
+  rc = launch_pair_depth<FWD_GATEUP, 128, true>(ta, tb0, tb1, tc0, tc1, ts, p,
+                                                 mt_upper * p.n_tiles, st);
+  if (rc) return rc;
+  // H in bf16 is quantized along I for the down projection
+  rc = launch_quantize_rows(h, offsets, E, M, I, hq, hsf, st);
+  if (rc) return rc;
+  if (!make_map_u8(&ta, hq, I, M, 128, BM) ||
+      !make_map_u8(&tb0, wd_q, I, static_cast<uint64_t>(E) * d, 128, 64) ||
+      !make_map_atoms(&tb1, hsf, static_cast<uint64_t>(tiles) * (I / 128)) ||
+      !make_map_atoms(&ts, wd_sf, static_cast<uint64_t>(E) * (d / 128) * (I / 128)) ||
+      !make_map(&tc0, y, d, M, 64, 32))
+    return MOE_ERR_CUDA;
+  p.n_tiles = d / 128;
+  p.k_blocks = I / 128;
+  p.out = reinterpret_cast<__nv_bfloat16*>(y);
+  p.out2 = nullptr;
+  p.ld_out = d;
+  return launch_pair_depth<FWD_DOWN, 128, true>(ta, tb0, tb1, tc0, tc0, ts, p,
+                                                 mt_upper * p.n_tiles, st);
 }

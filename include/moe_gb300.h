@@ -70,7 +70,8 @@ enum moe_op {
   MOE_OP_GROUPED_FFN = 3,
   MOE_OP_GROUPED_FFN_BACKWARD = 4,
   MOE_OP_LOAD_BALANCE = 5,
-  MOE_OP_EP_RECV_LAYOUT = 6
+  MOE_OP_EP_RECV_LAYOUT = 6,
+  MOE_OP_GROUPED_FFN_FP8 = 7
 };
 
 /* Bytes of device workspace the operation needs for these sizes (0 on bad
@@ -434,6 +435,59 @@ int moe_dispatch_backward_slice(const moe_bf16* dxs, const int32_t* inv_perm,
  *   expert's output or input gradient on the local tokens). */
 int moe_reduce_finish(const float* partial, const moe_bf16* extra, int T, int d, moe_bf16* out,
                       void* stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 (MXFP8) grouped SwiGLU experts, forward. [XT] (xtuner PR "Decouple
+ * expert parallelism from FSDP sharding (dp2ep layout)") "Changes", the Float8
+ * bullet, and "Verification": tile-wise scaled FP8 training. The pages fix no
+ * format; this library takes the block-scaled format the tensor cores read
+ * natively: E4M3 elements and, for every 32 consecutive elements along the
+ * reduction dimension K, one power-of-two scale 2^X stored as a UE8M0 byte
+ * (X + 127), X = floor(log2(max |v| of the block)) - 8 clamped to
+ * [-127, 127] (-127 for an all-zero block); elements are v / 2^X rounded to
+ * the nearest E4M3 value, ties to even, saturating at 448.
+ *
+ * Scale layout: 512-byte atoms of 128 rows x 4 K32 blocks (one atom covers 128
+ * rows and 128 K), row r of an atom at byte (r % 32) * 16 + (r / 32) * 4 + j
+ * for its K32 block j; atoms ordered [row tile][K / 128].
+ * ------------------------------------------------------------------------ */
+
+/* Quantizes the expert-ordered rows x [M, K] bf16 (K contiguous): q [M, K]
+ * E4M3 and scale atoms sf. Row tiles follow the experts: the rows of expert e
+ * (offsets [E+1] int32, device) fill tiles from 2 * P(e) on, where P(e) =
+ * sum_{e' < e} ceil(ceil(n_e' / 128) / 2), 128 rows per tile (the layout the
+ * grouped GEMM reads). sf holds (ceil(M / 128) + 2E) * (K / 128) * 512 bytes;
+ * scales of rows past an expert's last row are not written. Rows past
+ * offsets[E] are not read or written. K % 128 == 0, 1 <= E <= 1024. */
+int moe_mxfp8_quantize_rows(const moe_bf16* x, const int32_t* offsets, int E, int M, int K,
+                            uint8_t* q, uint8_t* sf, void* stream);
+
+/* Quantizes expert weights for the FP8 GEMM, transposing them so that K is
+ * contiguous. w_a [E, K, N] bf16 (N contiguous), w_b NULL: q [E, N, K] E4M3 and
+ * sf [E, N / 128, K / 128] atoms (the down projection: K = I, N = d). With
+ * w_b [E, K, N] (gate = w_a, up = w_b; K = d, N = I): q [E, 2N, K] where rows
+ * 128 t .. 128 t + 63 are gate columns 64 t .. 64 t + 63 and rows 128 t + 64 ..
+ * 128 t + 127 the same up columns, sf [E, 2N / 128, K / 128] atoms.
+ * K % 128 == 0, N % 128 == 0. Run it again whenever the weights change. */
+int moe_mxfp8_quantize_weights(const moe_bf16* w_a, const moe_bf16* w_b, int E, int K, int N,
+                               uint8_t* q, uint8_t* sf, void* stream);
+
+/* A6 on MXFP8 operands: per expert e, rows [offsets[e], offsets[e+1]) of xp,
+ *   G = mx(X) mx(Wg[e]), U = mx(X) mx(Wu[e]) (fp32 accumulation),
+ *   gu = bf16([G | U]) (if gu != NULL), h = bf16(silu(G) * U),
+ *   y = bf16(mx(h) mx(Wd[e])),
+ * mx() the MXFP8 quantization along each GEMM's K (d for X and the gate/up
+ * weights, I for h and the down weights). xp is quantized inside the call;
+ * the weights come quantized by moe_mxfp8_quantize_weights (wgu_q / wgu_sf
+ * from gate and up, wd_q / wd_sf from down). Shapes, layouts and limits as
+ * moe_grouped_ffn (d % 128 == 0, I % 128 == 0); ws:
+ * moe_workspace_size(MOE_OP_GROUPED_FFN_FP8, M, E, 1, 1, d, I) bytes (the
+ * quantized xp and h with their scales). Runs on 256 x 128 CTA-pair tiles with
+ * tcgen05.mma kind::mxf8f6f4 and block scaling. */
+int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, int E, int M, int d, int I,
+                        const uint8_t* wgu_q, const uint8_t* wgu_sf, const uint8_t* wd_q,
+                        const uint8_t* wd_sf, moe_bf16* y, moe_bf16* h, moe_bf16* gu, void* ws,
+                        size_t ws_bytes, void* stream);
 
 /* Diagnostics: runs the bounded device-side wait that every mbarrier wait of
  * the GEMM kernels uses, on an mbarrier that nothing completes, with a limit of

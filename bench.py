@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--config", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the MXFP8 forward comparison")
     ap.add_argument("--no-side-configs", action="store_true",
                     help="report only the headline workload (no configs sub-object)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
@@ -686,6 +687,74 @@ def load_balance_block(cfg, layer, logits, dev, flush_l2, steps, pk):
     return out
 
 
+def fp8_block(cfg, layer, dev, flush_l2, steps, pk):
+    """The MXFP8 grouped-expert forward beside the bf16 one on the headline
+    workload's dispatched rows (the layer's own xp and offsets after its last
+    forward): per-launch events on the launching stream, L2 flushed before each
+    forward. The FP8 tensor peak is the measured bf16 one times the nominal
+    FP8 / bf16 ratio of 2."""
+    import torch
+    from grouped_gemm_moe_gb300 import binding as B
+    w = layer.w
+    TK, d, I, E = cfg.T * cfg.K, cfg.d, cfg.I, cfg.E
+    wgu = B.moe_mxfp8_quantize_weights(w["w_gate"], w["w_up"])
+    wdq = B.moe_mxfp8_quantize_weights(w["w_down"])
+    ws = B.new_workspace(B.workspace_size(B.MOE_OP_GROUPED_FFN_FP8, TK, E, 1, 1, d, I), dev)
+    out8 = (torch.empty(TK, d, dtype=torch.bfloat16, device=dev),
+            torch.empty(TK, I, dtype=torch.bfloat16, device=dev),
+            torch.empty(TK, 2 * I, dtype=torch.bfloat16, device=dev))
+    out16 = (layer.y, layer.h, layer.gu)
+
+    def both():
+        flush_l2()
+        B.moe_grouped_ffn(layer.xp, layer.offsets, w["w_gate"], w["w_up"], w["w_down"],
+                          ws=layer.ws_ffn, out=out16)
+        flush_l2()
+        B.moe_grouped_ffn_fp8(layer.xp, layer.offsets, wgu, wdq, ws=ws, out=out8)
+        flush_l2()
+        B.moe_mxfp8_quantize_weights(w["w_gate"], w["w_up"], out=wgu)
+        B.moe_mxfp8_quantize_weights(w["w_down"], out=wdq)
+
+    for _ in range(3):
+        both()
+    torch.cuda.synchronize()
+    B.moe_profile_start(16 * steps + 16)
+    for _ in range(steps):
+        both()
+    torch.cuda.synchronize()
+    rec = {}
+    for n, ms in B.moe_profile_stop():
+        rec.setdefault(n, []).append(ms)
+    avg = {n: statistics.mean(v) for n, v in rec.items()}
+    fl = {"gemm_gate_up": 4 * TK * d * I, "gemm_down": 2 * TK * d * I,
+          "gemm_gate_up_fp8": 4 * TK * d * I, "gemm_down_fp8": 2 * TK * d * I}
+    peak8 = 2 * pk["bf16_tflops"]
+    kern = {}
+    for n, ms in avg.items():
+        k = {"launches": len(rec[n]), "avg_us": round(ms * 1e3, 1)}
+        if n in fl:
+            tf = fl[n] / (ms * 1e-3) / 1e12
+            k["tflops"] = round(tf, 1)
+            k["frac"] = round(tf / (peak8 if n.endswith("_fp8") else pk["bf16_tflops"]), 4)
+        kern[n] = k
+    f16 = avg.get("gemm_gate_up", 0) + avg.get("gemm_down", 0)
+    # the call quantizes xp and h: two row-quantizer launches per forward
+    f8 = (avg.get("gemm_gate_up_fp8", 0) + avg.get("gemm_down_fp8", 0) +
+          2 * avg.get("mxfp8_quantize_rows", 0))
+    out = {"workload": f"{cfg.name} experts' forward on its dispatched rows (M={TK}, d={d}, I={I}, E={E})",
+           "format": "MXFP8: E4M3 elements, one UE8M0 scale per 32 K",
+           "peaks_tflops": {"bf16_measured_burst": pk["bf16_tflops"], "fp8_derived_burst": peak8},
+           "bf16_forward_ms": round(f16, 4),
+           "fp8_forward_ms": round(f8, 4),
+           "fp8_forward_ms_note": "both GEMMs plus the quantization of xp and h inside the call",
+           "speedup": round(f16 / f8, 3) if f8 else None,
+           "weight_quantization_ms": round(2 * avg.get("mxfp8_quantize_weights", 0), 4),
+           "kernels": kern}
+    del out8, ws, wgu, wdq
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     if args.profile_case:
@@ -762,6 +831,7 @@ def main():
             "avg_launch_ms": davg}
 
     load_balance = load_balance_block(cfg, layer, run.logits, dev, flush_l2, args.steps, pk)
+    fp8 = None if args.no_fp8 else fp8_block(cfg, layer, dev, flush_l2, min(args.steps, 10), pk)
 
     # end to end through the layer API with pinned host buffers
     e2e = None
@@ -822,7 +892,7 @@ def main():
             "aa": {"ms_per_step": statistics.mean(step_ms_aa),
                    "rel_diff": abs(statistics.mean(step_ms_aa) - statistics.mean(step_ms))
                    / statistics.mean(step_ms)},
-            "kernels": kernels, "configs": configs, "load_balance": load_balance,
+            "kernels": kernels, "configs": configs, "load_balance": load_balance, "fp8": fp8,
             "device": torch.cuda.get_device_name(dev),
         }
         print(json.dumps(line), flush=True)

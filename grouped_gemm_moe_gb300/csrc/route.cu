@@ -2,7 +2,8 @@
 // "Expert Parallel (EP)" -> "Producing assignments": scores [T,E] against all
 // experts, top-K selection of expert_IDs and router_weights [T,K]).
 //
-// Forward: one warp per token; lane l holds experts l, l+32, ... Logits become
+// Forward: a group of lanes per token (one warp per token above 256 experts);
+// lane l of the group holds experts l, l + G, ... Logits become
 // order-preserving unsigned keys (-0.0 and +0.0 share one key, so they tie),
 // and each of the K rounds is a warp-wide max over the lanes' best untaken
 // keys followed by a warp-wide min over the ids that hold it: the larger logit
@@ -79,6 +80,86 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int ren
   if (lane < K) {
     topk_idx[t * K + lane] = mine_id;
     topk_w[t * K + lane] = expf(mine - top) / denom;
+  }
+}
+
+// Small expert counts (E <= 256): a group of G lanes per token (G = 4, 8, 16 or
+// 32, so 32 / G tokens share each warp instruction), lane g of the group holding
+// experts g, g + G, ... (at most V = 8 each). Each round: the lane's best
+// untaken key (lowest id on equal keys), the group's max key by shuffles, then
+// the lowest id holding it by shuffles: the same rule as route_topk_kernel.
+// Slot j's id and logit stay with lane j % G of the group, which also writes
+// slot j; every lane accumulates the renormalised denominator in slot order.
+// With one token per warp the kernel above issues about 500 warp instructions
+// per token at E = 128, K = 8, and that issue rate, not memory, bounds it.
+template <int G, int V>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+route_topk_group_kernel(const float* __restrict__ logits, int T, int E, int K, int renorm,
+                        int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  static_assert(G >= 4 && G <= 32 && (G & (G - 1)) == 0 && V >= 1 && V <= 8, "group shape");
+  constexpr int SLOTS = (32 + G - 1) / G;   // slots per lane for K <= 32
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const int g = lane & (G - 1);
+  const long long t = (static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) *
+                          (32 / G) + lane / G;
+  const bool live = t < T;                  // dead groups follow along for the shuffles
+  const float* row = logits + (live ? t : 0) * E;
+  float v[V];
+  uint32_t key[V];
+  uint32_t avail = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = g + G * i;
+    const bool ok = live && e < E;
+    v[i] = ok ? __ldg(row + e) : 0.f;
+    key[i] = ok ? order_key(v[i]) : 0u;
+    if (ok) avail |= 1u << i;
+  }
+  float top = 0.f, den = 0.f;
+  float sv[SLOTS];
+  int sid[SLOTS];
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) { sv[s] = 0.f; sid[s] = 0; }
+  for (int j = 0; j < K; ++j) {
+    uint32_t bk = 0;
+    int bi = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (((avail >> i) & 1u) && key[i] > bk) { bk = key[i]; bi = i; }
+    uint32_t m = bk;
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    uint32_t id = (bk == m && bk != 0u) ? static_cast<uint32_t>(g + G * bi) : 0xffffffffu;
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) id = min(id, __shfl_xor_sync(0xffffffffu, id, o));
+    if (static_cast<int>(id % G) == g) avail &= ~(1u << (id / G));
+    const float val = key_value(m);
+    if (j == 0) top = val;
+    if (renorm) den += expf(val - top);
+    if ((j % G) == g) {
+#pragma unroll
+      for (int s = 0; s < SLOTS; ++s)
+        if (s == j / G) { sv[s] = val; sid[s] = static_cast<int>(id); }
+    }
+  }
+  if (!renorm) {   // softmax over all E: the group's sum of its lanes' terms
+    float part = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (g + G * i < E) part += expf(v[i] - top);
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    den = part;
+  }
+  if (!live) return;
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) {
+    const int j = s * G + g;
+    if (j < K) {
+      topk_idx[t * K + j] = sid[s];
+      topk_w[t * K + j] = expf(sv[s] - top) / den;
+    }
   }
 }
 
@@ -361,6 +442,20 @@ struct BwdLauncher {
 }  // namespace
 }  // namespace moe
 
+namespace moe {
+namespace {
+template <int G, int V>
+int launch_route_group(const float* logits, int T, int E, int K, int renorm, int32_t* idx,
+                       float* w, cudaStream_t st) {
+  const long long per_block = static_cast<long long>(kWarpsPerBlock) * (32 / G);
+  const int blocks = static_cast<int>((T + per_block - 1) / per_block);
+  ProfScope prof("route_topk", st);
+  return launch_pdl(route_topk_group_kernel<G, V>, blocks, kWarpsPerBlock * 32, 0, st, 1, logits,
+                    T, E, K, renorm, idx, w);
+}
+}  // namespace
+}  // namespace moe
+
 extern "C" int moe_route_topk(const float* logits, int T, int E, int K, int renorm,
                               int32_t* topk_idx, float* topk_w, void* stream) {
   using namespace moe;
@@ -368,7 +463,13 @@ extern "C" int moe_route_topk(const float* logits, int T, int E, int K, int reno
   if (T == 0) return MOE_OK;
   if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(topk_w)) return MOE_ERR_MISALIGNED;
-  return dispatch_v<FwdLauncher>(E, logits, T, E, K, renorm, topk_idx, topk_w, as_stream(stream));
+  cudaStream_t st = as_stream(stream);
+  // up to 8 logits per lane: a group of G = 4 .. 32 lanes per token
+  if (E <= 32) return launch_route_group<4, 8>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  if (E <= 64) return launch_route_group<8, 8>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  if (E <= 128) return launch_route_group<16, 8>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  if (E <= 256) return launch_route_group<32, 8>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  return dispatch_v<FwdLauncher>(E, logits, T, E, K, renorm, topk_idx, topk_w, st);
 }
 
 extern "C" int moe_route_topk_backward(const float* logits, const int32_t* topk_idx,

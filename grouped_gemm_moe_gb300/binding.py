@@ -75,6 +75,7 @@ SIGNATURES = {
     "moe_mxfp8_quantize_rows": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_mxfp8_quantize_weights": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_ffn_fp8": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_debug_check_status": (_I, [ctypes.POINTER(ctypes.c_int)]),
     "moe_read_device_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
     "moe_debug_wait_timeout": (_I, [_P, _I, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -680,6 +681,14 @@ def moe_debug_wait_timeout(ws: torch.Tensor, timeout_us: int):
     status word of ``ws`` then reads MOE_ERR_DEVICE_TIMEOUT."""
     _check("moe_debug_wait_timeout", load().moe_debug_wait_timeout(_ptr(ws), int(timeout_us),
                                                                     _stream(ws.device)))
+
+
+def moe_debug_check_status() -> int:
+    """The debug build's index-check record (synchronises; clears it). Raises
+    MoEError(MOE_ERR_UNSUPPORTED) on a release build."""
+    st = ctypes.c_int(0)
+    _check("moe_debug_check_status", load().moe_debug_check_status(ctypes.byref(st)))
+    return st.value
 
 
 def moe_read_device_status(ws: torch.Tensor) -> int:

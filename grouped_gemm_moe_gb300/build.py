@@ -20,6 +20,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
+# The debug variant: every gathered or scattered index range-checked, the GEMM
+# tile scheduler's offsets checked (-DMOE_DEBUG_CHECKS); its own objects and library.
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libmoe_gb300_debug.so")
 SOURCES = ["api.cu", "route.cu", "permute.cu", "gather.cu", "ep.cu", "fp8.cu", "grouped_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -51,24 +55,27 @@ def _flags_digest(cc: str, flags) -> str:
     return hashlib.sha256(("\0".join([cc, *flags])).encode()).hexdigest()
 
 
-STAMP = os.path.join(BUILD, "flags.sha256")
-
-
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Builds the library (or, with debug=True, the debug-checks variant) and
+    returns its path; objects are rebuilt when a source, the shared header or the
+    compiler flags changed."""
+    bdir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    flags = _flags(tuple(extra_flags) + (("-DMOE_DEBUG_CHECKS",) if debug else ()))
+    stamp = os.path.join(bdir, "flags.sha256")
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
-    digest = _flags_digest(cc, _flags(extra_flags))
+    digest = _flags_digest(cc, flags)
     try:
-        with open(STAMP) as f:
+        with open(stamp) as f:
             force = force or f.read().strip() != digest
     except OSError:
         force = True
     jobs = []
     for s in SOURCES:
         src = os.path.join(CSRC, s)
-        obj = os.path.join(BUILD, s.replace(".cu", ".o"))
+        obj = os.path.join(bdir, s.replace(".cu", ".o"))
         if force or _stale(src, obj):
-            jobs.append([cc, *_flags(extra_flags), "-c", src, "-o", obj])
+            jobs.append([cc, *flags, "-c", src, "-o", obj])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -80,14 +87,14 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         list(ex.map(run, jobs))
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
-    if force or jobs or not os.path.exists(LIB):
+    objs = [os.path.join(bdir, s.replace(".cu", ".o")) for s in SOURCES]
+    if force or jobs or not os.path.exists(lib):
         run([cc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
-             "-o", LIB, *objs])
-    with open(STAMP, "w") as f:
+             "-o", lib, *objs])
+    with open(stamp, "w") as f:
         f.write(digest + "\n")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, debug="--debug" in sys.argv))

@@ -104,6 +104,40 @@ extern "C" size_t moe_workspace_size(int op, int T, int E, int K, int R, int d, 
   }
 }
 
+#ifdef MOE_DEBUG_CHECKS
+namespace moe {
+int debug_status_route();
+int debug_status_permute();
+int debug_status_gather();
+int debug_status_ep();
+int debug_status_fp8();
+int debug_status_gemm();
+}  // namespace moe
+#endif
+
+extern "C" int moe_debug_check_status(int* host_status) {
+  if (!host_status) return MOE_ERR_INVALID_ARG;
+#ifdef MOE_DEBUG_CHECKS
+  using namespace moe;
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  int first = 0;
+  for (int v : {debug_status_route(), debug_status_permute(), debug_status_gather(),
+                debug_status_ep(), debug_status_fp8(), debug_status_gemm()}) {
+    if (v == MOE_ERR_CUDA) return MOE_ERR_CUDA;
+    if (!first) first = v;
+  }
+  *host_status = first;
+  return MOE_OK;
+#else
+  *host_status = 0;
+  return MOE_ERR_UNSUPPORTED;
+#endif
+}
+
 extern "C" int moe_read_device_status(void* ws, void* stream, int* host_status) {
   using namespace moe;
   if (!ws || !host_status) return MOE_ERR_INVALID_ARG;

@@ -160,4 +160,30 @@ __device__ __forceinline__ void report_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Debug builds (-DMOE_DEBUG_CHECKS): every gathered or scattered index is
+// range-checked before its access and the GEMM tile scheduler checks the
+// expert offsets. A failed check skips or redirects the access to a valid row
+// and records MOE_ERR_DEVICE_CHECK in the translation unit's debug status word
+// (read and cleared by moe_debug_check_status). Release builds compile the
+// checks away.
+#ifdef MOE_DEBUG_CHECKS
+static __device__ int g_debug_status;   // one per translation unit
+__device__ __forceinline__ bool index_ok(bool ok) {
+  if (!ok) atomicCAS(&g_debug_status, 0, static_cast<int>(MOE_ERR_DEVICE_CHECK));
+  return ok;
+}
+// Host side: this translation unit's debug status word, read and cleared.
+#define MOE_DEBUG_STATUS_READER(name)                                                   \
+  int debug_status_##name() {                                                           \
+    int v = 0, z = 0;                                                                   \
+    if (cudaMemcpyFromSymbol(&v, g_debug_status, sizeof(int)) != cudaSuccess ||         \
+        cudaMemcpyToSymbol(g_debug_status, &z, sizeof(int)) != cudaSuccess)            \
+      return MOE_ERR_CUDA;                                                              \
+    return v;                                                                           \
+  }
+#else
+__device__ __forceinline__ bool index_ok(bool) { return true; }
+#define MOE_DEBUG_STATUS_READER(name)
+#endif
+
 }  // namespace moe

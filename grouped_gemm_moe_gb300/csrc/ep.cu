@@ -433,3 +433,7 @@ extern "C" int moe_reduce_finish(const float* partial, const moe_bf16* extra, in
                     reinterpret_cast<const float4*>(partial),
                     reinterpret_cast<const uint4*>(extra), total, reinterpret_cast<uint4*>(out));
 }
+
+namespace moe {
+MOE_DEBUG_STATUS_READER(ep)
+}  // namespace moe

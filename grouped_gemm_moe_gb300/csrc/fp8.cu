@@ -224,3 +224,7 @@ extern "C" int moe_mxfp8_quantize_weights(const moe_bf16* w_a, const moe_bf16* w
                     reinterpret_cast<const __nv_bfloat16*>(w_a),
                     reinterpret_cast<const __nv_bfloat16*>(w_b), K, N, q, static_cast<uint8_t*>(sf));
 }
+
+namespace moe {
+MOE_DEBUG_STATUS_READER(fp8)
+}  // namespace moe

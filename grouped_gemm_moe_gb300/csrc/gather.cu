@@ -46,7 +46,9 @@ dispatch_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm, i
   const long long nwarps = static_cast<long long>(gridDim.x) * (kThreads / 32);
   for (long long p = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
        p < rows; p += nwarps) {
-    const long long t = __ldg(perm + p) / K;
+    long long a = __ldg(perm + p);
+    if (!index_ok(a >= 0 && a < rows)) a = 0;
+    const long long t = a / K;
     const uint4* src = x + t * nv;
     uint4* dst = xp + p * nv;
     for (int c0 = 0; c0 < nv; c0 += 32 * kRowVecs) {
@@ -111,7 +113,9 @@ dispatch_bulk_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ 
       if (i >= kBulkSlots)   // the store of row i - kBulkSlots has read this slot
         asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kBulkSlots - kBulkLag - 1) : "memory");
       const long long p = first + i * step;
-      const long long t = __ldg(perm + p) / K;
+      long long a = __ldg(perm + p);
+      if (!index_ok(a >= 0 && a < rows)) a = 0;
+      const long long t = a / K;
       const uint32_t bar = bar_addr + 8 * slot;
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                    "r"(row_bytes)
@@ -166,9 +170,11 @@ dispatch_scatter_kernel(const uint4* __restrict__ x, const int32_t* __restrict__
     for (int j = 0; j < KMAX; ++j)
       if (j < K) pos[j] = __ldg(ip + j);
     const uint4 v = ldg_nc_v4(x + i);
+    const long long rows = (total / nv) * K;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
-      if (j < K) stg_v4(xp + static_cast<long long>(pos[j]) * nv + c, v);
+      if (j < K && index_ok(pos[j] >= 0 && pos[j] < rows))
+        stg_v4(xp + static_cast<long long>(pos[j]) * nv + c, v);
   }
 }
 
@@ -187,9 +193,15 @@ gather_sum_kernel(const uint4* __restrict__ rows, const float* __restrict__ w,
     const int32_t* ip = inv_perm + t * K;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     uint4 v[KMAX];
+    const long long nrows = (total / nv) * K;
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j)
-      if (j < K) v[j] = ldg_nc_v4(rows + static_cast<long long>(__ldg(ip + j)) * nv + c);
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < K) {
+        long long pj = __ldg(ip + j);
+        if (!index_ok(pj >= 0 && pj < nrows)) pj = 0;
+        v[j] = ldg_nc_v4(rows + pj * nv + c);
+      }
+    }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (j < K) {
@@ -232,7 +244,12 @@ combine_backward_kernel(const uint4* __restrict__ dout, const uint4* __restrict_
        a < TK; a += warps) {
     const long long t = a / K;
     const uint4* drow = dout + t * nv;
-    const long long prow = static_cast<long long>(__ldg(inv_perm + a)) * nv;
+    const int pa = __ldg(inv_perm + a);
+    if (!index_ok(pa >= 0 && pa < TK)) {   // debug builds: nothing is read or written for it
+      if (lane == 0) dw[a] = 0.f;
+      continue;
+    }
+    const long long prow = static_cast<long long>(pa) * nv;
     const uint4* yrow = y + prow;
     uint4* orow = dy + prow;
     const float wa = __ldg(w + a);
@@ -404,3 +421,7 @@ extern "C" int moe_combine_backward(const moe_bf16* dout, const moe_bf16* y, con
                     reinterpret_cast<const uint4*>(y), topk_w, inv_perm, TK, K, d / 8,
                     reinterpret_cast<uint4*>(dy), dtopk_w);
 }
+
+namespace moe {
+MOE_DEBUG_STATUS_READER(gather)
+}  // namespace moe

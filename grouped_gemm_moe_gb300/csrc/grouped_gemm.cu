@@ -389,6 +389,27 @@ __device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const float (&v
   p[1] = b;
 }
 
+// Debug builds: the expert offsets the tile scheduler decodes must start at 0,
+// never decrease and end within the M rows; otherwise the kernel records
+// MOE_ERR_DEVICE_CHECK in the workspace status word and takes no tile. Every
+// thread of the block calls it (it ends with a block-wide vote). Release builds:
+// always true.
+__device__ __forceinline__ bool offsets_ok(const int* s_off, const Params& p) {
+#ifdef MOE_DEBUG_CHECKS
+  bool ok = true;
+  for (int e = threadIdx.x; e < p.E; e += kThreads) ok = ok && s_off[e] <= s_off[e + 1];
+  if (threadIdx.x == 0) ok = ok && s_off[0] == 0 && s_off[p.E] <= p.M;
+  ok = __syncthreads_and(ok) != 0;
+  if (!ok && threadIdx.x == 0) report_status(p.status, MOE_ERR_DEVICE_CHECK);
+  index_ok(ok);
+  return ok;
+#else
+  (void)s_off;
+  (void)p;
+  return true;
+#endif
+}
+
 // ----------------------------------------------------------------- CTA-pair kernel
 // Forward and input-gradient kinds on a cluster of two CTAs that share one
 // tcgen05 MMA of M = 256 (cta_group::2): each CTA holds 128 rows of A and half
@@ -607,6 +628,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     reinterpret_cast<uint32_t*>(p.status)[kTagFirst + threadIdx.x] = p.tag[threadIdx.x];
   for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
   __syncthreads();
+  const bool offs_ok = offsets_ok(s_off, p);
   if (warp == 0) {   // exclusive prefix of per-expert m-tile pairs
     int carry = 0;
     for (int base = 0; base <= p.E; base += 32) {
@@ -635,7 +657,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                : "memory");
   const bool tmem_ok = (peer_base == tmem_base);
   if (!tmem_ok && threadIdx.x == 0) report_status(p.status, MOE_ERR_DEVICE_CHECK);
-  const int total = tmem_ok ? s_mp[p.E] * p.n_tiles : 0;
+  const int total = (tmem_ok && offs_ok) ? s_mp[p.E] * p.n_tiles : 0;
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(n_clusters_x());
 
@@ -1097,6 +1119,7 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
   for (int e = threadIdx.x; e <= p.E; e += kThreads) s_off[e] = __ldg(p.offsets + e);
   tc_fence_before();
   __syncthreads();
+  const bool offs_ok = offsets_ok(s_off, p);
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -1115,7 +1138,7 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int i = 0; i < kTagWords; ++i) tag_ok = tag_ok && rec[i] == p.tag[i];
     if (!tag_ok && blockIdx.x == 0 && threadIdx.x == 0) report_status(p.status, MOE_ERR_DEVICE_CHECK);
   }
-  const int total = (tmem_ok && tag_ok) ? p.E * p.m_tiles * p.n_tiles : 0;
+  const int total = (tmem_ok && tag_ok && offs_ok) ? p.E * p.m_tiles * p.n_tiles : 0;
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(n_clusters_x());
 
@@ -1876,3 +1899,7 @@ extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, i
   return launch_pair_depth<FWD_DOWN, 128, true>(ta, tb0, tb1, tc0, tc0, ts, p,
                                                  mt_upper * p.n_tiles, st);
 }
+
+namespace moe {
+MOE_DEBUG_STATUS_READER(gemm)
+}  // namespace moe

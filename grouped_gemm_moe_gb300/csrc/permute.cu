@@ -52,12 +52,14 @@ __device__ __forceinline__ void chunk_range(const ChunkGeom& g, int c, long long
 // This warp's experts of the chunk, one per lane and step (-1 past the chunk),
 // loaded up front so that their latency overlaps whatever the block does next.
 __device__ __forceinline__ void load_warp_ids(const int32_t* __restrict__ idx, long long wstart,
-                                              long long end, int (&ev)[kSteps]) {
+                                              long long end, int E, int (&ev)[kSteps]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int st = 0; st < kSteps; ++st) {
     const long long a = wstart + st * 32 + lane;
-    ev[st] = (a < end) ? __ldg(idx + a) : -1;
+    int e = (a < end) ? __ldg(idx + a) : -1;
+    if (e >= 0 && !index_ok(e < E)) e = -1;   // debug builds: an id past E is dropped
+    ev[st] = e;
   }
 }
 
@@ -103,7 +105,7 @@ hist_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int32_t* __rest
   chunk_range(g, blockIdx.x, start, end, s);
   const int w = threadIdx.x >> 5;
   int ev[kSteps];
-  load_warp_ids(idx, start + static_cast<long long>(w) * kPerWarp, end, ev);
+  load_warp_ids(idx, start + static_cast<long long>(w) * kPerWarp, end, E, ev);
   warp_count(ev, wh + w * E);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kThreads) {
@@ -152,7 +154,7 @@ scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
   const int w = threadIdx.x >> 5;
   const long long wstart = start + static_cast<long long>(w) * kPerWarp;
   int ev[kSteps];
-  load_warp_ids(idx, wstart, end, ev);
+  load_warp_ids(idx, wstart, end, E, ev);
 
   for (int i = threadIdx.x; i < kWarps * E; i += kThreads) wh[i] = 0;
   // Table pass: per expert, sums of hist over all chunks, the chunks before this
@@ -235,8 +237,8 @@ scatter_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int NC,
 #pragma unroll
   for (int st = 0; st < kSteps; ++st) {
     const long long a = wstart + st * 32 + lane;
-    const bool valid = a < end;
     const int e = ev[st];
+    const bool valid = e >= 0;   // -1 past the chunk (and, in debug builds, for a dropped id)
     const unsigned grp = __match_any_sync(0xffffffffu, e);
     const int before = valid ? mine[e] : 0;
     __syncwarp();
@@ -515,3 +517,7 @@ extern "C" int moe_build_permutation_static(const int32_t* topk_idx, int T, int 
   return launch_pdl(scatter_kernel<false>, NC, kThreads, sh_scatter, st, 1, topk_idx, E, g, NC, hist,
                     po, eo);
 }
+
+namespace moe {
+MOE_DEBUG_STATUS_READER(permute)
+}  // namespace moe

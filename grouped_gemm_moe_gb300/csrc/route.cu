@@ -521,3 +521,7 @@ extern "C" int moe_load_balance_backward(const float* logits, const float* load_
   return dispatch_v<LbBwdLauncher>(E, logits, load_frac, T, E, coef, accumulate ? 1 : 0, dlogits,
                                    as_stream(stream));
 }
+
+namespace moe {
+MOE_DEBUG_STATUS_READER(route)
+}  // namespace moe

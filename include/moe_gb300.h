@@ -497,6 +497,18 @@ int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, int E, int M
  * usable; read the result with moe_read_device_status. */
 int moe_debug_wait_timeout(void* ws, int timeout_us, void* stream);
 
+/* Debug builds only (compiled with -DMOE_DEBUG_CHECKS; the package builds
+ * them as libmoe_gb300_debug.so): every gathered or scattered index (perm,
+ * inv_perm, the expert ids the permutation sorts, the regroup indices) is
+ * range-checked before its access, and the grouped GEMMs check their expert
+ * offsets (non-decreasing from 0, ending within M; on failure they also set the
+ * workspace status word and compute nothing). A failed check skips the access
+ * (or redirects a read to row 0) and records MOE_ERR_DEVICE_CHECK. This call
+ * synchronises the device, stores the first recorded code (0 if none) in
+ * *host_status and clears the record. Release builds return
+ * MOE_ERR_UNSUPPORTED. */
+int moe_debug_check_status(int* host_status);
+
 /* Reads the workspace's device status word after synchronising `stream`,
  * stores it in *host_status (a moe_status value, 0 if no kernel reported an
  * error) and clears it. The only call in this library that synchronises. */

@@ -64,7 +64,7 @@ def parse():
                     help="report only the headline workload (no configs sub-object)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--profile-case", choices=["gemm", "gemm_ragged", "gemm_l2", "layer", "hbm",
-                                               "routing", "combine_side"],
+                                               "routing", "combine_side", "fp8"],
                     default=None,
                     help="run a small fixed case twice for an ncu capture and exit")
     return ap.parse_args()
@@ -84,6 +84,8 @@ def profile_case(which: str):
     routing: the forward's front on the qwen3 workload at full size (route top-k, the fused
              permutation + EP layout with its host copy, token-major dispatch), run twice;
              ~0.4 GB on the device.
+    fp8:     the MXFP8 forward (weight quantization, then moe_grouped_ffn_fp8) on E=64 experts
+             x 512 rows (d=2048, I=768), run twice; ~1.5 GB on the device.
     combine_side: the combine, its backward and the dispatch backward at the qwen3 workload's
              full size (T=8192, d=2048, K=8; the routing of the qwen3 inputs), on synthetic
              expert outputs and gradients (~1.1 GB on the device), run twice, with 256 MiB
@@ -148,6 +150,22 @@ def profile_case(which: str):
                 B.moe_profile_start(64)
             B.moe_grouped_ffn_backward(dy, xp, gu, h, off, wg, wu, wd)
             B.moe_grouped_ffn(xp, off, wg, wu, wd)
+    elif which == "fp8":
+        E, d, I, rows = 64, 2048, 768, 512
+        M = E * rows
+        bf = torch.bfloat16
+        rnd = lambda *s, sc=1.0: (torch.randn(*s, device=dev, generator=g) * sc).to(bf)  # noqa: E731
+        off = (torch.arange(E + 1, dtype=torch.int32) * rows).to(dev)
+        xp = rnd(M, d)
+        wg, wu, wd = rnd(E, d, I, sc=0.02), rnd(E, d, I, sc=0.02), rnd(E, I, d, sc=0.02)
+        flops = {"gemm_gate_up_fp8": 4 * M * d * I, "gemm_down_fp8": 2 * M * d * I}
+        for it in range(2):
+            if it == 1:
+                torch.cuda.synchronize()
+                B.moe_profile_start(64)
+            wgu = B.moe_mxfp8_quantize_weights(wg, wu)
+            wdq = B.moe_mxfp8_quantize_weights(wd)
+            B.moe_grouped_ffn_fp8(xp, off, wgu, wdq)
     elif which == "combine_side":
         cfg = W.CONFIGS["qwen3"]
         inp = W.make_inputs(cfg, with_backward=False)

@@ -22,9 +22,9 @@
 //    pair tile mg's CTA rank. Rows of a tile past its expert's end have no
 //    scale written (the GEMM never stores their results).
 //  * Weights [E, K, N] (N contiguous): transposed to K-major rows [E, Nq, K] with
-//    tiles of 128 rows; gate and up are interleaved in blocks of 64 rows (rows
-//    128 t .. +63 gate columns 64 t .. +63, rows 128 t + 64 .. +127 the same up
-//    columns), so one 128-row tile is one pair GEMM's B with its SwiGLU halves.
+//    tiles of 128 rows; gate and up are interleaved in blocks of 128 rows (rows
+//    256 t .. +127 gate columns 128 t .. +127, rows 256 t + 128 .. +255 the same
+//    up columns), so 256 rows are one pair GEMM's B with its SwiGLU halves.
 //
 // Both kernels are HBM-bound streams: 16-byte loads of bf16, 8- or 16-byte
 // stores of E4M3, a scale byte per 32 elements.
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(128)
 quantize_weights_kernel(const __nv_bfloat16* __restrict__ wa, const __nv_bfloat16* __restrict__ wb,
                         int K, int N, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
   pdl_enter();
-  const int Nq = wb ? 2 * N : N;
+  const int Nq = wb ? 2 * N : N;   // with wb: N % 128 == 0, so 2N % 256 == 0
   const int n_tiles = Nq / 128;
   const int kb32 = K / 32;
   long long b = blockIdx.x;
@@ -149,8 +149,8 @@ quantize_weights_kernel(const __nv_bfloat16* __restrict__ wa, const __nv_bfloat1
   const __nv_bfloat16* src = wa;
   int col = nrow;
   if (wb) {
-    src = ((nrow >> 6) & 1) ? wb : wa;
-    col = (nrow >> 7) * 64 + (nrow & 63);
+    src = ((nrow >> 7) & 1) ? wb : wa;
+    col = (nrow >> 8) * 128 + (nrow & 127);
   }
   const __nv_bfloat16* p = src + (static_cast<size_t>(e) * K + static_cast<size_t>(j) * 32) * N + col;
   float v[32];

@@ -545,7 +545,7 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float (&v
 // then 128 K (the same 128-byte rows), B is K-major (the weights are quantized
 // into a transposed layout, gate and up interleaved in 64-row blocks), and each
 // stage also carries one 512-byte scale atom for the CTA's 128 A rows (tmB1)
-// and one for the pair's 128 B columns (tmS): 128 rows x 4 K32 scales, row r
+// and one per 128 of the pair's B columns (tmS): 128 rows x 4 K32 scales, row r
 // at byte (r % 32) * 16 + (r / 32) * 4 + k. The MMA thread copies both atoms
 // into TMEM (tcgen05.cp, 32 x 128 bit repeated over the four lane quarters,
 // four columns each, a column ring per stage beside the accumulators) before
@@ -562,16 +562,23 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmS, const Params p) {
   static_assert(KIND == FWD_GATEUP || KIND == FWD_DOWN || KIND == BWD_DH || KIND == BWD_DX,
                 "pair kernel: forward and input-gradient kinds");
-  static_assert(!FP8 || ((KIND == FWD_GATEUP || KIND == FWD_DOWN) && BN == 128),
-                "MXFP8: forward kinds on 256 x 128 pair tiles");
+  static_assert(!FP8 || ((KIND == FWD_GATEUP || KIND == FWD_DOWN) && (BN == 128 || BN == 256)),
+                "MXFP8: forward kinds on 256 x 128 or 256 x 256 pair tiles");
   constexpr bool B_MN = !FP8 && (KIND == FWD_GATEUP || KIND == FWD_DOWN);
   constexpr uint32_t A_BYTES = BM * BK * 2;          // 128 rows x 128 bytes (bf16 or fp8)
   constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;
-  constexpr uint32_t SF_BYTES = FP8 ? 1024u : 0u;    // scale atoms: A rows, then B columns
+  constexpr uint32_t SFB_ATOMS = BN / 128;           // scale atoms of the pair's B columns
+  // scale atoms per stage: the A rows' atom, then the B columns' atoms, padded to 1 KB
+  constexpr uint32_t SF_BYTES = FP8 ? ((512u * (1u + SFB_ATOMS) + 1023u) & ~1023u) : 0u;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+  // Accumulator buffers: two (the epilogue of tile i overlaps the MMAs of tile
+  // i + 1), except for MXFP8 256 x 256 tiles, whose 256 columns leave the other
+  // half of TMEM to the scale ring.
+  constexpr int NACC = (FP8 && BN == 256) ? 1 : 2;
   constexpr uint32_t TMEM_COLS = FP8 ? 512u : 2u * BN;
-  constexpr uint32_t SF_COL0 = 2u * BN;              // scale columns: 8 per stage
-  static_assert(!FP8 || SF_COL0 + 8u * STAGES <= TMEM_COLS, "MXFP8 scale ring in TMEM");
+  constexpr uint32_t SF_COLS = 4u * (1u + SFB_ATOMS);   // TMEM columns of one stage's scales
+  constexpr uint32_t SF_COL0 = static_cast<uint32_t>(NACC) * BN;
+  static_assert(!FP8 || SF_COL0 + SF_COLS * STAGES <= TMEM_COLS, "MXFP8 scale ring in TMEM");
   constexpr uint32_t IDESC = FP8 ? make_idesc_mxf8<BN, 2 * BM>() : make_idesc<BN, false, B_MN, 2 * BM>();
   constexpr uint32_t MN_ATOM = 64 * 128;
 
@@ -675,7 +682,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           const uint32_t fb_local = full_bar(stage);
-          if (leader) mbar_expect_tx(fb_local, 2 * STAGE_BYTES);   // both CTAs' boxes
+          // both CTAs' boxes (the scale area's padding is not loaded)
+          if (leader)
+            mbar_expect_tx(fb_local, 2 * (FP8 ? A_BYTES + B_BYTES + 512u * (1u + SFB_ATOMS)
+                                              : STAGE_BYTES));
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           if constexpr (FP8) {
             // A rows, the CTA's 64 B rows (gate or up for gate/up: interleaved rows),
@@ -688,8 +698,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              tl.e * nq + nrow + static_cast<int>(rank) * (BN / 2));
             tma_load_2d_pair(sa + A_BYTES + B_BYTES, &tmB1, fb, 0,
                              (2 * tl.mg + static_cast<int>(rank)) * p.k_blocks + kb);
-            tma_load_2d_pair(sa + A_BYTES + B_BYTES + 512, &tmS, fb, 0,
-                             (tl.e * (nq / 128) + nrow / 128) * p.k_blocks + kb);
+#pragma unroll
+            for (uint32_t j = 0; j < SFB_ATOMS; ++j)
+              tma_load_2d_pair(sa + A_BYTES + B_BYTES + 512 * (1 + j), &tmS, fb, 0,
+                               (tl.e * (nq / 128) + nrow / 128 + static_cast<int>(j)) * p.k_blocks +
+                                   kb);
           } else {
             issue_pair<KIND, BN>(tl, kb, rank, p, &tmA, &tmB0, &tmB1, sa, sa + A_BYTES,
                                  map_to_rank(fb_local, 0));
@@ -732,11 +745,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t sb = sa + A_BYTES;
           if (lane == 0) {
             if constexpr (FP8) {
-              const uint32_t t_sfa = tmem_base + SF_COL0 + 8u * static_cast<uint32_t>(stage);
+              const uint32_t t_sfa = tmem_base + SF_COL0 + SF_COLS * static_cast<uint32_t>(stage);
               const uint32_t t_sfb = t_sfa + 4u;
               const uint32_t sf = sb + B_BYTES;
               tc_cp_pair_32x128(t_sfa, smem_desc_rows16(sf));
-              tc_cp_pair_32x128(t_sfb, smem_desc_rows16(sf + 512));
+#pragma unroll
+              for (uint32_t j = 0; j < SFB_ATOMS; ++j)
+                tc_cp_pair_32x128(t_sfb + 4u * j, smem_desc_rows16(sf + 512 * (1 + j)));
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {   // K32 steps of 32 bytes
                 const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
@@ -762,8 +777,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!ok) break;
         if (lane == 0) tc_commit_pair_both(tfull_bar(acc));
         __syncwarp();
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
       }
       if (lane == 0) {
         tc_commit_pair_local(drain_bar);
@@ -963,8 +977,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
     }
     if constexpr (KIND == BWD_DH) {
       if (lane == 0 && aux_pending) {
@@ -1397,7 +1410,8 @@ bool make_map_atoms(CUtensorMap* m, const void* base, uint64_t n_atoms) {
 
 template <int KIND, int BN, int STAGES, bool FP8 = false>
 constexpr size_t pair_smem_bytes(int E) {
-  return 1024 + STAGES * (BM * BK * 2 + (BN / 2) * BK * 2 + (FP8 ? 1024 : 0)) +
+  return 1024 + STAGES * (BM * BK * 2 + (BN / 2) * BK * 2 +
+                          (FP8 ? ((512 * (1 + BN / 128) + 1023) & ~1023) : 0)) +
          pair_epi_bytes<KIND>() + 8 * (2 * STAGES + 9) + 16 + sizeof(int) * 2 * (E + 1) + 16;
 }
 
@@ -1865,37 +1879,42 @@ extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, i
   int rc = launch_quantize_rows(xp, offsets, E, M, d, xq, xsf, st);
   if (rc) return rc;
   CUtensorMap ta, tb0, tb1, tc0, tc1, ts;
-  // gate/up on 256 x 128 pair tiles (64 gate + 64 up columns), SwiGLU epilogue
+  // gate/up on 256 x 256 pair tiles (128 gate + 128 up columns), SwiGLU epilogue
   if (!make_map_u8(&ta, xq, d, M, 128, BM) ||
-      !make_map_u8(&tb0, wgu_q, d, static_cast<uint64_t>(E) * 2 * I, 128, 64) ||
+      !make_map_u8(&tb0, wgu_q, d, static_cast<uint64_t>(E) * 2 * I, 128, 128) ||
       !make_map_atoms(&tb1, xsf, static_cast<uint64_t>(tiles) * (d / 128)) ||
       !make_map_atoms(&ts, wgu_sf, static_cast<uint64_t>(E) * (2 * I / 128) * (d / 128)) ||
       !make_map(&tc0, h, I, M, 64, 32) ||
       !make_map(&tc1, gu ? static_cast<const void*>(gu) : static_cast<const void*>(h),
                 gu ? 2 * static_cast<uint64_t>(I) : I, M, 64, 32))
     return MOE_ERR_CUDA;
-  p.n_tiles = I / 64;
+  p.n_tiles = I / 128;
   p.k_blocks = d / 128;
   p.out = reinterpret_cast<__nv_bfloat16*>(h);
   p.out2 = reinterpret_cast<__nv_bfloat16*>(gu);
   p.ld_out = I;
-  rc = launch_pair_depth<FWD_GATEUP, 128, true>(ta, tb0, tb1, tc0, tc1, ts, p,
+  rc = launch_pair_depth<FWD_GATEUP, 256, true>(ta, tb0, tb1, tc0, tc1, ts, p,
                                                  mt_upper * p.n_tiles, st);
   if (rc) return rc;
   // H in bf16 is quantized along I for the down projection
   rc = launch_quantize_rows(h, offsets, E, M, I, hq, hsf, st);
   if (rc) return rc;
+  // down on 256 x 256 pair tiles (256 x 128 when d is an odd multiple of 128)
+  const int bn = pair_bn(d);
   if (!make_map_u8(&ta, hq, I, M, 128, BM) ||
-      !make_map_u8(&tb0, wd_q, I, static_cast<uint64_t>(E) * d, 128, 64) ||
+      !make_map_u8(&tb0, wd_q, I, static_cast<uint64_t>(E) * d, 128, bn / 2) ||
       !make_map_atoms(&tb1, hsf, static_cast<uint64_t>(tiles) * (I / 128)) ||
       !make_map_atoms(&ts, wd_sf, static_cast<uint64_t>(E) * (d / 128) * (I / 128)) ||
       !make_map(&tc0, y, d, M, 64, 32))
     return MOE_ERR_CUDA;
-  p.n_tiles = d / 128;
+  p.n_tiles = d / bn;
   p.k_blocks = I / 128;
   p.out = reinterpret_cast<__nv_bfloat16*>(y);
   p.out2 = nullptr;
   p.ld_out = d;
+  if (bn == 256)
+    return launch_pair_depth<FWD_DOWN, 256, true>(ta, tb0, tb1, tc0, tc0, ts, p,
+                                                   mt_upper * p.n_tiles, st);
   return launch_pair_depth<FWD_DOWN, 128, true>(ta, tb0, tb1, tc0, tc0, ts, p,
                                                  mt_upper * p.n_tiles, st);
 }

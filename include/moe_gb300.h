@@ -466,8 +466,8 @@ int moe_mxfp8_quantize_rows(const moe_bf16* x, const int32_t* offsets, int E, in
  * contiguous. w_a [E, K, N] bf16 (N contiguous), w_b NULL: q [E, N, K] E4M3 and
  * sf [E, N / 128, K / 128] atoms (the down projection: K = I, N = d). With
  * w_b [E, K, N] (gate = w_a, up = w_b; K = d, N = I): q [E, 2N, K] where rows
- * 128 t .. 128 t + 63 are gate columns 64 t .. 64 t + 63 and rows 128 t + 64 ..
- * 128 t + 127 the same up columns, sf [E, 2N / 128, K / 128] atoms.
+ * 256 t .. 256 t + 127 are gate columns 128 t .. 128 t + 127 and rows
+ * 256 t + 128 .. 256 t + 255 the same up columns, sf [E, 2N / 128, K / 128] atoms.
  * K % 128 == 0, N % 128 == 0. Run it again whenever the weights change. */
 int moe_mxfp8_quantize_weights(const moe_bf16* w_a, const moe_bf16* w_b, int E, int K, int N,
                                uint8_t* q, uint8_t* sf, void* stream);
@@ -482,7 +482,8 @@ int moe_mxfp8_quantize_weights(const moe_bf16* w_a, const moe_bf16* w_b, int E, 
  * from gate and up, wd_q / wd_sf from down). Shapes, layouts and limits as
  * moe_grouped_ffn (d % 128 == 0, I % 128 == 0); ws:
  * moe_workspace_size(MOE_OP_GROUPED_FFN_FP8, M, E, 1, 1, d, I) bytes (the
- * quantized xp and h with their scales). Runs on 256 x 128 CTA-pair tiles with
+ * quantized xp and h with their scales). Runs on 256 x 256 CTA-pair tiles
+ * (256 x 128 for the down projection when d is an odd multiple of 128) with
  * tcgen05.mma kind::mxf8f6f4 and block scaling. */
 int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, int E, int M, int d, int I,
                         const uint8_t* wgu_q, const uint8_t* wgu_sf, const uint8_t* wd_q,

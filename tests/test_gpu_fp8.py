@@ -98,8 +98,8 @@ def test_quantize_weights_bit_exact(E, K, N, pair):
             qb, Xb = MX.mx_quantize(W_f64(wb[e]), axis=0)
         for n in range(Nq):
             if pair:
-                src_b = (n // 64) % 2 == 1
-                col = (n // 128) * 64 + n % 64
+                src_b = (n // 128) % 2 == 1
+                col = (n // 256) * 128 + n % 128
                 rq, rX = (qb, Xb) if src_b else (qa, Xa)
             else:
                 col, rq, rX = n, qa, Xa

@@ -779,17 +779,21 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
               }
             }
           }
-          if (lane == 0) tc_commit_pair_both(empty_bar(stage));
-          __syncwarp();
           if constexpr (FP8) {
             if (kb + 1 < p.k_blocks) {   // the next stage's scales, once its loads have landed
               const int nst = (stage + 1 == STAGES) ? 0 : stage + 1;
               const uint32_t nph = (stage + 1 == STAGES) ? (phase ^ 1u) : phase;
-              if (!mbar_wait(full_bar(nst), nph, abort_flag, p.status)) { ok = false; break; }
+              if (!mbar_wait(full_bar(nst), nph, abort_flag, p.status)) {
+                ok = false;
+                if (lane == 0) tc_commit_pair_both(empty_bar(stage));
+                __syncwarp();
+                break;
+              }
               if (lane == 0) copy_scales(nst);
-              __syncwarp();
             }
           }
+          if (lane == 0) tc_commit_pair_both(empty_bar(stage));
+          __syncwarp();
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;

@@ -739,28 +739,19 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        // MXFP8: a stage's scale atoms go to its TMEM columns one k-block ahead of
-        // its MMAs (the first k-block of a tile just before them), so the copy
-        // overlaps the previous k-block's MMAs instead of preceding each stage's.
-        auto copy_scales = [&](int st) {
-          const uint32_t t_sfa = tmem_base + SF_COL0 + SF_COLS * static_cast<uint32_t>(st);
-          const uint32_t sf = smem_base + st * STAGE_BYTES + A_BYTES + B_BYTES;
-          tc_cp_pair_32x128(t_sfa, smem_desc_rows16(sf));
-#pragma unroll
-          for (uint32_t j = 0; j < SFB_ATOMS; ++j)
-            tc_cp_pair_32x128(t_sfa + 4u + 4u * j, smem_desc_rows16(sf + 512 * (1 + j)));
-        };
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
-          if constexpr (FP8) {
-            if (kb == 0 && lane == 0) copy_scales(stage);
-          }
           if (lane == 0) {
             if constexpr (FP8) {
               const uint32_t t_sfa = tmem_base + SF_COL0 + SF_COLS * static_cast<uint32_t>(stage);
               const uint32_t t_sfb = t_sfa + 4u;
+              const uint32_t sf = sb + B_BYTES;
+              tc_cp_pair_32x128(t_sfa, smem_desc_rows16(sf));
+#pragma unroll
+              for (uint32_t j = 0; j < SFB_ATOMS; ++j)
+                tc_cp_pair_32x128(t_sfb + 4u * j, smem_desc_rows16(sf + 512 * (1 + j)));
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {   // K32 steps of 32 bytes
                 const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
@@ -778,21 +769,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 tc_mma_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
               }
             }
+            tc_commit_pair_both(empty_bar(stage));
           }
-          if constexpr (FP8) {
-            if (kb + 1 < p.k_blocks) {   // the next stage's scales, once its loads have landed
-              const int nst = (stage + 1 == STAGES) ? 0 : stage + 1;
-              const uint32_t nph = (stage + 1 == STAGES) ? (phase ^ 1u) : phase;
-              if (!mbar_wait(full_bar(nst), nph, abort_flag, p.status)) {
-                ok = false;
-                if (lane == 0) tc_commit_pair_both(empty_bar(stage));
-                __syncwarp();
-                break;
-              }
-              if (lane == 0) copy_scales(nst);
-            }
-          }
-          if (lane == 0) tc_commit_pair_both(empty_bar(stage));
           __syncwarp();
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }

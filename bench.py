@@ -63,8 +63,8 @@ def parse():
     ap.add_argument("--no-side-configs", action="store_true",
                     help="report only the headline workload (no configs sub-object)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
-    ap.add_argument("--profile-case", choices=["gemm", "gemm_ragged", "gemm_l2", "layer", "hbm",
-                                               "routing", "combine_side", "fp8"],
+    ap.add_argument("--profile-case", choices=["gemm", "gemm_ragged", "gemm_l2", "gemm_drafter",
+                                               "layer", "hbm", "routing", "combine_side", "fp8"],
                     default=None,
                     help="run a small fixed case twice for an ncu capture and exit")
     return ap.parse_args()
@@ -77,6 +77,9 @@ def profile_case(which: str):
              (d=2048, I=768; the qwen3 workload's rows per expert), run twice.
     gemm_ragged: as gemm, with seeded expert sizes 512 + round(N(0, 21)) (the spread of the
              qwen3 workload's routed rows; most experts end inside a K16 step), run twice.
+    gemm_drafter: the grouped-GEMM entry points on the drafter workload's expert shape (d=4096,
+             I=2048) with E=8 experts of 4096 + round(N(0, 64)) rows (~3.2 GB on the device),
+             run twice: the tensor-bound regime of the headline workload.
     gemm_l2: the same entry points on one expert of 16384 rows (d=2048, I=768): weights
              and activations mostly resident in L2, which isolates the kernels' own
              pipeline from DRAM streaming.
@@ -128,11 +131,13 @@ def profile_case(which: str):
     dev = torch.device("cuda:0")
     g = torch.Generator(device=dev).manual_seed(0)
     flops = {}
-    if which in ("gemm", "gemm_ragged", "gemm_l2"):
-        E, d, I, rows = (1, 2048, 768, 16384) if which == "gemm_l2" else (64, 2048, 768, 512)
-        if which == "gemm_ragged":
+    if which in ("gemm", "gemm_ragged", "gemm_l2", "gemm_drafter"):
+        E, d, I, rows = {"gemm_l2": (1, 2048, 768, 16384),
+                         "gemm_drafter": (8, 4096, 2048, 4096)}.get(which, (64, 2048, 768, 512))
+        if which in ("gemm_ragged", "gemm_drafter"):
             gc = torch.Generator().manual_seed(3)
-            sizes = (rows + torch.randn(E, generator=gc) * 21).round().clamp(min=1).to(torch.int64)
+            spread = 64 if which == "gemm_drafter" else 21
+            sizes = (rows + torch.randn(E, generator=gc) * spread).round().clamp(min=1).to(torch.int64)
         else:
             sizes = torch.full((E,), rows, dtype=torch.int64)
         M = int(sizes.sum())

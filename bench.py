@@ -64,7 +64,8 @@ def parse():
                     help="report only the headline workload (no configs sub-object)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--profile-case", choices=["gemm", "gemm_ragged", "gemm_l2", "gemm_drafter",
-                                               "layer", "hbm", "routing", "combine_side", "fp8"],
+                                               "gemm_drafter64", "layer", "hbm", "routing",
+                                               "combine_side", "fp8"],
                     default=None,
                     help="run a small fixed case twice for an ncu capture and exit")
     return ap.parse_args()
@@ -80,6 +81,7 @@ def profile_case(which: str):
     gemm_drafter: the grouped-GEMM entry points on the drafter workload's expert shape (d=4096,
              I=2048) with E=8 experts of 4096 + round(N(0, 64)) rows (~3.2 GB on the device),
              run twice: the tensor-bound regime of the headline workload.
+    gemm_drafter64: the same with all 64 of the drafter's experts (~21 GB on the device).
     gemm_l2: the same entry points on one expert of 16384 rows (d=2048, I=768): weights
              and activations mostly resident in L2, which isolates the kernels' own
              pipeline from DRAM streaming.
@@ -131,12 +133,13 @@ def profile_case(which: str):
     dev = torch.device("cuda:0")
     g = torch.Generator(device=dev).manual_seed(0)
     flops = {}
-    if which in ("gemm", "gemm_ragged", "gemm_l2", "gemm_drafter"):
+    if which in ("gemm", "gemm_ragged", "gemm_l2", "gemm_drafter", "gemm_drafter64"):
         E, d, I, rows = {"gemm_l2": (1, 2048, 768, 16384),
-                         "gemm_drafter": (8, 4096, 2048, 4096)}.get(which, (64, 2048, 768, 512))
-        if which in ("gemm_ragged", "gemm_drafter"):
+                         "gemm_drafter": (8, 4096, 2048, 4096),
+                         "gemm_drafter64": (64, 4096, 2048, 4096)}.get(which, (64, 2048, 768, 512))
+        if which in ("gemm_ragged", "gemm_drafter", "gemm_drafter64"):
             gc = torch.Generator().manual_seed(3)
-            spread = 64 if which == "gemm_drafter" else 21
+            spread = 21 if which == "gemm_ragged" else 64
             sizes = (rows + torch.randn(E, generator=gc) * spread).round().clamp(min=1).to(torch.int64)
         else:
             sizes = torch.full((E,), rows, dtype=torch.int64)

@@ -838,7 +838,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         tc_fence_after();
         const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
         bool ok = true;
-        for (int c0 = 0; c0 < BN; c0 += 64) {
+        // with I an odd multiple of 128 the last n-tile's upper half lies past
+        // column I: its accumulator columns are neither read nor stored
+        const int cend = min(BN, p.I - tl.n0);
+        for (int c0 = 0; c0 < cend; c0 += 64) {
           if (c0) request(c0);
           if (!mbar_wait(ab, aux_phase, abort_flag, p.status)) { ok = false; break; }
           aux_phase ^= 1u;
@@ -1732,14 +1735,17 @@ int ffn_backward_parts(int parts, const moe_bf16* dy, const moe_bf16* xp, const 
   CUtensorMap ta, tb0, tb1, tc0, tc1;
   int rc = MOE_OK;
   if (data) {
-    // dH = dY Wd^T with the SwiGLU backward epilogue -> [dG | dU]
-    const int bn_h = pair_bn(I);
+    // dH = dY Wd^T with the SwiGLU backward epilogue -> [dG | dU], on 256-wide
+    // tiles also when I is an odd multiple of 128 (the last tile's upper half
+    // reads the next expert's rows of Wd, or the TMA fill value, and stores
+    // nothing): 128-wide tiles fetch 1.5x the operand bytes per MMA flop.
+    const int bn_h = MOE_PAIR_BN_MAX >= 256 ? 256 : 128;
     if (!make_map(&ta, dy, d, M, 64, BM) ||
         !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h / 2) ||
         !make_map(&tc0, gu, 2 * static_cast<uint64_t>(I), M, 64, 32) ||
         !make_map(&tc1, dgu, 2 * static_cast<uint64_t>(I), M, 64, 32))
       return MOE_ERR_CUDA;
-    p.n_tiles = I / bn_h;
+    p.n_tiles = (I + bn_h - 1) / bn_h;
     p.k_blocks = d / BK;
     p.out = dgu;
     p.aux = reinterpret_cast<const __nv_bfloat16*>(gu);

@@ -86,7 +86,7 @@ def profile_case(which: str):
              and activations mostly resident in L2, which isolates the kernels' own
              pipeline from DRAM streaming.
     layer:   one qwen3-shaped layer at T=2048 tokens (forward + backward), run twice.
-    routing: the forward's front on the qwen3 workload at full size (route top-k, the fused
+    routing: the forward's front on the qwen3 workload at full size (the fused route +
              permutation + EP layout with its host copy, token-major dispatch), run twice;
              ~0.4 GB on the device.
     fp8:     the MXFP8 forward (weight quantization, then moe_grouped_ffn_fp8) on E=64 experts
@@ -206,9 +206,8 @@ def profile_case(which: str):
             if it == 1:
                 torch.cuda.synchronize()
                 B.moe_profile_start(64)
-            idx, w = B.moe_route_topk(logits, cfg.K, cfg.renorm)
-            res = B.moe_build_permutation_ep(idx, cfg.E, cfg.R, host_splits=host)
-            B.moe_dispatch_scatter(x, res[3], cfg.K)
+            res = B.moe_route_permute_ep(logits, cfg.K, cfg.R, cfg.renorm, host_splits=host)
+            B.moe_dispatch_scatter(x, res[5], cfg.K)
         torch.cuda.synchronize()
         for name, ms in B.moe_profile_stop():
             print(f"  {name:22s} {ms * 1e3:9.1f} us")
@@ -289,6 +288,10 @@ def kernel_work(name: str, cfg, shared: bool):
         return gemm[name]
     hbm = {
         "route_topk": T * (4 * E + 8 * K),
+        # the fused front: logits read and top-k written (route_hist), then the ids
+        # read and five index arrays written (place_ep)
+        "route_hist": T * (4 * E + 8 * K),
+        "place_ep": 24 * TK,
         "route_topk_backward": T * (12 * K + 4 * E),
         "perm_hist": 4 * TK, "perm_scatter": 12 * TK, "ep_hist": 4 * TK,
         # the layer's fused call also writes perm and inv_perm from the EP scatter
@@ -305,7 +308,9 @@ def kernel_work(name: str, cfg, shared: bool):
 NOMINAL_GBS = 7900.0
 NOMINAL_TFLOPS = 2250.0
 
-KERNEL_SOURCE = {"route": "route.cu", "perm": "permute.cu", "ep_": "permute.cu",
+KERNEL_SOURCE = {"route_hist": "front.cu", "place": "front.cu", "route": "route.cu",
+                 "perm": "permute.cu",
+                 "ep_": "permute.cu",
                  "dispatch": "gather.cu", "combine": "gather.cu", "gemm": "grouped_gemm.cu"}
 
 

@@ -35,6 +35,7 @@ MOE_OP_GROUPED_FFN_BACKWARD = 4
 MOE_OP_LOAD_BALANCE = 5
 MOE_OP_EP_RECV_LAYOUT = 6
 MOE_OP_GROUPED_FFN_FP8 = 7
+MOE_OP_ROUTE_PERMUTE_EP = 8
 
 WORKSPACE_HEADER = 256
 
@@ -54,6 +55,8 @@ SIGNATURES = {
     "moe_ep_layout": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_build_permutation_ep": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                       _SZ, _P]),
+    "moe_route_permute_ep": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                  _P, _P, _SZ, _P]),
     "moe_dispatch": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_dispatch_scatter": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_grouped_ffn": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -325,6 +328,38 @@ def moe_build_permutation_ep(topk_idx: torch.Tensor, E: int, R: int,
         _ptr(splits), _ptr(send), _ptr(a2a), _ptr(reg), _ptr(host_splits), _ptr(ws), ws.numel(),
         _stream(dev)))
     return counts, offsets, perm, inv, splits, send, a2a, reg, host_splits
+
+
+def moe_route_permute_ep(logits: torch.Tensor, K: int, R: int, renorm: int = 1,
+                         host_splits: Optional[torch.Tensor] = None,
+                         ws: Optional[torch.Tensor] = None, out=None):
+    """moe_route_topk and moe_build_permutation_ep in one launch. Returns
+    (topk_idx, topk_w, counts, offsets, perm, inv_perm, ep_splits, send_index,
+    a2a_index, regroup_index, host_splits); ``host_splits=False`` skips the
+    device-to-host copy."""
+    _need(logits, torch.float32, 2, "logits")
+    T, E = logits.shape
+    dev = logits.device
+    n = R * E + R * R
+    if host_splits is None:
+        host_splits = torch.empty(n, dtype=torch.int32, pin_memory=True)
+    elif host_splits is False:
+        host_splits = None
+    nbytes = workspace_size(MOE_OP_ROUTE_PERMUTE_EP, T, E, K, R)
+    if nbytes == 0:
+        raise ValueError("R must divide E and T")
+    if ws is None:
+        ws = new_workspace(nbytes, dev)
+    if out is None:
+        e = lambda *s: torch.empty(*s, dtype=torch.int32, device=dev)  # noqa: E731
+        out = (e(T, K), torch.empty(T, K, dtype=torch.float32, device=dev), e(E), e(E + 1),
+               e(T * K), e(T * K), e(n), e(T * K), e(T * K), e(T * K))
+    idx, w, counts, offsets, perm, inv, splits, send, a2a, reg = out
+    _check("moe_route_permute_ep", load().moe_route_permute_ep(
+        _ptr(logits), T, E, K, int(renorm), R, _ptr(idx), _ptr(w), _ptr(counts), _ptr(offsets),
+        _ptr(perm), _ptr(inv), _ptr(splits), _ptr(send), _ptr(a2a), _ptr(reg), _ptr(host_splits),
+        _ptr(ws), ws.numel(), _stream(dev)))
+    return idx, w, counts, offsets, perm, inv, splits, send, a2a, reg, host_splits
 
 
 def moe_dispatch(x: torch.Tensor, perm: torch.Tensor, K: int, out: Optional[torch.Tensor] = None):

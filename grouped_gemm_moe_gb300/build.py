@@ -24,7 +24,8 @@ LIB = os.path.join(PKG, "libmoe_gb300.so")
 # tile scheduler's offsets checked (-DMOE_DEBUG_CHECKS); its own objects and library.
 BUILD_DEBUG = os.path.join(PKG, "_build_debug")
 LIB_DEBUG = os.path.join(PKG, "libmoe_gb300_debug.so")
-SOURCES = ["api.cu", "route.cu", "permute.cu", "gather.cu", "ep.cu", "fp8.cu", "grouped_gemm.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "front.cu", "gather.cu", "ep.cu", "fp8.cu",
+           "grouped_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,7 +45,8 @@ def _stale(src: str, obj: str) -> bool:
     if not os.path.exists(obj):
         return True
     t = os.path.getmtime(obj)
-    deps = [src, os.path.join(CSRC, "common.cuh"), os.path.join(INCLUDE, "moe_gb300.h")]
+    deps = [src, os.path.join(INCLUDE, "moe_gb300.h")]
+    deps += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
     return any(os.path.getmtime(p) > t for p in deps)
 
 

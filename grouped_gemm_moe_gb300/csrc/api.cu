@@ -11,6 +11,7 @@ size_t permutation_workspace(long long TK, int E, int R);   // permute.cu
 size_t ffn_backward_scratch(long long M, int E, int d, int I);   // grouped_gemm.cu
 size_t load_balance_workspace(int E);                       // route.cu
 size_t ffn_fp8_scratch(long long M, int E, int d, int I);   // grouped_gemm.cu
+size_t route_permute_workspace(long long TK, int E, int R);   // front.cu
 
 namespace {
 thread_local int g_last_cuda_error = 0;
@@ -96,6 +97,9 @@ extern "C" size_t moe_workspace_size(int op, int T, int E, int K, int R, int d, 
       return load_balance_workspace(E);
     case MOE_OP_EP_RECV_LAYOUT:
       return kWorkspaceHeader;
+    case MOE_OP_ROUTE_PERMUTE_EP:
+      if (R < 1 || E % R || T % R) return 0;
+      return route_permute_workspace(TK, E, R);
     case MOE_OP_GROUPED_FFN_FP8:
       if (I < 128 || d < 128 || d % 128 || I % 128) return 0;
       return kWorkspaceHeader + ffn_fp8_scratch(TK, E, d, I);

@@ -155,6 +155,30 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
+// Exclusive scan of a[0..n) in shared memory by one warp (called by that warp
+// only): each lane sums a run of ceil(n / 32) consecutive entries, one warp
+// scan offsets the runs, and each lane rewrites its run (integer sums: exact in
+// any order).
+__device__ __forceinline__ void warp_exscan(int* a, int n) {
+  const int lane = threadIdx.x & 31;
+  const int per = (n + 31) >> 5;
+  const int b = min(lane * per, n), e = min(b + per, n);
+  int sum = 0;
+  for (int i = b; i < e; ++i) sum += a[i];
+  int x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  int run = x - sum;
+  for (int i = b; i < e; ++i) {
+    const int v = a[i];
+    a[i] = run;
+    run += v;
+  }
+}
+
 // Records a device-side error code in the workspace status word (first one wins).
 __device__ __forceinline__ void report_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);

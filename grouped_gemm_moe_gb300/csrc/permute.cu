@@ -75,24 +75,6 @@ __device__ __forceinline__ void warp_count(const int (&ev)[kSteps], int* wh) {
   }
 }
 
-// Exclusive scan of a[0..n) in shared memory by one warp (called by that warp only).
-__device__ __forceinline__ void warp_exscan(int* a, int n) {
-  const int lane = threadIdx.x & 31;
-  int carry = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    const int v = (i < n) ? a[i] : 0;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (i < n) a[i] = carry + x - v;
-    carry += __shfl_sync(0xffffffffu, x, 31);
-  }
-}
-
 __global__ void __launch_bounds__(kThreads)
 hist_kernel(const int32_t* __restrict__ idx, int E, ChunkGeom g, int32_t* __restrict__ hist) {
   pdl_enter();

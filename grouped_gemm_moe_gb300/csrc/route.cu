@@ -12,21 +12,12 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
-
-// Order-preserving map of a finite float to an unsigned key; 0 is never a key.
-__device__ __forceinline__ uint32_t order_key(float f) {
-  if (f == 0.f) f = 0.f;   // -0.0 -> +0.0
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
 
 // V = ceil(E / 32) logits per lane. Round j: each lane's best untaken key
 // (lowest id on equal keys), the warp max M of those (redux.sync), then the
@@ -83,75 +74,32 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int K, int ren
   }
 }
 
-// Small expert counts (E <= 256): a group of G lanes per token (G = 4, 8, 16 or
-// 32, so 32 / G tokens share each warp instruction), lane g of the group holding
-// experts g, g + G, ... (at most V = 8 each). Each round: the lane's best
+// Small expert counts (E <= 256): a group of G lanes per token (G = 4, 8 or 16,
+// so 32 / G tokens share each warp instruction), lane g of the group holding
+// experts g, g + G, ... (at most V = 16 each). Each round: the lane's best
 // untaken key (lowest id on equal keys), the group's max key by shuffles, then
 // the lowest id holding it by shuffles: the same rule as route_topk_kernel.
 // Slot j's id and logit stay with lane j % G of the group, which also writes
 // slot j; every lane accumulates the renormalised denominator in slot order.
 // With one token per warp the kernel above issues about 500 warp instructions
-// per token at E = 128, K = 8, and that issue rate, not memory, bounds it.
+// per token at E = 128, K = 8, and that issue rate, not memory, bounds it. Per
+// token and round the lanes' scans cost E / 32 compares whatever G is, while
+// the group's shuffles cost 2 G log2(G) / 32: small groups with 16 logits per
+// lane issue the fewest instructions.
 template <int G, int V>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 route_topk_group_kernel(const float* __restrict__ logits, int T, int E, int K, int renorm,
                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
-  static_assert(G >= 4 && G <= 32 && (G & (G - 1)) == 0 && V >= 1 && V <= 8, "group shape");
-  constexpr int SLOTS = (32 + G - 1) / G;   // slots per lane for K <= 32
+  constexpr int SLOTS = (32 + G - 1) / G;
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int g = lane & (G - 1);
   const long long t = (static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) *
                           (32 / G) + lane / G;
   const bool live = t < T;                  // dead groups follow along for the shuffles
-  const float* row = logits + (live ? t : 0) * E;
-  float v[V];
-  uint32_t key[V];
-  uint32_t avail = 0;
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int e = g + G * i;
-    const bool ok = live && e < E;
-    v[i] = ok ? __ldg(row + e) : 0.f;
-    key[i] = ok ? order_key(v[i]) : 0u;
-    if (ok) avail |= 1u << i;
-  }
-  float top = 0.f, den = 0.f;
-  float sv[SLOTS];
+  float sv[SLOTS], top, den;
   int sid[SLOTS];
-#pragma unroll
-  for (int s = 0; s < SLOTS; ++s) { sv[s] = 0.f; sid[s] = 0; }
-  for (int j = 0; j < K; ++j) {
-    uint32_t bk = 0;
-    int bi = 0;
-#pragma unroll
-    for (int i = 0; i < V; ++i)
-      if (((avail >> i) & 1u) && key[i] > bk) { bk = key[i]; bi = i; }
-    uint32_t m = bk;
-#pragma unroll
-    for (int o = 1; o < G; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    uint32_t id = (bk == m && bk != 0u) ? static_cast<uint32_t>(g + G * bi) : 0xffffffffu;
-#pragma unroll
-    for (int o = 1; o < G; o <<= 1) id = min(id, __shfl_xor_sync(0xffffffffu, id, o));
-    if (static_cast<int>(id % G) == g) avail &= ~(1u << (id / G));
-    const float val = key_value(m);
-    if (j == 0) top = val;
-    if (renorm) den += expf(val - top);
-    if ((j % G) == g) {
-#pragma unroll
-      for (int s = 0; s < SLOTS; ++s)
-        if (s == j / G) { sv[s] = val; sid[s] = static_cast<int>(id); }
-    }
-  }
-  if (!renorm) {   // softmax over all E: the group's sum of its lanes' terms
-    float part = 0.f;
-#pragma unroll
-    for (int i = 0; i < V; ++i)
-      if (g + G * i < E) part += expf(v[i] - top);
-#pragma unroll
-    for (int o = 1; o < G; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    den = part;
-  }
+  group_topk<G, V>(logits + (live ? t : 0) * E, live, g, E, K, renorm, sv, sid, top, den);
   if (!live) return;
 #pragma unroll
   for (int s = 0; s < SLOTS; ++s) {
@@ -464,11 +412,11 @@ extern "C" int moe_route_topk(const float* logits, int T, int E, int K, int reno
   if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(topk_w)) return MOE_ERR_MISALIGNED;
   cudaStream_t st = as_stream(stream);
-  // up to 8 logits per lane: a group of G = 4 .. 32 lanes per token
+  // up to 16 logits per lane: a group of G = 4 .. 16 lanes per token
   if (E <= 32) return launch_route_group<4, 8>(logits, T, E, K, renorm, topk_idx, topk_w, st);
-  if (E <= 64) return launch_route_group<8, 8>(logits, T, E, K, renorm, topk_idx, topk_w, st);
-  if (E <= 128) return launch_route_group<16, 8>(logits, T, E, K, renorm, topk_idx, topk_w, st);
-  if (E <= 256) return launch_route_group<32, 8>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  if (E <= 64) return launch_route_group<4, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  if (E <= 128) return launch_route_group<8, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
+  if (E <= 256) return launch_route_group<16, 16>(logits, T, E, K, renorm, topk_idx, topk_w, st);
   return dispatch_v<FwdLauncher>(E, logits, T, E, K, renorm, topk_idx, topk_w, st);
 }
 

@@ -1,7 +1,7 @@
 """One MoE layer's forward and backward on one GPU, as a fixed sequence of
 library calls on the current CUDA stream with every buffer preallocated.
 
-Forward:  moe_route_topk -> moe_build_permutation_ep (the permutation and
+Forward:  moe_route_permute_ep (router top-k, the permutation and
           the simulated expert-parallel layout from one pass, with the one
           device-to-host copy of the splits) -> moe_dispatch_scatter ->
           moe_grouped_ffn (routed experts; shared experts as E=1 on x) ->
@@ -51,7 +51,7 @@ class MoELayer:
         self.xp = e(TK, d, dt=bf)
         self.y, self.h, self.gu = e(TK, d, dt=bf), e(TK, I, dt=bf), e(TK, 2 * I, dt=bf)
         self.out = e(T, d, dt=bf)
-        self.ws_ep = B.new_workspace(B.workspace_size(B.MOE_OP_EP_LAYOUT, T, E, K, R), dev)
+        self.ws_ep = B.new_workspace(B.workspace_size(B.MOE_OP_ROUTE_PERMUTE_EP, T, E, K, R), dev)
         self.ws_ffn = B.new_workspace(B.workspace_size(B.MOE_OP_GROUPED_FFN, T, E, K, 1, d, I), dev)
         # backward buffers
         self.dy, self.dtopk_w = e(TK, d, dt=bf), e(T, K, dt=f32)
@@ -111,12 +111,11 @@ class MoELayer:
         self.logits, self.x = logits, x
         w = self.w
         K, E, R = self.K, self.E, self.R
-        self._run("route_topk", B.moe_route_topk, logits, K, self.renorm,
-                  out=(self.topk_idx, self.topk_w))
-        self._run("build_permutation_ep", B.moe_build_permutation_ep, self.topk_idx, E, R,
+        self._run("route_permute_ep", B.moe_route_permute_ep, logits, K, R, self.renorm,
                   host_splits=self.host_splits if copy_splits else False, ws=self.ws_ep,
-                  out=(self.counts, self.offsets, self.perm, self.inv_perm, self.ep_splits,
-                       self.send_index, self.a2a_index, self.regroup_index))
+                  out=(self.topk_idx, self.topk_w, self.counts, self.offsets, self.perm,
+                       self.inv_perm, self.ep_splits, self.send_index, self.a2a_index,
+                       self.regroup_index))
         if self.aux_loss_coef > 0:
             self._run("load_balance", B.moe_load_balance, logits, self.counts, K, ws=self.ws_lb,
                       out=(self.lb_frac, self.lb_pmean, self.lb_stats))

@@ -71,7 +71,8 @@ enum moe_op {
   MOE_OP_GROUPED_FFN_BACKWARD = 4,
   MOE_OP_LOAD_BALANCE = 5,
   MOE_OP_EP_RECV_LAYOUT = 6,
-  MOE_OP_GROUPED_FFN_FP8 = 7
+  MOE_OP_GROUPED_FFN_FP8 = 7,
+  MOE_OP_ROUTE_PERMUTE_EP = 8
 };
 
 /* Bytes of device workspace the operation needs for these sizes (0 on bad
@@ -220,6 +221,27 @@ int moe_build_permutation_ep(const int32_t* topk_idx, int T, int E, int K, int R
                              int32_t* ep_splits, int32_t* send_index, int32_t* a2a_index,
                              int32_t* regroup_index, int32_t* host_splits,
                              void* ws, size_t ws_bytes, void* stream);
+
+/* A1 + A2 + A3 + A4: the outputs of moe_route_topk followed by
+ * moe_build_permutation_ep, bit for bit (same arguments, layouts, host copy and
+ * limits as those calls; [TAS] "Producing assignments", "Dispatch, expert
+ * computation and combine"; [MOD] "Design" items 1-2), in two launches instead
+ * of three: the first routes a contiguous chunk of tokens per CTA (about one
+ * chunk per SM) and writes the chunk's expert histogram beside the top-k
+ * outputs; the second reads the whole histogram table into shared memory and
+ * places every assignment. Shapes outside the fused kernels (E > 256, more than
+ * 16384 assignments per chunk, tables beyond the shared memory) run
+ * moe_route_topk and moe_build_permutation_ep instead.
+ *   ws: moe_workspace_size(MOE_OP_ROUTE_PERMUTE_EP, T, E, K, R, 0, 0) bytes;
+ *       one workspace per stream (concurrent calls on one workspace race). A
+ *       bounded wait for the table that runs out records MOE_ERR_DEVICE_TIMEOUT
+ *       in the workspace status word (moe_read_device_status) and leaves the
+ *       permutation outputs unwritten. */
+int moe_route_permute_ep(const float* logits, int T, int E, int K, int renorm, int R,
+                         int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                         int32_t* perm, int32_t* inv_perm, int32_t* ep_splits,
+                         int32_t* send_index, int32_t* a2a_index, int32_t* regroup_index,
+                         int32_t* host_splits, void* ws, size_t ws_bytes, void* stream);
 
 /* A5. Dispatch gather ([TAS] "Producing assignments": the assignment buffer
  * in expert-major order; [MOD] "Design": the index_select half of the

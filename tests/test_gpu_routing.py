@@ -183,3 +183,65 @@ def test_build_permutation_ep_shapes(T, E, K, R):
     rng = np.random.default_rng(T * 11 + R)
     ridx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
     _check_perm_ep(ridx, T, E, K, R)
+
+
+def _check_route_permute(l, K, R, renorm, ws=None):
+    """The fused front against the oracle (route top-k, the permutation and the
+    EP layout) and bit for bit against the stand-alone route + permutation."""
+    T, E = l.shape
+    out = B.moe_route_permute_ep(to_dev(l, torch.float32), K, R, renorm, ws=ws)
+    torch.cuda.synchronize()
+    idx, w, counts, offsets, perm, inv, splits, send, a2a, reg, host = out
+    ridx, rw = O.route_topk(l.numpy(), K, renorm)
+    assert np.array_equal(i64(idx), ridx)
+    assert_rel_close(f64(w), rw, name="topk_w")
+    rc, ro = O.expert_counts_offsets(ridx, E)
+    rp, ri = O.stable_permutation(ridx, E)
+    ref = O.ep_layout(ridx, T, E, K, R)
+    assert np.array_equal(i64(counts), rc)
+    assert np.array_equal(i64(offsets), ro)
+    assert np.array_equal(i64(perm), rp)
+    assert np.array_equal(i64(inv), ri)
+    s = i64(splits)
+    assert np.array_equal(s[:R * E].reshape(R, E), ref["ep_counts"])
+    assert np.array_equal(s[R * E:].reshape(R, R), ref["send_splits"])
+    assert np.array_equal(host.numpy().astype(np.int64), s)
+    assert np.array_equal(i64(send), ref["send_index"])
+    assert np.array_equal(i64(a2a), ref["a2a_index"])
+    assert np.array_equal(i64(reg), ref["regroup_index"])
+    # the stand-alone kernels give the same bits (weights included)
+    sidx, sw = B.moe_route_topk(to_dev(l, torch.float32), K, renorm)
+    assert torch.equal(sidx, idx) and torch.equal(sw, w)
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_route_permute_ep_workloads(name):
+    cfg = W.CONFIGS[name]
+    _check_route_permute(_logits(cfg), cfg.K, cfg.R, cfg.renorm)
+
+
+@pytest.mark.parametrize("T,E,K,R,renorm", [(4, 4, 2, 2, 1), (64, 8, 2, 1, 0), (8192, 64, 6, 64, 1),
+                                            (6000, 16, 4, 4, 1), (12, 6, 3, 3, 0),
+                                            (1000, 256, 32, 8, 1), (40000, 32, 2, 8, 0),
+                                            (153, 33, 5, 1, 1), (300, 512, 8, 4, 1),
+                                            (65536, 128, 8, 8, 1)])
+def test_route_permute_ep_shapes(T, E, K, R, renorm):
+    """Odd chunk geometries (fewer tokens than SMs, senders of a few tokens,
+    chunks of more than 1024 assignments) and E > 256 (the stand-alone path)."""
+    g = torch.Generator().manual_seed(T + 13 * E + K)
+    _check_route_permute(torch.randn(T, E, generator=g) * 2, K, R, renorm)
+
+
+def test_route_permute_ep_ties_and_reuse():
+    """Three-valued logits (dense ties, signed zeros); the same workspace for
+    several calls in a row, with other routings in between."""
+    T, E, K, R = 4096, 128, 8, 8
+    ws = B.new_workspace(B.workspace_size(B.MOE_OP_ROUTE_PERMUTE_EP, T, E, K, R), dev())
+    g = torch.Generator().manual_seed(5)
+    for it in range(3):
+        l = torch.randint(-1, 2, (T, E), generator=g).to(torch.float32)
+        l[::3] = -l[::3]
+        if it == 1:
+            l = torch.randn(T, E, generator=g)
+        _check_route_permute(l, K, R, 1, ws=ws)
+    assert B.moe_read_device_status(ws) == 0

@@ -102,17 +102,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// bf16 of the exact product a*b, rounded once (to nearest, ties to even).
-// p = fl32(a*b) can only round differently from the exact product when p lies
-// exactly on a midpoint between two bf16 values; the FMA residual a*b - p
-// (exact) then says on which side the exact product lies, and p is nudged one
-// fp32 ulp that way before the bf16 rounding.
+// The exact product a*b prepared for one rounding to bf16 (to nearest, ties to
+// even, by the caller's pack): rounded to odd at fp32 first (truncated toward
+// zero, then the last bit set when the truncation was inexact, which the FMA
+// residual a*b - trunc tells exactly). Rounding to odd at a precision at least
+// two bits above the target's makes the second rounding (to nearest) correct:
+// Boldo and Melquiond, "Emulation of FMA and correctly rounded sums: proved
+// algorithms using rounding to odd" (IEEE Trans. Computers, 2008). The residual
+// is exact while it is representable, i.e. for |a*b| above about 2^-103; below
+// that a nonzero residual can round to zero and the odd bit be missed.
 __device__ __forceinline__ float mul_bf16_exact(float a, float b) {
-  const float p = a * b;
-  const float r = fmaf(a, b, -p);
-  uint32_t u = __float_as_uint(p);
-  if ((u & 0xffffu) == 0x8000u && r != 0.f) u += ((r > 0.f) == (p > 0.f)) ? 1u : 0xffffffffu;
-  return __uint_as_float(u);
+  const float pz = __fmul_rz(a, b);
+  const float r = fmaf(a, b, -pz);
+  return __uint_as_float(__float_as_uint(pz) | (r != 0.f ? 1u : 0u));
 }
 
 __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {

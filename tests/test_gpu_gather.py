@@ -108,3 +108,28 @@ def test_dispatch_backward(T, d, E, K, shared):
     ref = O.dispatch_backward(dxp.double().numpy(), inv, K, T,
                               None if dxs is None else dxs.double().numpy(), pre=True)
     assert_out_close(f64(dx), ref, name="dx")
+
+
+def test_combine_backward_rounding_midpoints():
+    """dy = bf16(w * dout) rounded once from the exact product, on inputs where
+    the fp32-rounded product lands exactly on a bf16 midpoint: there a second
+    rounding of the fp32 product would go the wrong way about half the time."""
+    T, d = 2048, 4096
+    g = np.random.default_rng(11)
+    dout = torch.from_numpy(g.standard_normal((T, d)).astype(np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy(g.uniform(0.05, 1.0, T).astype(np.float32))
+    # midpoint cases of this draw (fp32 product's low 16 bits == 0x8000 and inexact)
+    prod32 = (dout.float() * w[:, None]).numpy()
+    low = prod32.view(np.uint32) & 0xFFFF
+    exact = dout.double().numpy() * w.double().numpy()[:, None]
+    mid = (low == 0x8000) & (exact != prod32.astype(np.float64))
+    assert mid.sum() > 20, "the draw must contain midpoint products"
+    inv = np.arange(T, dtype=np.int32)
+    y = torch.zeros(T, d, dtype=torch.bfloat16)
+    dy, _ = B.moe_combine_backward(to_dev(dout, torch.bfloat16), to_dev(y, torch.bfloat16),
+                                   to_dev(w[:, None].contiguous(), torch.float32),
+                                   to_dev(inv, torch.int32))
+    rdy, _ = O.combine_backward(dout.double().numpy(), y.double().numpy(),
+                                w.double().numpy()[:, None], inv, 1)
+    got = f64(dy)
+    assert np.array_equal(got, rdy), "dy must be the correctly rounded product"

@@ -28,35 +28,12 @@
 //
 // Both kernels are HBM-bound streams: 16-byte loads of bf16, 8- or 16-byte
 // stores of E4M3, a scale byte per 32 elements.
-#include <cuda_fp8.h>
-
-#include "common.cuh"
+#include "mxfp8.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kQThreads = 256;
-
-__device__ __forceinline__ int mx_exponent(float amax) {
-  if (!(amax > 0.f)) return -127;
-  int ex;
-  frexpf(amax, &ex);                        // amax = m * 2^ex, m in [0.5, 1)
-  int X = (ex - 1) - 8;                     // floor(log2 amax) - E4M3's largest exponent
-  return X < -127 ? -127 : (X > 127 ? 127 : X);
-}
-
-// 2^-X as a float (X in [-127, 126]: the result is a normal float).
-__device__ __forceinline__ float inv_pow2(int X) { return __int_as_float((127 - X) << 23); }
-
-__device__ __forceinline__ uint32_t to_e4m3x4(float a, float b, float c, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return lo | (hi << 16);
-}
-
-__device__ __forceinline__ size_t atom_byte(long long atom, int r, int j) {
-  return static_cast<size_t>(atom) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
-}
 
 // Rows of x [M, K] bf16 -> q [M, K] E4M3 and scale atoms (expert-ordered row tiles).
 // A CTA takes whole rows (grid-stride); within a row a thread takes 16

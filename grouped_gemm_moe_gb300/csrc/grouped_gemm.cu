@@ -46,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "mxfp8.cuh"
 
 namespace moe {
 namespace gemm {
@@ -103,6 +104,8 @@ struct Params {
   PadJob pad[2];           // BWD_DH: the weight gradients' pads of X and H (a == null: none)
   int tag_mode;            // kTagNone, kTagWrite (data part's dH) or kTagCheck (weight part)
   uint32_t tag[kTagWords]; // the backward's scratch tag: magic, M, E, d, I, offsets (low 32 bits)
+  uint8_t* hq;             // MXFP8 gate/up: E4M3 of H for the down projection (null: not fused)
+  uint8_t* hsf;            //   and H's scale atoms (row tiles in the tile list's m-tile order)
 };
 
 // ----------------------------------------------------------------- PTX helpers
@@ -540,6 +543,27 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float (&v
   }
 }
 
+// One K32 block of H for the MXFP8 down projection: the values rounded to bf16
+// (as H is stored), their amax and power-of-two scale, and the 32 E4M3 bytes
+// (the row quantizer's arithmetic, element for element). Returns X (the byte
+// stored is X + 127).
+__device__ __forceinline__ int quantize_row32(const float (&h)[32], uint4 (&q)[2]) {
+  float hb[32];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    hb[i] = __bfloat162float(__float2bfloat16_rn(h[i]));
+    amax = fmaxf(amax, fabsf(hb[i]));
+  }
+  const int X = mx_exponent(amax);
+  const float sc = inv_pow2(X);
+  uint32_t* w = reinterpret_cast<uint32_t*>(q);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = to_e4m3x4(hb[4 * i] * sc, hb[4 * i + 1] * sc, hb[4 * i + 2] * sc, hb[4 * i + 3] * sc);
+  return X;
+}
+
 // FP8 = true: the forward kinds on MXFP8 operands (E4M3 elements, one UE8M0
 // scale per 32 K; tcgen05.mma kind::mxf8f6f4 with block scaling). A k-block is
 // then 128 K (the same 128-byte rows), B is K-major (the weights are quantized
@@ -903,6 +927,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           // staging at 8 KB per warp and leaves shared memory for a deeper ring.
           constexpr int HALF = BN / 2;
           const int nstreams = p.out2 ? 3 : 1;
+          // MXFP8: H's E4M3 copy for the down projection is written with the H
+          // stream, from the same registers (fused quantization: the bf16-rounded
+          // H of each K32 block, its amax, scale and elements, as the row
+          // quantizer computes them; each lane stores its row's 32 bytes)
+          const bool fuse_q = FP8 && p.hq != nullptr;
+          const int nst = nstreams;
+          const int rr = q * 32 + lane;                                // row in the CTA's m-tile
+          const long long qtile = 2LL * tl.mg + static_cast<long long>(rank);
           for (int c64 = 0; c64 < HALF; c64 += 64) {
             if (!full) {   // a slice that crosses the expert's end: row-wise stores
               for (int sub = 0; sub < 64; sub += 32) {
@@ -918,11 +950,21 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                     store32_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c64 + sub, g);
                     store32_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c64 + sub, u);
                   }
+                  if (fuse_q) {
+                    uint4 qb[2];
+                    const int X = quantize_row32(h, qb);
+                    uint4* dst = reinterpret_cast<uint4*>(p.hq + grow * p.I + tl.n0 + c64 + sub);
+                    dst[0] = qb[0];
+                    dst[1] = qb[1];
+                    const int col = tl.n0 + c64 + sub;
+                    p.hsf[atom_byte(qtile * (p.I / 128) + col / 128, rr, (col & 127) >> 5)] =
+                        static_cast<uint8_t>(X + 127);
+                  }
                 }
               }
               continue;
             }
-            for (int sidx = 0; sidx < nstreams; ++sidx) {
+            for (int sidx = 0; sidx < nst; ++sidx) {
               uint8_t* st = epi + ew * 8192 + buf * 4096;
               if (lane == 0) bulk_wait_read_1();   // the store that used this box is done
               __syncwarp();
@@ -935,6 +977,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                   tmem_wait_ld();
 #pragma unroll
                   for (int i = 0; i < 32; ++i) v[i] = silu_f(g[i]) * u[i];
+                  if (fuse_q) {
+                    uint4 qb[2];
+                    const int X = quantize_row32(v, qb);
+                    uint4* dst = reinterpret_cast<uint4*>(p.hq + grow * p.I + tl.n0 + c64 + sub);
+                    dst[0] = qb[0];
+                    dst[1] = qb[1];
+                    const int col = tl.n0 + c64 + sub;
+                    p.hsf[atom_byte(qtile * (p.I / 128) + col / 128, rr, (col & 127) >> 5)] =
+                        static_cast<uint8_t>(X + 127);
+                  }
                 } else {
                   tmem_ld32(tacc + (sidx == 1 ? 0 : HALF) + c64 + sub, v);
                   tmem_wait_ld();
@@ -1380,9 +1432,11 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D tensor map over a row-major [outer, inner] array of bytes (E4M3), 128-byte swizzle.
+// 2-D tensor map over a row-major [outer, inner] array of bytes (E4M3), 128-byte
+// swizzle unless another is given.
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                 uint32_t box_inner, uint32_t box_outer) {
+                 uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -1390,7 +1444,7 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1885,7 +1939,9 @@ extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, i
   int rc = launch_quantize_rows(xp, offsets, E, M, d, xq, xsf, st);
   if (rc) return rc;
   CUtensorMap ta, tb0, tb1, tc0, tc1, ts;
-  // gate/up on 256 x 256 pair tiles (128 gate + 128 up columns), SwiGLU epilogue
+  // gate/up on 256 x 256 pair tiles (128 gate + 128 up columns), SwiGLU epilogue;
+  // the epilogue also writes H's E4M3 copy and its scale atoms for the down
+  // projection (the quantization fused: no second pass over H)
   if (!make_map_u8(&ta, xq, d, M, 128, BM) ||
       !make_map_u8(&tb0, wgu_q, d, static_cast<uint64_t>(E) * 2 * I, 128, 128) ||
       !make_map_atoms(&tb1, xsf, static_cast<uint64_t>(tiles) * (d / 128)) ||
@@ -1899,12 +1955,13 @@ extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, i
   p.out = reinterpret_cast<__nv_bfloat16*>(h);
   p.out2 = reinterpret_cast<__nv_bfloat16*>(gu);
   p.ld_out = I;
+  p.hq = hq;
+  p.hsf = hsf;
   rc = launch_pair_depth<FWD_GATEUP, 256, true>(ta, tb0, tb1, tc0, tc1, ts, p,
                                                  mt_upper * p.n_tiles, st);
   if (rc) return rc;
-  // H in bf16 is quantized along I for the down projection
-  rc = launch_quantize_rows(h, offsets, E, M, I, hq, hsf, st);
-  if (rc) return rc;
+  p.hq = nullptr;
+  p.hsf = nullptr;
   // down on 256 x 256 pair tiles (256 x 128 when d is an odd multiple of 128)
   const int bn = pair_bn(d);
   if (!make_map_u8(&ta, hq, I, M, 128, BM) ||

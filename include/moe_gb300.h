@@ -499,8 +499,10 @@ int moe_mxfp8_quantize_weights(const moe_bf16* w_a, const moe_bf16* w_b, int E, 
  *   gu = bf16([G | U]) (if gu != NULL), h = bf16(silu(G) * U),
  *   y = bf16(mx(h) mx(Wd[e])),
  * mx() the MXFP8 quantization along each GEMM's K (d for X and the gate/up
- * weights, I for h and the down weights). xp is quantized inside the call;
- * the weights come quantized by moe_mxfp8_quantize_weights (wgu_q / wgu_sf
+ * weights, I for h and the down weights; mx(h) quantizes the bf16-rounded h).
+ * xp is quantized inside the call and mx(h) comes from the gate/up GEMM's
+ * epilogue, from the same registers as h; the weights come quantized by
+ * moe_mxfp8_quantize_weights (wgu_q / wgu_sf
  * from gate and up, wd_q / wd_sf from down). Shapes, layouts and limits as
  * moe_grouped_ffn (d % 128 == 0, I % 128 == 0); ws:
  * moe_workspace_size(MOE_OP_GROUPED_FFN_FP8, M, E, 1, 1, d, I) bytes (the

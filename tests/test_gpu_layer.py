@@ -271,11 +271,13 @@ def _carry_dw(a, da, b, db, offsets):
     return out
 
 
-def test_layer_full_size_every_element_qwen3():
+@pytest.mark.parametrize("name", ["qwen3", "skew"])
+def test_layer_full_size_every_element(name):
     """The benchmarked launch sequence on the whole Qwen3-shaped workload
     (T=8192, d=2048, E=128, K=8, I=768, R=8), forward and backward, compared
     element by element on every output with the oracle's layer run on the same
-    seeded inputs.
+    seeded inputs; and on its Zipf-skewed routing (hot experts of thousands of
+    rows, empty experts whose weight gradients are zero).
 
     Stated bounds where the compared value is the first rounding of a sum of
     exact inputs: routing, permutation and expert-parallel indices bit-exact;
@@ -293,7 +295,7 @@ def test_layer_full_size_every_element_qwen3():
     ulp(dG) |Wg|^T + ulp(dU) |Wu|^T; dx sum_j (ulp(dxp_j) + dxp_j's own bound);
     dW_gate / dW_up |X|^T ulp(dG) / |X|^T ulp(dU); dW_down
     |H|^T ulp(dY) + ulp(H)^T |dY|. All on top of 2e-2 RMS."""
-    cfg = W.CONFIGS["qwen3"]
+    cfg = W.CONFIGS[name]
     T, K, d, I = cfg.T, cfg.K, cfg.d, cfg.I
     inp = W.make_inputs(cfg, with_backward=True)
     layer = L.layer_from_config(cfg, inp, dev())

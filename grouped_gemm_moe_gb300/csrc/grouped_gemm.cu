@@ -92,8 +92,9 @@ struct Params {
   int d;
   int I;
   int n_tiles;             // tiles along N
-  int m_tiles;             // weight gradients: tiles along M (d/128 or I/128)
-  int k_blocks;            // forward / input gradients: K / 64
+  int m_tiles;             // weight gradients: 256-row tile pairs along M (dW rows d or I)
+  int k_blocks;            // forward / input gradients: k-blocks of K (64 bf16 or 128 E4M3)
+  int nt_half;             // gate/up weight gradients: n-tiles of each of dWg and dWu
   __nv_bfloat16* out;      // h, y, dgu or dxp
   __nv_bfloat16* out2;     // gu (forward, may be null)
   const __nv_bfloat16* aux;  // gu (BWD_DH)
@@ -102,6 +103,7 @@ struct Params {
   int ld_out;              // row length of `out` in elements
   int* status;             // workspace status word
   PadJob pad[2];           // BWD_DH: the weight gradients' pads of X and H (a == null: none)
+  int kb_half;             // BWD_DX: k-blocks of the dG half of K (then as many of the dU half)
   int tag_mode;            // kTagNone, kTagWrite (data part's dH) or kTagCheck (weight part)
   uint32_t tag[kTagWords]; // the backward's scratch tag: magic, M, E, d, I, offsets (low 32 bits)
   uint8_t* hq;             // MXFP8 gate/up: E4M3 of H for the down projection (null: not fused)
@@ -224,6 +226,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -282,6 +292,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+// The same over a 3-D map [E][rows][cols] (x = column, y = row, z = expert):
+// rows and columns past the expert's extent read the fill value (zero).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
       : "memory");
 }
 // D[tmem of both CTAs] (+)= A[smem of both] * B[smem of both]^T, M = 256.
@@ -381,15 +401,17 @@ __device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t addr) {
 // overflows and the quotient is 0, the limit of silu.
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
 
-__device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const float (&v)[16]) {
+// nvalid: the row's columns left from dst (a multiple of 8); 8-column chunks
+// past it are not written.
+__device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const float (&v)[16], int nvalid) {
   uint4 a, b;
   a.x = pack_bf16(v[0], v[1]);   a.y = pack_bf16(v[2], v[3]);
   a.z = pack_bf16(v[4], v[5]);   a.w = pack_bf16(v[6], v[7]);
   b.x = pack_bf16(v[8], v[9]);   b.y = pack_bf16(v[10], v[11]);
   b.z = pack_bf16(v[12], v[13]); b.w = pack_bf16(v[14], v[15]);
   uint4* p = reinterpret_cast<uint4*>(dst);
-  p[0] = a;
-  p[1] = b;
+  if (nvalid > 0) p[0] = a;
+  if (nvalid > 8) p[1] = b;
 }
 
 // Debug builds: the expert offsets the tile scheduler decodes must start at 0,
@@ -455,29 +477,35 @@ __device__ __forceinline__ PTile decode_pair(int t, int rank, const Params& p, c
 // for the gate/up GEMM), counted on the leader's full barrier.
 template <int KIND, int BN>
 __device__ __forceinline__ void issue_pair(const PTile& tl, int kb, uint32_t rank, const Params& p,
-                                           const CUtensorMap* tmA, const CUtensorMap* tmB0,
-                                           const CUtensorMap* tmB1, uint32_t sa, uint32_t sb,
-                                           uint32_t fb) {
+                                           const CUtensorMap* tmA, const CUtensorMap* tmA2,
+                                           const CUtensorMap* tmB0, const CUtensorMap* tmB1,
+                                           uint32_t sa, uint32_t sb, uint32_t fb) {
   constexpr uint32_t MN_ATOM = 64 * 128;
   constexpr int HB = BN / 2;
+  // The weights are 3-D maps [E][rows][cols]: a box past the expert's rows or
+  // columns reads zeros, so K and N tails need no masking.
+  if constexpr (KIND == BWD_DX) {
+    // K = [dG | dU]: the dG half's k-blocks, then the dU half's, each from its
+    // own half map (so no k-block mixes the two halves) with Wg or Wu
+    const bool up = kb >= p.kb_half;
+    const int kx = (up ? kb - p.kb_half : kb) * BK;
+    tma_load_2d_pair(sa, up ? tmA2 : tmA, fb, kx, tl.row0);
+    tma_load_3d_pair(sb, up ? tmB1 : tmB0, fb, kx, tl.n0 + static_cast<int>(rank) * HB, tl.e);
+    return;
+  }
   tma_load_2d_pair(sa, tmA, fb, kb * BK, tl.row0);
   if constexpr (KIND == FWD_GATEUP) {
     const CUtensorMap* m = rank ? tmB1 : tmB0;
 #pragma unroll
     for (int i = 0; i < HB / 64; ++i)
-      tma_load_2d_pair(sb + i * MN_ATOM, m, fb, tl.n0 + 64 * i, tl.e * p.d + kb * BK);
+      tma_load_3d_pair(sb + i * MN_ATOM, m, fb, tl.n0 + 64 * i, kb * BK, tl.e);
   } else if constexpr (KIND == FWD_DOWN) {
 #pragma unroll
     for (int i = 0; i < HB / 64; ++i)
-      tma_load_2d_pair(sb + i * MN_ATOM, tmB0, fb, tl.n0 + static_cast<int>(rank) * HB + 64 * i,
-                       tl.e * p.I + kb * BK);
-  } else if constexpr (KIND == BWD_DH) {
-    tma_load_2d_pair(sb, tmB0, fb, kb * BK, tl.e * p.I + tl.n0 + static_cast<int>(rank) * HB);
-  } else {  // BWD_DX
-    const int kx = kb * BK;
-    const int y = tl.e * p.d + tl.n0 + static_cast<int>(rank) * HB;
-    if (kx < p.I) tma_load_2d_pair(sb, tmB0, fb, kx, y);
-    else tma_load_2d_pair(sb, tmB1, fb, kx - p.I, y);
+      tma_load_3d_pair(sb + i * MN_ATOM, tmB0, fb, tl.n0 + static_cast<int>(rank) * HB + 64 * i,
+                       kb * BK, tl.e);
+  } else {  // BWD_DH
+    tma_load_3d_pair(sb, tmB0, fb, kb * BK, tl.n0 + static_cast<int>(rank) * HB, tl.e);
   }
 }
 
@@ -532,14 +560,14 @@ __device__ __forceinline__ void stage_row32(uint8_t* box, int lane, int j0, cons
   }
 }
 
-__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float (&v)[32]) {
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float (&v)[32], int nvalid) {
   uint4* p = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     float f[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) f[i] = v[8 * jj + i];
-    p[jj] = pack8(f);
+    if (8 * jj < nvalid) p[jj] = pack8(f);
   }
 }
 
@@ -583,6 +611,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB1,
                          const __grid_constant__ CUtensorMap tmC0,
                          const __grid_constant__ CUtensorMap tmC1,
+                         const __grid_constant__ CUtensorMap tmC2,
                          const __grid_constant__ CUtensorMap tmS, const Params p) {
   static_assert(KIND == FWD_GATEUP || KIND == FWD_DOWN || KIND == BWD_DH || KIND == BWD_DX,
                 "pair kernel: forward and input-gradient kinds");
@@ -643,8 +672,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB1)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC1)) : "memory");
-    if constexpr (FP8)
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmS)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC2)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmS)) : "memory");
   }
   if (warp == 1) {   // one warp in each CTA of the pair allocates collectively
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -728,7 +757,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                                (tl.e * (nq / 128) + nrow / 128 + static_cast<int>(j)) * p.k_blocks +
                                    kb);
           } else {
-            issue_pair<KIND, BN>(tl, kb, rank, p, &tmA, &tmB0, &tmB1, sa, sa + A_BYTES,
+            issue_pair<KIND, BN>(tl, kb, rank, p, &tmA, &tmC2, &tmB0, &tmB1, sa, sa + A_BYTES,
                                  map_to_rank(fb_local, 0));
           }
           issued[stage] += 1;
@@ -852,8 +881,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           if (lane == 0) {
             bulk_wait_read_all();          // earlier dG/dU stores from these boxes are done
             mbar_expect_tx(ab, 8192);
-            tma_load_2d(aux_addr, &tmC0, ab, tl.n0 + c0, growq);
-            tma_load_2d(aux_addr + 4096, &tmC0, ab, p.I + tl.n0 + c0, growq);
+            tma_load_2d(aux_addr, &tmC0, ab, tl.n0 + c0, growq);          // G half of gu
+            tma_load_2d(aux_addr + 4096, &tmS, ab, tl.n0 + c0, growq);    // U half of gu
           }
           aux_pending = true;
         };
@@ -862,8 +891,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         tc_fence_after();
         const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
         bool ok = true;
-        // with I an odd multiple of 128 the last n-tile's upper half lies past
-        // column I: its accumulator columns are neither read nor stored
+        // when I % 256 != 0 the last n-tile's columns past I are neither read nor stored
         const int cend = min(BN, p.I - tl.n0);
         for (int c0 = 0; c0 < cend; c0 += 64) {
           if (c0) request(c0);
@@ -903,15 +931,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
               }
             } else if (valid) {
               __nv_bfloat16* orow = p.out + grow * (2 * p.I);
-              store16_bf16(orow + tl.n0 + c0 + c, dg);
-              store16_bf16(orow + p.I + tl.n0 + c0 + c, du);
+              const int left = p.I - (tl.n0 + c0 + c);
+              store16_bf16(orow + tl.n0 + c0 + c, dg, left);
+              store16_bf16(orow + p.I + tl.n0 + c0 + c, du, left);
             }
           }
           fence_proxy_async();
           __syncwarp();
           if (full && lane == 0) {
-            tma_store_2d(&tmC1, aux_addr, tl.n0 + c0, growq);
-            tma_store_2d(&tmC1, aux_addr + 4096, p.I + tl.n0 + c0, growq);
+            tma_store_2d(&tmC1, aux_addr, tl.n0 + c0, growq);          // dG half of dgu
+            tma_store_2d(&tmC2, aux_addr + 4096, tl.n0 + c0, growq);   // dU half of dgu
             bulk_commit();
           }
         }
@@ -935,7 +964,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           const int nst = nstreams;
           const int rr = q * 32 + lane;                                // row in the CTA's m-tile
           const long long qtile = 2LL * tl.mg + static_cast<long long>(rank);
-          for (int c64 = 0; c64 < HALF; c64 += 64) {
+          const int cend = min(HALF, p.I - tl.n0);   // columns of the tile within I
+          for (int c64 = 0; c64 < cend; c64 += 64) {
             if (!full) {   // a slice that crosses the expert's end: row-wise stores
               for (int sub = 0; sub < 64; sub += 32) {
                 float g[32], u[32], h[32];
@@ -945,10 +975,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 if (valid) {
 #pragma unroll
                   for (int i = 0; i < 32; ++i) h[i] = silu_f(g[i]) * u[i];
-                  store32_bf16(p.out + grow * p.I + tl.n0 + c64 + sub, h);
+                  const int left = p.I - (tl.n0 + c64 + sub);
+                  store32_bf16(p.out + grow * p.I + tl.n0 + c64 + sub, h, left);
                   if (p.out2) {
-                    store32_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c64 + sub, g);
-                    store32_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c64 + sub, u);
+                    store32_bf16(p.out2 + grow * (2 * p.I) + tl.n0 + c64 + sub, g, left);
+                    store32_bf16(p.out2 + grow * (2 * p.I) + p.I + tl.n0 + c64 + sub, u, left);
                   }
                   if (fuse_q) {
                     uint4 qb[2];
@@ -996,15 +1027,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
               fence_proxy_async();
               __syncwarp();
               if (lane == 0) {
-                if (sidx == 0) tma_store_2d(&tmC0, smem_u32(st), tl.n0 + c64, growq);
-                else tma_store_2d(&tmC1, smem_u32(st), (sidx == 1 ? 0 : p.I) + tl.n0 + c64, growq);
+                // H, then the G and U halves of gu (each its own half map)
+                tma_store_2d(sidx == 0 ? &tmC0 : (sidx == 1 ? &tmC1 : &tmC2), smem_u32(st),
+                             tl.n0 + c64, growq);
                 bulk_commit();
               }
               buf ^= 1;
             }
           }
         } else {  // FWD_DOWN, BWD_DX: one bf16 output, two staging boxes in turn
-          for (int c64 = 0; c64 < BN; c64 += 64) {
+          const int cend = min(BN, p.ld_out - tl.n0);   // columns of the tile within the output
+          for (int c64 = 0; c64 < cend; c64 += 64) {
             uint8_t* st = epi + ew * 8192 + buf * 4096;
             if (full) {
               if (lane == 0) bulk_wait_read_1();   // the store that used this box is done
@@ -1015,7 +1048,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
               tmem_ld32(tacc + c64 + sub, v);
               tmem_wait_ld();
               if (full) stage_row32(st, lane, sub >> 3, v);
-              else if (valid) store32_bf16(p.out + grow * p.ld_out + tl.n0 + c64 + sub, v);
+              else if (valid)
+                store32_bf16(p.out + grow * p.ld_out + tl.n0 + c64 + sub, v,
+                             p.ld_out - (tl.n0 + c64 + sub));
             }
             if (full) {
               fence_proxy_async();
@@ -1084,15 +1119,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 // kernel about a third of its time.)
 //
 // The epilogue streams fp32 rows out through two alternating [32 x 32] staging
-// blocks per warp and bulk tensor stores. When the M extent is an odd multiple
-// of 128, the follower's rows of the last m-tile lie past it: its A boxes read
-// the fill value and it stores nothing.
+// blocks per warp and bulk tensor stores into 3-D maps of dW ([E][rows][cols]).
+// Rows past the M extent (d or I) and columns past the N extent read the fill
+// value in A and B; a 32 x 32 block that starts past either is not stored and
+// one that ends past it is clipped by the store.
 struct WTile {
   int e;
   int row0;   // expert's first packed row (the K start)
   int rows;   // expert's rows (K)
   int m0;     // this CTA's first dW row
   int n0;     // the tile's first dW column (this CTA loads n0 + 128*rank ..)
+  int part;   // gate/up: 0 for dWg, 1 for dWu (each its own n-tiles and half of [dG | dU])
   int nkb;
 };
 
@@ -1106,7 +1143,8 @@ __device__ __forceinline__ WTile decode_wgrad_pair(int t, int rank, const Params
   const int mt = rem / p.n_tiles;
   const int nt = rem - mt * p.n_tiles;
   tl.m0 = mt * 2 * BM + rank * BM;
-  tl.n0 = nt * 256;
+  tl.part = (KIND == WGRAD_GU && nt >= p.nt_half) ? 1 : 0;
+  tl.n0 = (nt - tl.part * p.nt_half) * 256;
   tl.row0 = s_off[tl.e];
   tl.rows = s_off[tl.e + 1] - tl.row0;
   tl.nkb = (tl.rows + BK - 1) / BK;
@@ -1125,6 +1163,7 @@ template <int KIND, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
                                const __grid_constant__ CUtensorMap tmB,
+                               const __grid_constant__ CUtensorMap tmB2,
                                const __grid_constant__ CUtensorMap tmC0,
                                const __grid_constant__ CUtensorMap tmC1,
                                const __grid_constant__ CUtensorMap tmA16,
@@ -1170,6 +1209,7 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB2)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC0)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC1)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA16)) : "memory");
@@ -1244,8 +1284,9 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
               tma_load_2d_pair(da + nfull * 2048, &tmP, fr, x, tl.e * 16);
             }
           }
-          tma_load_2d_pair(sa + A_BYTES, &tmB, fr, nb, ky);
-          tma_load_2d_pair(sa + A_BYTES + MN_ATOM, &tmB, fr, nb + 64, ky);
+          const CUtensorMap* mb = tl.part ? &tmB2 : &tmB;   // dG or dU half (gate/up)
+          tma_load_2d_pair(sa + A_BYTES, mb, fr, nb, ky);
+          tma_load_2d_pair(sa + A_BYTES + MN_ATOM, mb, fr, nb + 64, ky);
           fpar ^= 1u << stage;
           fused |= 1u << stage;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -1326,8 +1367,8 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
       }
-      const bool in_range = tl.m0 < mdim;   // false only for the follower past an odd M extent
-      const int ncols = (KIND == WGRAD_GU) ? 2 * p.I : p.d;
+      const bool in_range = tl.m0 < mdim;   // false only for the follower past the M extent
+      const int ncols = (KIND == WGRAD_GU) ? p.I : p.d;   // columns of this tile's dW
       const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
       const int mrow = tl.m0 + q * 32;
       for (int c = 0; c < BN; c += 32) {
@@ -1339,7 +1380,8 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        if (!in_range || tl.n0 + c >= ncols) continue;   // past the M or N extent: not stored
+        // past the M or N extent: not stored (a slice that ends past it is clipped by the store)
+        if (!in_range || mrow >= mdim || tl.n0 + c >= ncols) continue;
         uint8_t* stg = epi + ew * 8192 + buf * 4096;
         if (lane == 0) bulk_wait_read_1();   // the store that last used this block has read it
         __syncwarp();
@@ -1351,13 +1393,8 @@ grouped_gemm_pair_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          const int n = tl.n0 + c;
-          if constexpr (KIND == WGRAD_GU) {
-            if (n < p.I) tma_store_2d(&tmC0, smem_u32(stg), n, tl.e * p.d + mrow);
-            else tma_store_2d(&tmC1, smem_u32(stg), n - p.I, tl.e * p.d + mrow);
-          } else {
-            tma_store_2d(&tmC0, smem_u32(stg), n, tl.e * p.I + mrow);
-          }
+          // 3-D maps [E][rows][cols] of dW: rows and columns past the expert's are clipped
+          tma_store_3d(tl.part ? &tmC1 : &tmC0, smem_u32(stg), tl.n0 + c, mrow, tl.e);
           bulk_commit();
         }
         buf ^= 1;
@@ -1419,14 +1456,42 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D tensor map over a row-major [outer, inner] array of bf16 (or fp32), 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, bool fp32 = false) {
+              uint32_t box_outer, bool fp32 = false, uint64_t row_elems = 0) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * (fp32 ? 4 : 2)};
+  cuuint64_t strides[1] = {(row_elems ? row_elems : inner) * (fp32 ? 4 : 2)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
   return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One half of a row-major [rows, 2 * half] bf16 array ([G | U] and [dG | dU]):
+// columns [col0, col0 + half) of every row as a [rows, half] tensor, so a box
+// past column half reads zeros and a store past it is clipped (the other half
+// is never touched).
+bool make_half_map(CUtensorMap* m, const void* base, uint64_t half, uint64_t rows, uint64_t col0,
+                   uint32_t box_inner, uint32_t box_outer) {
+  return make_map(m, static_cast<const uint16_t*>(base) + col0, half, rows, box_inner, box_outer,
+                  false, 2 * half);
+}
+
+// 3-D tensor map over a row-major [E, rows, cols] array of bf16 (or fp32), 128-byte
+// swizzle: boxes of box_cols x box_rows x 1 at (column, row, expert); rows and
+// columns past an expert's extent read zeros and are clipped on stores.
+bool make_map3(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t E,
+               uint32_t box_cols, uint32_t box_rows, bool fp32 = false) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t es_b = fp32 ? 4 : 2;
+  cuuint64_t dims[3] = {cols, rows, E};
+  cuuint64_t strides[2] = {cols * es_b, cols * rows * es_b};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
             const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1519,8 +1584,9 @@ int launch_cluster2(void (*kern)(KArgs...), size_t sm, size_t sm_max, int* confi
 // shared-memory opt-in sized for the largest expert count it is used with.
 template <int KIND, int BN, int STAGES, bool FP8 = false>
 int launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                const CUtensorMap& c0, const CUtensorMap& c1, const CUtensorMap& s,
-                const Params& p, long long tiles_upper, int e_max, cudaStream_t st) {
+                const CUtensorMap& c0, const CUtensorMap& c1, const CUtensorMap& c2,
+                const CUtensorMap& s, const Params& p, long long tiles_upper, int e_max,
+                cudaStream_t st) {
   static thread_local int configured = -1;
   static thread_local int max_clusters = 0;
   static const char* kNames[] = {"gemm_gate_up", "gemm_down", "gemm_dh", "gemm_dx", "", ""};
@@ -1529,7 +1595,7 @@ int launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& 
                          pair_smem_bytes<KIND, BN, STAGES, FP8>(p.E),
                          pair_smem_bytes<KIND, BN, STAGES, FP8>(e_max), &configured,
                          &max_clusters, tiles_upper, FP8 ? kNamesFp8[KIND] : kNames[KIND], st, a,
-                         b0, b1, c0, c1, s, p);
+                         b0, b1, c0, c1, c2, s, p);
 }
 
 // Weight gradients on CTA pairs: six 32 KB stages while the expert table fits
@@ -1544,9 +1610,10 @@ static_assert(pair_wgrad_smem_bytes<6>(kWgradPair6MaxE) <= 232448, "pair wgrad s
 static_assert(pair_wgrad_smem_bytes<5>(1024) <= 232448, "pair wgrad smem (5 stages)");
 
 template <int KIND, int STAGES>
-int launch_pair_wgrad_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c0,
-                             const CUtensorMap& c1, const CUtensorMap& a16, const CUtensorMap& pad,
-                             const Params& p, long long tiles, cudaStream_t st) {
+int launch_pair_wgrad_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
+                             const CUtensorMap& c0, const CUtensorMap& c1, const CUtensorMap& a16,
+                             const CUtensorMap& pad, const Params& p, long long tiles,
+                             cudaStream_t st) {
   static thread_local int configured = -1;
   static thread_local int max_clusters = 0;
   return launch_cluster2(grouped_gemm_pair_wgrad_kernel<KIND, STAGES>,
@@ -1554,17 +1621,19 @@ int launch_pair_wgrad_stages(const CUtensorMap& a, const CUtensorMap& b, const C
                          pair_wgrad_smem_bytes<STAGES>(STAGES == 6 ? kWgradPair6MaxE : 1024),
                          &configured, &max_clusters, tiles,
                          KIND == WGRAD_GU ? "gemm_wgrad_gate_up" : "gemm_wgrad_down", st, a, b,
-                         c0, c1, a16, pad, p);
+                         b2, c0, c1, a16, pad, p);
 }
 
-// a16: A again with 16-row boxes; pad: the zero-padded straddling steps of A.
+// b, b2: B (gate/up: the dG and dU halves); c0, c1: the dW maps (gate/up: dWg
+// and dWu); a16: A again with 16-row boxes; pad: the zero-padded straddling
+// steps of A.
 template <int KIND>
-int launch_pair_wgrad(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c0,
-                      const CUtensorMap& c1, const CUtensorMap& a16, const CUtensorMap& pad,
-                      const Params& p, long long tiles, cudaStream_t st) {
+int launch_pair_wgrad(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
+                      const CUtensorMap& c0, const CUtensorMap& c1, const CUtensorMap& a16,
+                      const CUtensorMap& pad, const Params& p, long long tiles, cudaStream_t st) {
   if (p.E <= kWgradPair6MaxE)
-    return launch_pair_wgrad_stages<KIND, 6>(a, b, c0, c1, a16, pad, p, tiles, st);
-  return launch_pair_wgrad_stages<KIND, 5>(a, b, c0, c1, a16, pad, p, tiles, st);
+    return launch_pair_wgrad_stages<KIND, 6>(a, b, b2, c0, c1, a16, pad, p, tiles, st);
+  return launch_pair_wgrad_stages<KIND, 5>(a, b, b2, c0, c1, a16, pad, p, tiles, st);
 }
 
 constexpr long long kSmemOptIn = 232448;   // shared memory a CTA may opt into
@@ -1594,8 +1663,9 @@ constexpr int pair_stages_deep() {
 
 template <int KIND, int BN, bool FP8 = false>
 int launch_pair_depth(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                      const CUtensorMap& c0, const CUtensorMap& c1, const CUtensorMap& s,
-                      const Params& p, long long tiles_upper, cudaStream_t st) {
+                      const CUtensorMap& c0, const CUtensorMap& c1, const CUtensorMap& c2,
+                      const CUtensorMap& s, const Params& p, long long tiles_upper,
+                      cudaStream_t st) {
   constexpr int kDeep = pair_stages_deep<KIND, BN>();
   constexpr int kShallow = pair_stages<KIND, BN>();
   constexpr int kDeepMaxE = pair_max_e<KIND, BN, kDeep, FP8>();
@@ -1603,25 +1673,31 @@ int launch_pair_depth(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
                 "shallow pair ring must fit 1024 experts");
   if constexpr (kDeepMaxE >= 1) {
     if (p.E <= kDeepMaxE)
-      return launch_pair<KIND, BN, kDeep, FP8>(a, b0, b1, c0, c1, s, p, tiles_upper,
+      return launch_pair<KIND, BN, kDeep, FP8>(a, b0, b1, c0, c1, c2, s, p, tiles_upper,
                                                kDeepMaxE < 1024 ? kDeepMaxE : 1024, st);
   }
-  return launch_pair<KIND, BN, kShallow, FP8>(a, b0, b1, c0, c1, s, p, tiles_upper, 1024, st);
+  return launch_pair<KIND, BN, kShallow, FP8>(a, b0, b1, c0, c1, c2, s, p, tiles_upper, 1024, st);
 }
 
+// The bf16 kinds: c0..c2 the epilogue's maps (gate/up: H and the G, U halves of
+// [G | U]; dH: the G half of [G | U], then the dG and dU halves of [dG | dU]),
+// s the U half of [G | U] for dH (another map otherwise, not read).
 template <int KIND>
 int launch_pair_bn(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                   const CUtensorMap& c0, const CUtensorMap& c1, const Params& p,
-                   long long tiles_upper, cudaStream_t st) {
-  // the scale-atom map is read by the MXFP8 instantiation only
+                   const CUtensorMap& c0, const CUtensorMap& c1, const CUtensorMap& c2,
+                   const CUtensorMap& s, const Params& p, long long tiles_upper, cudaStream_t st) {
 #if MOE_PAIR_BN_MAX >= 256
-  if (bn == 256) return launch_pair_depth<KIND, 256>(a, b0, b1, c0, c1, a, p, tiles_upper, st);
+  if (bn == 256) return launch_pair_depth<KIND, 256>(a, b0, b1, c0, c1, c2, s, p, tiles_upper, st);
 #endif
-  return launch_pair_depth<KIND, 128>(a, b0, b1, c0, c1, a, p, tiles_upper, st);
+  return launch_pair_depth<KIND, 128>(a, b0, b1, c0, c1, c2, s, p, tiles_upper, st);
 }
 
-// The N width a pair tile uses for an output of n columns (n % 128 == 0).
-inline int pair_bn(int n) { return (n % 256 == 0 && MOE_PAIR_BN_MAX >= 256) ? 256 : 128; }
+// The N width a pair tile uses for an output of n columns: 256 unless 128-wide
+// tiles leave fewer columns idle (n % 256 in 1 .. 128).
+inline int pair_bn(int n) {
+  const int r = n % 256;
+  return ((r == 0 || r > 128) && MOE_PAIR_BN_MAX >= 256) ? 256 : 128;
+}
 
 
 }  // namespace gemm
@@ -1659,7 +1735,7 @@ size_t ffn_fp8_scratch(long long M, int E, int d, int I) { return ffn_fp8_layout
 namespace {
 
 bool ffn_shape_ok(int E, int M, int d, int I) {
-  return E >= 1 && E <= 1024 && M >= 0 && d > 0 && I > 0 && d % 128 == 0 && I % 128 == 0;
+  return E >= 1 && E <= 1024 && M >= 0 && d > 0 && I > 0 && d % 8 == 0 && I % 8 == 0;
 }
 
 }  // namespace
@@ -1670,10 +1746,7 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
                                void* ws, size_t ws_bytes, void* stream) {
   using namespace moe;
   using namespace moe::gemm;
-  if (!ffn_shape_ok(E, M, d, I)) {
-    if (E >= 1 && M >= 0 && d > 0 && I > 0 && d % 8 == 0 && I % 8 == 0) return MOE_ERR_UNSUPPORTED;
-    return MOE_ERR_INVALID_ARG;
-  }
+  if (!ffn_shape_ok(E, M, d, I)) return MOE_ERR_INVALID_ARG;
   if (M == 0) return MOE_OK;
   if (!xp || !offsets || !w_gate || !w_up || !w_down || !y || !h) return MOE_ERR_INVALID_ARG;
   if (!aligned16(xp) || !aligned16(offsets) || !aligned16(w_gate) || !aligned16(w_up) ||
@@ -1696,33 +1769,40 @@ extern "C" int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E
   p.tag[4] = static_cast<uint32_t>(I);
   p.tag[5] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(offsets));
   const long long mt_upper = (M + BM - 1) / BM + E;
-  CUtensorMap ta, tb0, tb1, tc0, tc1;
-  // gate/up projection with the SwiGLU epilogue (H and [G|U] leave through bulk stores)
-  if (!make_map(&ta, xp, d, M, 64, BM) || !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, 64) ||
-      !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, 64) ||
-      !make_map(&tc0, h, I, M, 64, 32) ||
-      !make_map(&tc1, gu ? static_cast<const void*>(gu) : static_cast<const void*>(h),
-                gu ? 2 * static_cast<uint64_t>(I) : I, M, 64, 32))
+  CUtensorMap ta, tb0, tb1, tc0, tc1, tc2;
+  // gate/up projection with the SwiGLU epilogue (H and [G|U] leave through bulk
+  // stores). The weights are 3-D maps [E][d][I]: a K or N tail past d or I reads
+  // zeros, and the stores clip at column I of H and of each half of [G|U].
+  if (!make_map(&ta, xp, d, M, 64, BM) || !make_map3(&tb0, w_gate, I, d, E, 64, 64) ||
+      !make_map3(&tb1, w_up, I, d, E, 64, 64) || !make_map(&tc0, h, I, M, 64, 32))
     return MOE_ERR_CUDA;
-  const int bn_gu = (MOE_PAIR_BN_MAX >= 256) ? 256 : 128;   // half gate, half up columns
-  p.n_tiles = I / (bn_gu / 2);
-  p.k_blocks = d / BK;
+  if (gu) {
+    if (!make_half_map(&tc1, gu, I, M, 0, 64, 32) || !make_half_map(&tc2, gu, I, M, I, 64, 32))
+      return MOE_ERR_CUDA;
+  } else {
+    tc1 = tc2 = tc0;   // not stored through
+  }
+  // 128 gate + 128 up columns per tile, or 64 + 64 when that leaves fewer idle
+  const int bn_gu = (I % 128 == 0 || I % 128 > 64) && MOE_PAIR_BN_MAX >= 256 ? 256 : 128;
+  p.n_tiles = (I + bn_gu / 2 - 1) / (bn_gu / 2);
+  p.k_blocks = (d + BK - 1) / BK;
   p.out = reinterpret_cast<__nv_bfloat16*>(h);
   p.out2 = reinterpret_cast<__nv_bfloat16*>(gu);
   p.ld_out = I;
-  int rc = launch_pair_bn<FWD_GATEUP>(bn_gu, ta, tb0, tb1, tc0, tc1, p, mt_upper * p.n_tiles, st);
+  int rc = launch_pair_bn<FWD_GATEUP>(bn_gu, ta, tb0, tb1, tc0, tc1, tc2, tc0, p,
+                                      mt_upper * p.n_tiles, st);
   if (rc) return rc;
-  // down projection
+  // down projection (Wd as [E][I][d])
   const int bn = pair_bn(d);
-  if (!make_map(&ta, h, I, M, 64, BM) || !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, 64) ||
+  if (!make_map(&ta, h, I, M, 64, BM) || !make_map3(&tb0, w_down, d, I, E, 64, 64) ||
       !make_map(&tc0, y, d, M, 64, 32))
     return MOE_ERR_CUDA;
-  p.n_tiles = d / bn;
-  p.k_blocks = I / BK;
+  p.n_tiles = (d + bn - 1) / bn;
+  p.k_blocks = (I + BK - 1) / BK;
   p.out = reinterpret_cast<__nv_bfloat16*>(y);
   p.out2 = nullptr;
   p.ld_out = d;
-  return launch_pair_bn<FWD_DOWN>(bn, ta, tb0, tb0, tc0, tc0, p, mt_upper * p.n_tiles, st);
+  return launch_pair_bn<FWD_DOWN>(bn, ta, tb0, tb0, tc0, tc0, tc0, tc0, p, mt_upper * p.n_tiles, st);
 }
 
 namespace {
@@ -1741,10 +1821,7 @@ int ffn_backward_parts(int parts, const moe_bf16* dy, const moe_bf16* xp, const 
   using namespace moe;
   using namespace moe::gemm;
   const bool data = parts & kBwdData, weights = parts & kBwdWeights;
-  if (!ffn_shape_ok(E, M, d, I) || d % 128 != 0) {
-    if (E >= 1 && M >= 0 && d > 0 && I > 0 && d % 8 == 0 && I % 8 == 0) return MOE_ERR_UNSUPPORTED;
-    return MOE_ERR_INVALID_ARG;
-  }
+  if (!ffn_shape_ok(E, M, d, I)) return MOE_ERR_INVALID_ARG;
   if (!offsets) return MOE_ERR_INVALID_ARG;
   if (data && (!w_gate || !w_up || !w_down)) return MOE_ERR_INVALID_ARG;
   if (weights && (!dw_gate || !dw_up || !dw_down)) return MOE_ERR_INVALID_ARG;
@@ -1786,21 +1863,21 @@ int ffn_backward_parts(int parts, const moe_bf16* dy, const moe_bf16* xp, const 
   p.tag[4] = static_cast<uint32_t>(I);
   p.tag[5] = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(offsets));
   const long long mt_upper = (M + BM - 1) / BM + E;
-  CUtensorMap ta, tb0, tb1, tc0, tc1;
+  CUtensorMap ta, tb0, tb1, tc0, tc1, tc2, ts;
   int rc = MOE_OK;
   if (data) {
     // dH = dY Wd^T with the SwiGLU backward epilogue -> [dG | dU], on 256-wide
-    // tiles also when I is an odd multiple of 128 (the last tile's upper half
-    // reads the next expert's rows of Wd, or the TMA fill value, and stores
-    // nothing): 128-wide tiles fetch 1.5x the operand bytes per MMA flop.
+    // tiles also when I % 256 != 0 (the last tile's columns past I read zeros
+    // from the 3-D map of Wd and store nothing): 128-wide tiles fetch 1.5x the
+    // operand bytes per MMA flop. G and U come in, and dG and dU leave, through
+    // half maps of [G | U] and [dG | dU].
     const int bn_h = MOE_PAIR_BN_MAX >= 256 ? 256 : 128;
-    if (!make_map(&ta, dy, d, M, 64, BM) ||
-        !make_map(&tb0, w_down, d, static_cast<uint64_t>(E) * I, 64, bn_h / 2) ||
-        !make_map(&tc0, gu, 2 * static_cast<uint64_t>(I), M, 64, 32) ||
-        !make_map(&tc1, dgu, 2 * static_cast<uint64_t>(I), M, 64, 32))
+    if (!make_map(&ta, dy, d, M, 64, BM) || !make_map3(&tb0, w_down, d, I, E, 64, bn_h / 2) ||
+        !make_half_map(&tc0, gu, I, M, 0, 64, 32) || !make_half_map(&ts, gu, I, M, I, 64, 32) ||
+        !make_half_map(&tc1, dgu, I, M, 0, 64, 32) || !make_half_map(&tc2, dgu, I, M, I, 64, 32))
       return MOE_ERR_CUDA;
     p.n_tiles = (I + bn_h - 1) / bn_h;
-    p.k_blocks = d / BK;
+    p.k_blocks = (d + BK - 1) / BK;
     p.out = dgu;
     p.aux = reinterpret_cast<const __nv_bfloat16*>(gu);
     p.ld_out = 2 * I;
@@ -1808,54 +1885,60 @@ int ffn_backward_parts(int parts, const moe_bf16* dy, const moe_bf16* xp, const 
     p.pad[0] = PadJob{reinterpret_cast<const __nv_bfloat16*>(xp), pad_x, d};
     p.pad[1] = PadJob{reinterpret_cast<const __nv_bfloat16*>(h), pad_h, I};
     p.tag_mode = kTagWrite;
-    rc = launch_pair_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc1, p, mt_upper * p.n_tiles, st);
+    rc = launch_pair_bn<BWD_DH>(bn_h, ta, tb0, tb0, tc0, tc1, tc2, ts, p, mt_upper * p.n_tiles, st);
     p.tag_mode = kTagNone;
     if (rc) return rc;
-    // dX = dG Wg^T + dU Wu^T
+    // dX = dG Wg^T + dU Wu^T: K runs over the dG half's k-blocks (with Wg), then
+    // the dU half's (with Wu), each A from its own half map (tc2: the dU half) so
+    // that a K tail reads zeros instead of the other half
     const int bn_x = pair_bn(d);
-    if (!make_map(&ta, dgu, 2 * static_cast<uint64_t>(I), M, 64, BM) ||
-        !make_map(&tb0, w_gate, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2) ||
-        !make_map(&tb1, w_up, I, static_cast<uint64_t>(E) * d, 64, bn_x / 2) ||
-        !make_map(&tc0, dxp, d, M, 64, 32))
+    if (!make_half_map(&ta, dgu, I, M, 0, 64, BM) || !make_half_map(&tc2, dgu, I, M, I, 64, BM) ||
+        !make_map3(&tb0, w_gate, I, d, E, 64, bn_x / 2) ||
+        !make_map3(&tb1, w_up, I, d, E, 64, bn_x / 2) || !make_map(&tc0, dxp, d, M, 64, 32))
       return MOE_ERR_CUDA;
-    p.n_tiles = d / bn_x;
-    p.k_blocks = 2 * I / BK;
+    p.n_tiles = (d + bn_x - 1) / bn_x;
+    p.kb_half = (I + BK - 1) / BK;
+    p.k_blocks = 2 * p.kb_half;
     p.out = reinterpret_cast<__nv_bfloat16*>(dxp);
     p.aux = nullptr;
     p.ld_out = d;
     p.pad[0] = p.pad[1] = PadJob{nullptr, nullptr, 0};
-    rc = launch_pair_bn<BWD_DX>(bn_x, ta, tb0, tb1, tc0, tc0, p, mt_upper * p.n_tiles, st);
+    rc = launch_pair_bn<BWD_DX>(bn_x, ta, tb0, tb1, tc0, tc0, tc2, tc0, p, mt_upper * p.n_tiles, st);
     if (rc) return rc;
   }
   if (!weights) return MOE_OK;
-  // [dWg | dWu] = X^T [dG | dU]
-  CUtensorMap ta16, tpad;
-  if (!make_map(&ta, xp, d, M, 64, 64) || !make_map(&tb0, dgu, 2 * static_cast<uint64_t>(I), M, 64, 64) ||
-      !make_map(&ta16, xp, d, M, 64, 16) || !make_map(&tpad, pad_x, d, static_cast<uint64_t>(E) * 16, 64, 16) ||
-      !make_map(&tc0, dw_gate, I, static_cast<uint64_t>(E) * d, 32, 32, true) ||
-      !make_map(&tc1, dw_up, I, static_cast<uint64_t>(E) * d, 32, 32, true))
+  // dWg = X^T dG and dWu = X^T dU on CTA pairs over 256 dW rows x 256 columns:
+  // the n-tiles of dWg, then those of dWu, B from the matching half map of
+  // [dG | dU]; the dW maps are 3-D [E][d][I], so rows past d and columns past I
+  // (the TMA fill value in the operands) are clipped from the stores.
+  CUtensorMap ta16, tpad, tb2;
+  if (!make_map(&ta, xp, d, M, 64, 64) || !make_half_map(&tb0, dgu, I, M, 0, 64, 64) ||
+      !make_half_map(&tb2, dgu, I, M, I, 64, 64) || !make_map(&ta16, xp, d, M, 64, 16) ||
+      !make_map(&tpad, pad_x, d, static_cast<uint64_t>(E) * 16, 64, 16) ||
+      !make_map3(&tc0, dw_gate, I, d, E, 32, 32, true) ||
+      !make_map3(&tc1, dw_up, I, d, E, 32, 32, true))
     return MOE_ERR_CUDA;
-  // CTA pairs over 256 dW rows x 256 columns (2I is a multiple of 256)
   p.m_tiles = (d + 2 * BM - 1) / (2 * BM);
-  p.n_tiles = 2 * I / 256;
+  p.nt_half = (I + 255) / 256;
+  p.n_tiles = 2 * p.nt_half;
   p.outf0 = dw_gate;
   p.outf1 = dw_up;
   p.out = nullptr;
   p.tag_mode = kTagCheck;
-  rc = launch_pair_wgrad<WGRAD_GU>(ta, tb0, tc0, tc1, ta16, tpad, p,
+  rc = launch_pair_wgrad<WGRAD_GU>(ta, tb0, tb2, tc0, tc1, ta16, tpad, p,
                                    static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
   if (rc) return rc;
-  // dWd = H^T dY on CTA pairs (when d is an odd multiple of 128 the last n-tile's
-  // upper half reads the TMA fill value past column d and stores nothing)
+  // dWd = H^T dY on CTA pairs, dWd as [E][I][d]
   if (!make_map(&ta, h, I, M, 64, 64) || !make_map(&tb0, dy, d, M, 64, 64) ||
-      !make_map(&tc0, dw_down, d, static_cast<uint64_t>(E) * I, 32, 32, true) ||
-      !make_map(&ta16, h, I, M, 64, 16) || !make_map(&tpad, pad_h, I, static_cast<uint64_t>(E) * 16, 64, 16))
+      !make_map3(&tc0, dw_down, d, I, E, 32, 32, true) || !make_map(&ta16, h, I, M, 64, 16) ||
+      !make_map(&tpad, pad_h, I, static_cast<uint64_t>(E) * 16, 64, 16))
     return MOE_ERR_CUDA;
   p.outf0 = dw_down;
   p.outf1 = nullptr;
   p.m_tiles = (I + 2 * BM - 1) / (2 * BM);
+  p.nt_half = 0;
   p.n_tiles = (d + 255) / 256;
-  return launch_pair_wgrad<WGRAD_D>(ta, tb0, tc0, tc0, ta16, tpad, p,
+  return launch_pair_wgrad<WGRAD_D>(ta, tb0, tb0, tc0, tc0, ta16, tpad, p,
                                     static_cast<long long>(E) * p.m_tiles * p.n_tiles, st);
 }
 
@@ -1908,10 +1991,8 @@ extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, i
                                    void* stream) {
   using namespace moe;
   using namespace moe::gemm;
-  if (!ffn_shape_ok(E, M, d, I)) {
-    if (E >= 1 && M >= 0 && d > 0 && I > 0 && d % 8 == 0 && I % 8 == 0) return MOE_ERR_UNSUPPORTED;
-    return MOE_ERR_INVALID_ARG;
-  }
+  if (!ffn_shape_ok(E, M, d, I)) return MOE_ERR_INVALID_ARG;
+  if (d % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;   // whole scale blocks and tiles
   if (M == 0) return MOE_OK;
   if (!xp || !offsets || !wgu_q || !wgu_sf || !wd_q || !wd_sf || !y || !h) return MOE_ERR_INVALID_ARG;
   if (!aligned16(xp) || !aligned16(offsets) || !aligned16(wgu_q) || !aligned16(wgu_sf) ||
@@ -1938,7 +2019,7 @@ extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, i
   const long long mt_upper = (M + BM - 1) / BM + E;
   int rc = launch_quantize_rows(xp, offsets, E, M, d, xq, xsf, st);
   if (rc) return rc;
-  CUtensorMap ta, tb0, tb1, tc0, tc1, ts;
+  CUtensorMap ta, tb0, tb1, tc0, tc1, tc2, ts;
   // gate/up on 256 x 256 pair tiles (128 gate + 128 up columns), SwiGLU epilogue;
   // the epilogue also writes H's E4M3 copy and its scale atoms for the down
   // projection (the quantization fused: no second pass over H)
@@ -1946,10 +2027,14 @@ extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, i
       !make_map_u8(&tb0, wgu_q, d, static_cast<uint64_t>(E) * 2 * I, 128, 128) ||
       !make_map_atoms(&tb1, xsf, static_cast<uint64_t>(tiles) * (d / 128)) ||
       !make_map_atoms(&ts, wgu_sf, static_cast<uint64_t>(E) * (2 * I / 128) * (d / 128)) ||
-      !make_map(&tc0, h, I, M, 64, 32) ||
-      !make_map(&tc1, gu ? static_cast<const void*>(gu) : static_cast<const void*>(h),
-                gu ? 2 * static_cast<uint64_t>(I) : I, M, 64, 32))
+      !make_map(&tc0, h, I, M, 64, 32))
     return MOE_ERR_CUDA;
+  if (gu) {
+    if (!make_half_map(&tc1, gu, I, M, 0, 64, 32) || !make_half_map(&tc2, gu, I, M, I, 64, 32))
+      return MOE_ERR_CUDA;
+  } else {
+    tc1 = tc2 = tc0;   // not stored through
+  }
   p.n_tiles = I / 128;
   p.k_blocks = d / 128;
   p.out = reinterpret_cast<__nv_bfloat16*>(h);
@@ -1957,7 +2042,7 @@ extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, i
   p.ld_out = I;
   p.hq = hq;
   p.hsf = hsf;
-  rc = launch_pair_depth<FWD_GATEUP, 256, true>(ta, tb0, tb1, tc0, tc1, ts, p,
+  rc = launch_pair_depth<FWD_GATEUP, 256, true>(ta, tb0, tb1, tc0, tc1, tc2, ts, p,
                                                  mt_upper * p.n_tiles, st);
   if (rc) return rc;
   p.hq = nullptr;
@@ -1976,9 +2061,9 @@ extern "C" int moe_grouped_ffn_fp8(const moe_bf16* xp, const int32_t* offsets, i
   p.out2 = nullptr;
   p.ld_out = d;
   if (bn == 256)
-    return launch_pair_depth<FWD_DOWN, 256, true>(ta, tb0, tb1, tc0, tc0, ts, p,
+    return launch_pair_depth<FWD_DOWN, 256, true>(ta, tb0, tb1, tc0, tc0, tc0, ts, p,
                                                    mt_upper * p.n_tiles, st);
-  return launch_pair_depth<FWD_DOWN, 128, true>(ta, tb0, tb1, tc0, tc0, ts, p,
+  return launch_pair_depth<FWD_DOWN, 128, true>(ta, tb0, tb1, tc0, tc0, tc0, ts, p,
                                                  mt_upper * p.n_tiles, st);
 }
 

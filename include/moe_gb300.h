@@ -273,8 +273,10 @@ int moe_dispatch_scatter(const moe_bf16* x, int T, int d, int K, const int32_t* 
  *   y  [M,d] bf16 out.   h [M,I] bf16 out (needed by the down projection).
  *   gu [M,2I] bf16 out, or NULL to skip saving it.
  *   ws: moe_workspace_size(MOE_OP_GROUPED_FFN, ...), status word only.
- * Limits: d % 128 == 0, I % 128 == 0, E <= 1024. Also used with E = 1 and
- * offsets {0, T} for always-on shared experts ([SF] "What this adds"). */
+ * Limits: d % 8 == 0, I % 8 == 0 (rows of 16 bytes; tails of the 64-column
+ * tiles read zeros and are not stored), E <= 1024; other d or I return
+ * MOE_ERR_INVALID_ARG. Also used with E = 1 and offsets {0, T} for always-on
+ * shared experts ([SF] "What this adds"). */
 int moe_grouped_ffn(const moe_bf16* xp, const int32_t* offsets, int E, int M, int d, int I,
                     const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
                     moe_bf16* y, moe_bf16* h, moe_bf16* gu,
@@ -503,8 +505,9 @@ int moe_mxfp8_quantize_weights(const moe_bf16* w_a, const moe_bf16* w_b, int E, 
  * xp is quantized inside the call and mx(h) comes from the gate/up GEMM's
  * epilogue, from the same registers as h; the weights come quantized by
  * moe_mxfp8_quantize_weights (wgu_q / wgu_sf
- * from gate and up, wd_q / wd_sf from down). Shapes, layouts and limits as
- * moe_grouped_ffn (d % 128 == 0, I % 128 == 0); ws:
+ * from gate and up, wd_q / wd_sf from down). Shapes and layouts as
+ * moe_grouped_ffn; d % 128 == 0 and I % 128 == 0 (whole scale atoms and
+ * tiles; other multiples of 8 return MOE_ERR_UNSUPPORTED); ws:
  * moe_workspace_size(MOE_OP_GROUPED_FFN_FP8, M, E, 1, 1, d, I) bytes (the
  * quantized xp and h with their scales). Runs on 256 x 256 CTA-pair tiles
  * (256 x 128 for the down projection when d is an odd multiple of 128) with

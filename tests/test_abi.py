@@ -95,8 +95,13 @@ def test_argument_validation_rows_and_gemm(lib):
     f = lib.moe_grouped_ffn
     ok = (FAKE, FAKE, 4, 256, 128, 256, FAKE, FAKE, FAKE, FAKE, FAKE, None)
     assert f(*ok, FAKE, 0, None) == B.MOE_ERR_WORKSPACE
-    assert f(FAKE, FAKE, 4, 256, 128, 200, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 256,
-             None) == B.MOE_ERR_UNSUPPORTED                                           # I % 128
+    assert f(FAKE, FAKE, 4, 256, 128, 204, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 256,
+             None) == B.MOE_ERR_INVALID_ARG                                           # I % 8
+    assert f(FAKE, FAKE, 4, 256, 136, 200, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 0,
+             None) == B.MOE_ERR_WORKSPACE                                  # d, I % 8: accepted
+    f8 = lib.moe_grouped_ffn_fp8
+    assert f8(FAKE, FAKE, 4, 256, 136, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20,
+              None) == B.MOE_ERR_UNSUPPORTED                                     # MXFP8: d % 128
     assert f(FAKE, FAKE, 4, 256, 100, 256, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 256,
              None) == B.MOE_ERR_INVALID_ARG                                           # d % 8
     assert f(FAKE, FAKE, 4, 256, 128, 256, FAKE, FAKE, FAKE, MIS, FAKE, None, FAKE, 256,

@@ -48,6 +48,13 @@ SMALL = [
     # packed rows (its activation boxes reach past M)
     ([1, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 257, 384, 552, 255, 256, 0, 40],
      256, 256),
+    # d and I multiples of 8 only: K and N tails inside a 64-column box (the weights'
+    # 3-D maps and the half maps of [G | U] and [dG | dU] read zeros past the edge,
+    # the stores clip at it); 64 + 64-column gate/up tiles (I % 128 = 8), dW row and
+    # column tiles that end inside a box, and dimensions below one box
+    ([40, 0, 300, 1, 129], 136, 264),
+    ([200, 17, 0, 333], 200, 72),
+    ([1, 100, 0, 64, 130], 56, 40),
 ]
 
 
@@ -64,7 +71,7 @@ def test_grouped_ffn_forward_small(counts, d, I):
     assert_out_close(f64(y), ry, name="y")
 
 
-@pytest.mark.parametrize("counts,d,I", [c for c in SMALL if c[1] % 128 == 0])
+@pytest.mark.parametrize("counts,d,I", SMALL)
 def test_grouped_ffn_backward_small(counts, d, I):
     off, xp, wg, wu, wd = _problem(counts, d, I, 3 * sum(counts) + I)
     g = torch.Generator().manual_seed(11)

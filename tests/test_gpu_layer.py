@@ -25,6 +25,8 @@ CASES = [
     W.small_config("shared", T=384, d=128, E=8, K=2, I=128, R=2, shared_I=256),
     W.small_config("skewed", T=1024, d=128, E=32, K=4, I=128, R=8, skew=True),
     W.small_config("norenorm", T=256, d=128, E=8, K=3, I=128, R=2, renorm=0),
+    # hidden and intermediate sizes that are multiples of 8 only (GEMM K and N tails)
+    W.small_config("odd", T=600, d=136, E=12, K=3, I=200, R=4, shared_I=72),
 ]
 
 

@@ -262,24 +262,36 @@ def test_layer_full_size_sampled_tokens(name, n_tok):
 
 def _carry_dw(a, da, b, db, offsets):
     """Per-element bound on how far X^T B moves when each bf16 entry of the
-    operands moves by at most da, db (one ulp): per expert |A|^T db + da^T |B|."""
+    operands moves by at most da, db (one ulp; None: exact): per expert
+    |A|^T db + da^T |B|."""
     out = np.zeros((len(offsets) - 1, a.shape[1], b.shape[1]))
     for e in range(len(offsets) - 1):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi > lo:
-            out[e] = np.abs(a[lo:hi]).T @ db[lo:hi]
+            if db is not None:
+                out[e] = np.abs(a[lo:hi]).T @ db[lo:hi]
             if da is not None:
                 out[e] += da[lo:hi].T @ np.abs(b[lo:hi])
     return out
 
 
-@pytest.mark.parametrize("name", ["qwen3", "skew"])
+def _swiglu_grads(dh, gu, I):
+    """dG and dU of the SwiGLU backward (rounded to bf16 as stored) from dH and
+    the saved [G | U]."""
+    G, U = gu[:, :I], gu[:, I:]
+    sg = 1.0 / (1.0 + np.exp(-G))
+    return (O.round_bf16(dh * U * sg * (1.0 + G * (1.0 - sg))), O.round_bf16(dh * G * sg))
+
+
+@pytest.mark.parametrize("name", ["qwen3", "skew", "dsv2lite"])
 def test_layer_full_size_every_element(name):
     """The benchmarked launch sequence on the whole Qwen3-shaped workload
     (T=8192, d=2048, E=128, K=8, I=768, R=8), forward and backward, compared
     element by element on every output with the oracle's layer run on the same
-    seeded inputs; and on its Zipf-skewed routing (hot experts of thousands of
-    rows, empty experts whose weight gradients are zero).
+    seeded inputs; on its Zipf-skewed routing (hot experts of thousands of
+    rows, empty experts whose weight gradients are zero); and on the
+    DeepSeek-V2-Lite-shaped workload (T=16384, E=64, K=6, I=1408, two always-on
+    shared experts of 1408 as one of 2816).
 
     Stated bounds where the compared value is the first rounding of a sum of
     exact inputs: routing, permutation and expert-parallel indices bit-exact;
@@ -296,7 +308,10 @@ def test_layer_full_size_every_element(name):
     sum_c |dout_c| ulp(y_c) and dlogits through the router's Jacobian; dxp
     ulp(dG) |Wg|^T + ulp(dU) |Wu|^T; dx sum_j (ulp(dxp_j) + dxp_j's own bound);
     dW_gate / dW_up |X|^T ulp(dG) / |X|^T ulp(dU); dW_down
-    |H|^T ulp(dY) + ulp(H)^T |dY|. All on top of 2e-2 RMS."""
+    |H|^T ulp(dY) + ulp(H)^T |dY|. The shared expert adds one ulp of its output
+    to out, and to dx one ulp of its input gradient plus that gradient's own
+    carry; its weight gradients carry as the routed ones (its dY is dout,
+    exact). All on top of 2e-2 RMS."""
     cfg = W.CONFIGS[name]
     T, K, d, I = cfg.T, cfg.K, cfg.d, cfg.I
     inp = W.make_inputs(cfg, with_backward=True)
@@ -322,9 +337,20 @@ def test_layer_full_size_every_element(name):
     assert_bf16_close(f64(layer.h), ref["h_pre"], name="h")
     assert_bf16_close(f64(layer.gu), ref["gu_pre"], name="gu")
     assert_out_close(f64(layer.y), ref["y_pre"], name="y")
-    # combine: one ulp of each weighted y it sums
+    shared = bool(cfg.shared_I)
+    if shared:   # the shared expert on every token (E = 1 over x)
+        Is = cfg.shared_I
+        ys_pre, gus_pre, hs_pre = O.swiglu_expert(np_inp["x"], np_inp["ws_gate"], np_inp["ws_up"],
+                                                  np_inp["ws_down"], pre=True)
+        assert_bf16_close(f64(layer.hs), hs_pre, name="h shared")
+        assert_bf16_close(f64(layer.gus), gus_pre, name="gu shared")
+        assert_out_close(f64(layer.ys), ys_pre, name="y shared")
+        del ys_pre, gus_pre, hs_pre
+    # combine: one ulp of each weighted y it sums (and of the shared expert's y)
     w_ref, ip = ref["topk_w"], ref["inv_perm"].reshape(T, K)
     carry = np.einsum("tk,tkd->td", np.abs(w_ref), 2 * half_ulp_bf16(ref["y"])[ip])
+    if shared:
+        carry += 2 * half_ulp_bf16(ref["ys"])
     rms = np.sqrt(np.mean(ref["out_pre"] ** 2))
     assert (rounding_excess(f64(out), ref["out_pre"]) <= RMS_TOL * rms + carry).all(), "out"
     del carry
@@ -352,11 +378,8 @@ def test_layer_full_size_every_element(name):
     for e in range(E):
         lo, hi = int(off[e]), int(off[e + 1])
         dH[lo:hi] = dyo[lo:hi] @ np_inp["w_down"][e].T
-    G, U = gu[:, :I], gu[:, I:]
-    sg = 1.0 / (1.0 + np.exp(-G))
-    dG = O.round_bf16(dH * U * sg * (1.0 + G * (1.0 - sg)))
-    dU = O.round_bf16(dH * G * sg)
-    del dH, G, U, sg
+    dG, dU = _swiglu_grads(dH, gu, I)
+    del dH
     # dxp sums dG Wg^T + dU Wu^T: one ulp of each dG, dU weighted by |W|
     carry_dxp = np.empty((T * K, d))
     uG, uU = 2 * half_ulp_bf16(dG), 2 * half_ulp_bf16(dU)
@@ -370,6 +393,11 @@ def test_layer_full_size_every_element(name):
     # dx sums the K rows of dxp: each may be an ulp off, plus what dxp itself carries
     carry = ((2 * half_ulp_bf16(rb["dxp"]) + carry_dxp)[ip]).sum(axis=1)
     del carry_dxp
+    if shared:   # plus the shared expert's dx: an ulp of it and its own carry
+        dGs, dUs = _swiglu_grads(dout @ np_inp["ws_down"].T, ref["gus"], Is)
+        carry += (2 * half_ulp_bf16(rb["dx_shared"]) +
+                  2 * half_ulp_bf16(dGs) @ np.abs(np_inp["ws_gate"]).T +
+                  2 * half_ulp_bf16(dUs) @ np.abs(np_inp["ws_up"]).T)
     rms = np.sqrt(np.mean(rb["dx_pre"] ** 2))
     assert (rounding_excess(f64(dx), rb["dx_pre"]) <= RMS_TOL * rms + carry).all(), "dx"
     del carry
@@ -383,3 +411,18 @@ def test_layer_full_size_every_element(name):
         assert (err <= RMS_TOL * rms + carry).all(), name
         # the carries bound the worst case; in aggregate the error stays far smaller
         assert np.sqrt(np.mean(err ** 2)) <= 1e-3 * rms, name
+    if shared:
+        off1 = np.array([0, T])
+        xs, hs = np_inp["x"], ref["hs"]
+        for name, got, want, carry in (
+                ("dws_gate", layer.dws_gate, rb["dws_gate"],
+                 _carry_dw(xs, None, dGs, 2 * half_ulp_bf16(dGs), off1)),
+                ("dws_up", layer.dws_up, rb["dws_up"],
+                 _carry_dw(xs, None, dUs, 2 * half_ulp_bf16(dUs), off1)),
+                ("dws_down", layer.dws_down, rb["dws_down"],
+                 _carry_dw(hs, 2 * half_ulp_bf16(hs), dout, None, off1))):
+            want = want[None] if want.ndim == 2 else want
+            rms = np.sqrt(np.mean(want ** 2))
+            err = np.abs(f64(got) - want)
+            assert (err <= RMS_TOL * rms + carry).all(), name
+            assert np.sqrt(np.mean(err ** 2)) <= 1e-3 * rms, name

@@ -595,7 +595,7 @@ __device__ __forceinline__ int quantize_row32(const float (&h)[32], uint4 (&q)[2
 // FP8 = true: the forward kinds on MXFP8 operands (E4M3 elements, one UE8M0
 // scale per 32 K; tcgen05.mma kind::mxf8f6f4 with block scaling). A k-block is
 // then 128 K (the same 128-byte rows), B is K-major (the weights are quantized
-// into a transposed layout, gate and up interleaved in 64-row blocks), and each
+// into a transposed layout, gate and up interleaved in 128-row blocks), and each
 // stage also carries one 512-byte scale atom for the CTA's 128 A rows (tmB1)
 // and one per 128 of the pair's B columns (tmS): 128 rows x 4 K32 scales, row r
 // at byte (r % 32) * 16 + (r / 32) * 4 + k. The MMA thread copies both atoms
@@ -741,8 +741,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                                               : STAGE_BYTES));
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           if constexpr (FP8) {
-            // A rows, the CTA's 64 B rows (gate or up for gate/up: interleaved rows),
-            // then the A rows' scale atom and the pair's B scale atom
+            // A rows, the CTA's BN / 2 B rows (gate or up for gate/up: interleaved
+            // blocks), then the A rows' scale atom and the pair's B scale atoms
             const uint32_t fb = map_to_rank(fb_local, 0);
             const int nq = (KIND == FWD_GATEUP) ? 2 * p.I : p.d;    // B rows per expert
             const int nrow = (KIND == FWD_GATEUP) ? 2 * tl.n0 : tl.n0;

@@ -107,6 +107,8 @@ def test_argument_validation_rows_and_gemm(lib):
     assert f(FAKE, FAKE, 4, 256, 128, 256, FAKE, FAKE, FAKE, MIS, FAKE, None, FAKE, 256,
              None) == B.MOE_ERR_MISALIGNED
     g = lib.moe_grouped_ffn_backward
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 132, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+             FAKE, FAKE, 1 << 30, None) == B.MOE_ERR_INVALID_ARG                       # d % 8
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
              FAKE, FAKE, 256, None) == B.MOE_ERR_WORKSPACE
     gd = lib.moe_grouped_ffn_backward_data

@@ -55,6 +55,8 @@ SMALL = [
     ([40, 0, 300, 1, 129], 136, 264),
     ([200, 17, 0, 333], 200, 72),
     ([1, 100, 0, 64, 130], 56, 40),
+    ([3, 0, 70, 129], 8, 16),
+    ([17, 200], 24, 8),
 ]
 
 

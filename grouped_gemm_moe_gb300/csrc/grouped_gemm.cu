@@ -625,14 +625,22 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   // scale atoms per stage: the A rows' atom, then the B columns' atoms, padded to 1 KB
   constexpr uint32_t SF_BYTES = FP8 ? ((512u * (1u + SFB_ATOMS) + 1023u) & ~1023u) : 0u;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
-  // Accumulator buffers: two (the epilogue of tile i overlaps the MMAs of tile
-  // i + 1), except for MXFP8 256 x 256 tiles, whose 256 columns leave the other
-  // half of TMEM to the scale ring.
-  constexpr int NACC = (FP8 && BN == 256) ? 1 : 2;
+  // Two accumulator buffers: the epilogue of tile i overlaps the MMAs of tile
+  // i + 1. MXFP8 keeps its per-stage scale ring in TMEM too: beside the two
+  // buffers for 256 x 128 tiles; for 256 x 256 tiles (the two buffers fill all
+  // 512 columns) in the first 64 columns of the buffer the previous tile
+  // accumulated into (RING_SWAP): tile i's MMAs start once tile i - 1's
+  // epilogue has read those columns (its first 64-column step, which signals
+  // ring_free), and tile i's own accumulator region held tile i - 1's ring,
+  // whose MMAs completed before that epilogue began.
+  constexpr int NACC = 2;
+  constexpr bool RING_SWAP = FP8 && BN == 256;
   constexpr uint32_t TMEM_COLS = FP8 ? 512u : 2u * BN;
   constexpr uint32_t SF_COLS = 4u * (1u + SFB_ATOMS);   // TMEM columns of one stage's scales
   constexpr uint32_t SF_COL0 = static_cast<uint32_t>(NACC) * BN;
-  static_assert(!FP8 || SF_COL0 + SF_COLS * STAGES <= TMEM_COLS, "MXFP8 scale ring in TMEM");
+  static_assert(!FP8 || RING_SWAP || SF_COL0 + SF_COLS * STAGES <= TMEM_COLS,
+                "MXFP8 scale ring in TMEM");
+  static_assert(!RING_SWAP || SF_COLS * STAGES <= 64, "MXFP8 scale ring in a drained step");
   constexpr uint32_t IDESC = FP8 ? make_idesc_mxf8<BN, 2 * BM>() : make_idesc<BN, false, B_MN, 2 * BM>();
   constexpr uint32_t MN_ATOM = 64 * 128;
 
@@ -641,8 +649,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* epi = smem + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + pair_epi_bytes<KIND>());
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, aux[4]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 9);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, aux[4], ring_free[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_mp = s_off + (p.E + 1);
@@ -659,11 +667,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
   auto aux_bar = [&](int w) { return bar_base + 8u * (2 * STAGES + 5 + w); };
+  auto ring_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 9 + a); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
-    // the leader's accumulator-empty barriers collect the four epilogue warps of both CTAs
-    for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 8); }
+    // the leader's accumulator-empty (and ring-free) barriers collect the four
+    // epilogue warps of both CTAs
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);
+      mbar_init(ring_bar(a), 8);
+    }
     mbar_init(drain_bar, 1);
     for (int w = 0; w < 4; ++w) mbar_init(aux_bar(w), 1);
     *abort_flag = 0;
@@ -789,17 +803,24 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = cid; t < total && ok; t += ncl) {
+      int j = 0;   // this cluster's tile count
+      for (int t = cid; t < total && ok; t += ncl, ++j) {
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        if (RING_SWAP && j > 0) {
+          // the previous tile's epilogue has read the columns this tile's scale ring takes
+          if (!mbar_wait(ring_bar(acc ^ 1), static_cast<uint32_t>((j - 1) >> 1) & 1u, abort_flag,
+                         p.status)) { ok = false; break; }
+        }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t ring0 = RING_SWAP ? static_cast<uint32_t>((acc ^ 1) * BN) : SF_COL0;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
           if (lane == 0) {
             if constexpr (FP8) {
-              const uint32_t t_sfa = tmem_base + SF_COL0 + SF_COLS * static_cast<uint32_t>(stage);
+              const uint32_t t_sfa = tmem_base + ring0 + SF_COLS * static_cast<uint32_t>(stage);
               const uint32_t t_sfb = t_sfa + 4u;
               const uint32_t sf = sb + B_BYTES;
               tc_cp_pair_32x128(t_sfa, smem_desc_rows16(sf));
@@ -950,6 +971,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * BN);
+        // MXFP8 256 x 256: once this tile's columns [0, 64) have been read for the
+        // last time (in its first 64-column step), the next tile's scale ring may
+        // take them
+        auto ring_free = [&]() {
+          if constexpr (RING_SWAP) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(ring_bar(acc), 0));
+          }
+        };
         if constexpr (KIND == FWD_GATEUP) {
           // H, then (when saved) G and U leave one stream at a time through the
           // warp's two alternating [32 x 64] boxes; the accumulator is read again for
@@ -973,6 +1004,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 tmem_ld32(tacc + c64 + sub, g);   // warp-wide: every lane loads
                 tmem_ld32(tacc + HALF + c64 + sub, u);
                 tmem_wait_ld();
+                if (c64 == 0 && sub == 32) ring_free();
                 if (valid) {
 #pragma unroll
                   for (int i = 0; i < 32; ++i) h[i] = silu_f(g[i]) * u[i];
@@ -1023,6 +1055,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                   tmem_ld32(tacc + (sidx == 1 ? 0 : HALF) + c64 + sub, v);
                   tmem_wait_ld();
                 }
+                // columns [0, 64) are last read by the G stream (H alone: the H stream)
+                if (c64 == 0 && sub == 32 && sidx == (nst > 1 ? 1 : 0)) ring_free();
                 stage_row32(st, lane, sub >> 3, v);
               }
               fence_proxy_async();
@@ -1048,6 +1082,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
               float v[32];
               tmem_ld32(tacc + c64 + sub, v);
               tmem_wait_ld();
+              if (c64 == 0 && sub == 32) ring_free();
               if (full) stage_row32(st, lane, sub >> 3, v);
               else if (valid)
                 store32_bf16(p.out + grow * p.ld_out + tl.n0 + c64 + sub, v,
@@ -1556,7 +1591,7 @@ template <int KIND, int BN, int STAGES, bool FP8 = false>
 constexpr size_t pair_smem_bytes(int E) {
   return 1024 + STAGES * (BM * BK * 2 + (BN / 2) * BK * 2 +
                           (FP8 ? ((512 * (1 + BN / 128) + 1023) & ~1023) : 0)) +
-         pair_epi_bytes<KIND>() + 8 * (2 * STAGES + 9) + 16 + sizeof(int) * 2 * (E + 1) + 16;
+         pair_epi_bytes<KIND>() + 8 * (2 * STAGES + 11) + 16 + sizeof(int) * 2 * (E + 1) + 16;
 }
 
 // Launches a cluster-of-two kernel on as many clusters as can be resident

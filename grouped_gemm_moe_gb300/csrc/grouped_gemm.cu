@@ -1028,7 +1028,46 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
               }
               continue;
             }
-            for (int sidx = 0; sidx < nst; ++sidx) {
+            // MXFP8 256 x 256, first step with G and U saved: H and G are staged
+            // together from the same registers (both boxes), so columns [0, 64)
+            // are read once and the next tile's scale ring can take them sooner
+            const bool hg = RING_SWAP && c64 == 0 && nst == 3;
+            if (hg) {
+              uint8_t* sth = epi + ew * 8192 + buf * 4096;
+              uint8_t* stg = epi + ew * 8192 + (buf ^ 1) * 4096;
+              if (lane == 0) bulk_wait_read_all();   // both boxes' stores are done
+              __syncwarp();
+              for (int sub = 0; sub < 64; sub += 32) {
+                float g[32], u[32], v[32];
+                tmem_ld32(tacc + sub, g);
+                tmem_ld32(tacc + HALF + sub, u);
+                tmem_wait_ld();
+                if (sub == 32) ring_free();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = silu_f(g[i]) * u[i];
+                if (fuse_q) {
+                  uint4 qb[2];
+                  const int X = quantize_row32(v, qb);
+                  uint4* dst = reinterpret_cast<uint4*>(p.hq + grow * p.I + tl.n0 + sub);
+                  dst[0] = qb[0];
+                  dst[1] = qb[1];
+                  const int col = tl.n0 + sub;
+                  p.hsf[atom_byte(qtile * (p.I / 128) + col / 128, rr, (col & 127) >> 5)] =
+                      static_cast<uint8_t>(X + 127);
+                }
+                stage_row32(sth, lane, sub >> 3, v);
+                stage_row32(stg, lane, sub >> 3, g);
+              }
+              fence_proxy_async();
+              __syncwarp();
+              if (lane == 0) {   // two bulk groups: H's box is the older one
+                tma_store_2d(&tmC0, smem_u32(sth), tl.n0, growq);
+                bulk_commit();
+                tma_store_2d(&tmC1, smem_u32(stg), tl.n0, growq);
+                bulk_commit();
+              }
+            }
+            for (int sidx = hg ? 2 : 0; sidx < nst; ++sidx) {
               uint8_t* st = epi + ew * 8192 + buf * 4096;
               if (lane == 0) bulk_wait_read_1();   // the store that used this box is done
               __syncwarp();
@@ -1056,7 +1095,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                   tmem_wait_ld();
                 }
                 // columns [0, 64) are last read by the G stream (H alone: the H stream)
-                if (c64 == 0 && sub == 32 && sidx == (nst > 1 ? 1 : 0)) ring_free();
+                if (!hg && c64 == 0 && sub == 32 && sidx == (nst > 1 ? 1 : 0)) ring_free();
                 stage_row32(st, lane, sub >> 3, v);
               }
               fence_proxy_async();

@@ -36,13 +36,15 @@ namespace {
 constexpr int kQThreads = 256;
 
 // Rows of x [M, K] bf16 -> q [M, K] E4M3 and scale atoms (expert-ordered row tiles).
-// A CTA takes whole rows (grid-stride); within a row a thread takes 16
-// consecutive elements (two 16-byte loads), the two threads of a pair share a
-// K32 block (amax by one shuffle), and the eight threads of a 128-element atom
-// column gather their four scale bytes into one 32-bit store (the atom keeps a
-// row's four K32 scales in consecutive bytes). The row's expert and scale tile
-// come from a binary search over the offsets once per row. Loops advance whole
-// warps, so every lane reaches every shuffle.
+// A CTA takes RPI whole rows at a time (grid-stride) and issues all their loads
+// before it converts any; within a row a thread takes 16 consecutive elements
+// (two 16-byte loads), the two threads of a pair share a K32 block (amax by one
+// shuffle), and the eight threads of a 128-element atom column gather their four
+// scale bytes into one 32-bit store (the atom keeps a row's four K32 scales in
+// consecutive bytes). A row's expert and scale tile come from a binary search
+// over the offsets once per row. Loops advance whole warps, so every lane
+// reaches every shuffle.
+template <int RPI>
 __global__ void __launch_bounds__(kQThreads)
 quantize_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ offsets, int E,
                      int M, int K, uint4* __restrict__ q, uint8_t* __restrict__ sf) {
@@ -73,48 +75,64 @@ quantize_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ of
   const int kq = K / 128;
   const int rows = s_off[E] < M ? s_off[E] : M;
   const int span = ((nv + 31) / 32) * 32;   // whole warps
-  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-    int lo = 0, hi = E - 1;                 // the expert holding row r: largest e with off[e] <= r
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_off[mid] <= r) lo = mid; else hi = mid - 1;
+  for (int r0 = blockIdx.x * RPI; r0 < rows; r0 += gridDim.x * RPI) {
+    long long tile[RPI];
+    int rr[RPI];
+    bool live[RPI];
+#pragma unroll
+    for (int i = 0; i < RPI; ++i) {
+      const int r = r0 + i;
+      live[i] = r < rows;
+      int lo = 0, hi = E - 1;   // the expert holding row r: largest e with off[e] <= r
+      while (live[i] && lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      const int local = r - s_off[lo];
+      tile[i] = s_tile[lo] + local / 128;
+      rr[i] = local & 127;
     }
-    const int local = r - s_off[lo];
-    const long long tile = s_tile[lo] + local / 128;
-    const int rr = local & 127;
-    const uint4* xr = x + static_cast<size_t>(r) * (K / 8);
     for (int v = threadIdx.x; v < span; v += kQThreads) {
       const bool valid = v < nv;
-      float f[16];
+      uint4 a[RPI], b[RPI];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) f[u] = 0.f;
-      if (valid) {
-        const uint4 a = ldg_nc_v4(xr + 2 * v), b = ldg_nc_v4(xr + 2 * v + 1);
-        unpack8(a, f);
-        unpack8(b, f + 8);
+      for (int i = 0; i < RPI; ++i) {
+        if (valid && live[i]) {
+          const uint4* xr = x + static_cast<size_t>(r0 + i) * (K / 8);
+          a[i] = ldg_nc_v4(xr + 2 * v);
+          b[i] = ldg_nc_v4(xr + 2 * v + 1);
+        } else {
+          a[i] = b[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
-      float amax = 0.f;
 #pragma unroll
-      for (int u = 0; u < 16; ++u) amax = fmaxf(amax, fabsf(f[u]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      const int X = mx_exponent(amax);
-      const float sc = inv_pow2(X);
-      // the K32 block's scale byte (pair leader), gathered over the atom's four blocks
-      const uint32_t byte = static_cast<uint32_t>(X + 127) & 0xffu;
-      const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 2);
-      const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 4);
-      const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 6);
-      if (!valid) continue;
-      uint4 o;
-      o.x = to_e4m3x4(f[0] * sc, f[1] * sc, f[2] * sc, f[3] * sc);
-      o.y = to_e4m3x4(f[4] * sc, f[5] * sc, f[6] * sc, f[7] * sc);
-      o.z = to_e4m3x4(f[8] * sc, f[9] * sc, f[10] * sc, f[11] * sc);
-      o.w = to_e4m3x4(f[12] * sc, f[13] * sc, f[14] * sc, f[15] * sc);
-      q[static_cast<size_t>(r) * nv + v] = o;
-      if ((lane & 7) == 0) {   // v is a multiple of 8: the atom column v / 8
-        const long long atom = tile * kq + v / 8;
-        *reinterpret_cast<uint32_t*>(sf + atom_byte(atom, rr, 0)) =
-            byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      for (int i = 0; i < RPI; ++i) {
+        float f[16];
+        unpack8(a[i], f);
+        unpack8(b[i], f + 8);
+        float amax = 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) amax = fmaxf(amax, fabsf(f[u]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        const int X = mx_exponent(amax);
+        const float sc = inv_pow2(X);
+        // the K32 block's scale byte (pair leader), gathered over the atom's four blocks
+        const uint32_t byte = static_cast<uint32_t>(X + 127) & 0xffu;
+        const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 2);
+        const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 4);
+        const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 6);
+        if (!valid || !live[i]) continue;
+        uint4 o;
+        o.x = to_e4m3x4(f[0] * sc, f[1] * sc, f[2] * sc, f[3] * sc);
+        o.y = to_e4m3x4(f[4] * sc, f[5] * sc, f[6] * sc, f[7] * sc);
+        o.z = to_e4m3x4(f[8] * sc, f[9] * sc, f[10] * sc, f[11] * sc);
+        o.w = to_e4m3x4(f[12] * sc, f[13] * sc, f[14] * sc, f[15] * sc);
+        q[static_cast<size_t>(r0 + i) * nv + v] = o;
+        if ((lane & 7) == 0) {   // v is a multiple of 8: the atom column v / 8
+          const long long atom = tile[i] * kq + v / 8;
+          *reinterpret_cast<uint32_t*>(sf + atom_byte(atom, rr[i], 0)) =
+              byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        }
       }
     }
   }
@@ -176,13 +194,17 @@ long long mxfp8_row_tiles(long long M, int E) { return (M + 127) / 128 + 2LL * E
 
 int launch_quantize_rows(const void* x, const int32_t* offsets, int E, int M, int K, void* q,
                          void* sf, cudaStream_t st) {
-  long long grid = M;   // a CTA per row, at most eight resident CTAs per SM (grid-stride)
+#ifndef MOE_QROWS_RPI
+#define MOE_QROWS_RPI 2
+#endif
+  constexpr int kRpi = MOE_QROWS_RPI;   // rows per CTA iteration
+  long long grid = (M + kRpi - 1) / kRpi;   // at most eight resident CTAs per SM (grid-stride)
   const long long cap = static_cast<long long>(num_sms()) * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   const size_t smem = sizeof(int) * 2 * (E + 1);
   ProfScope prof("mxfp8_quantize_rows", st);
-  return launch_pdl(quantize_rows_kernel, static_cast<unsigned>(grid), kQThreads, smem, st, 1,
+  return launch_pdl(quantize_rows_kernel<kRpi>, static_cast<unsigned>(grid), kQThreads, smem, st, 1,
                     static_cast<const uint4*>(x), offsets, E, M, K, static_cast<uint4*>(q),
                     static_cast<uint8_t*>(sf));
 }

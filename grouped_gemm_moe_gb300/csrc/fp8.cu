@@ -2,7 +2,7 @@
 //
 // Source: xtuner PR "Decouple expert parallelism from FSDP sharding (dp2ep
 // layout)", "Changes" (the Float8 bullet: tile-wise scaling) and
-// "Verification" (tile-wise FP8 runs); the pages fix no format, so this build
+// "Verification" (tile-wise FP8 runs); the pages fix no format, so this library
 // takes the block-scaled format the GB300 tensor cores read natively (OCP
 // Microscaling MXFP8): E4M3 elements, and for every 32 consecutive elements
 // along the reduction dimension K one power-of-two scale 2^X stored as an

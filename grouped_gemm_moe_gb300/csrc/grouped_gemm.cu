@@ -27,6 +27,10 @@
 //     double-buffered in TMEM so the epilogue of tile i overlaps the MMAs of
 //     tile i+1; the ring depth grows when the expert count leaves shared
 //     memory for it;
+//   * d and I are any multiples of 8: the weights are 3-D tensor maps
+//     [E][rows][cols] and [G | U], [dG | dU] are read and written through maps
+//     of their halves, so K and N tails read zeros and bulk stores clip at the
+//     edges (no padding, no copies);
 //   * operands use the 128-byte swizzle. K-major tiles come from row-major
 //     activations and from the weights in the backward; MN-major tiles from
 //     the weights in the forward and from both operands of the weight

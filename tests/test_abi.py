@@ -118,9 +118,17 @@ def test_argument_validation_rows_and_gemm(lib):
               None) == B.MOE_ERR_INVALID_ARG                                          # gu
     assert gd(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, None, FAKE, FAKE, FAKE, FAKE, 256,
               None) == B.MOE_ERR_INVALID_ARG                                          # w_gate
+    assert gd(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 136, 200, FAKE, FAKE, FAKE, FAKE, FAKE, 256,
+              None) == B.MOE_ERR_WORKSPACE                                   # d, I % 8: accepted
+    assert gd(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 136, 204, FAKE, FAKE, FAKE, FAKE, FAKE, 256,
+              None) == B.MOE_ERR_INVALID_ARG                                          # I % 8
     gw = lib.moe_grouped_ffn_backward_weights
     assert gw(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, FAKE, FAKE, FAKE, FAKE, 256,
               None) == B.MOE_ERR_WORKSPACE
+    assert gw(FAKE, FAKE, FAKE, FAKE, 4, 256, 8, 8, FAKE, FAKE, FAKE, FAKE, 256,
+              None) == B.MOE_ERR_WORKSPACE                                   # d, I = 8: accepted
+    assert gw(FAKE, FAKE, FAKE, FAKE, 4, 256, 12, 8, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+              None) == B.MOE_ERR_INVALID_ARG                                          # d % 8
     assert gw(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, FAKE, None, FAKE, FAKE, 256,
               None) == B.MOE_ERR_INVALID_ARG                                          # dw_up
     assert gw(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 256, FAKE, MIS, FAKE, FAKE, 1 << 30,

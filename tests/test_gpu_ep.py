@@ -36,6 +36,8 @@ CASES = [
     W.small_config("ep2_idle_rank", T=512, d=128, E=8, K=2, I=256, R=2, seed=3),
     W.small_config("ep4_norenorm", T=512, d=128, E=16, K=3, I=128, R=4, renorm=0),
     W.small_config("ep8_qwen3_shape", T=2048, d=2048, E=128, K=8, I=768, R=8),
+    # hidden and intermediate sizes that are multiples of 8 only
+    W.small_config("ep2_odd", T=512, d=136, E=8, K=2, I=200, R=2, shared_I=72),
 ]
 
 

@@ -150,6 +150,22 @@ def test_grouped_ffn_fp8_matches_oracle(counts, d, I):
     assert_out_close(f64(y), ref_y, name="y")
 
 
+def test_grouped_ffn_fp8_without_saved_gu():
+    """save_gu=False: the gate/up epilogue stores H (and its E4M3 copy) only; y and
+    h are the same as with [G | U] saved."""
+    counts = [300, 0, 129, 640, 1, 257]
+    d, I = 256, 384
+    off, xp, wg, wu, wd = _ffn_problem(counts, d, I, 77)
+    y, h, _, offd = _run_fp8(off, xp, wg, wu, wd)
+    D = dev()
+    wgu = B.moe_mxfp8_quantize_weights(wg.to(D), wu.to(D))
+    wdq = B.moe_mxfp8_quantize_weights(wd.to(D))
+    y2, h2, gu2 = B.moe_grouped_ffn_fp8(xp.to(D), offd, wgu, wdq, save_gu=False)
+    torch.cuda.synchronize()
+    assert gu2 is None
+    assert torch.equal(y2, y) and torch.equal(h2, h)
+
+
 def test_grouped_ffn_fp8_many_experts_and_against_bf16():
     """64 experts of ~512 rows at d=2048, I=768 (the qwen3 workload's expert
     shape): the oracle on every row; and the FP8 result stays within FP8's

@@ -3,9 +3,13 @@ layer's forward and backward.
 
 Independent references: a per-token torch implementation of the MoE layer
 (out[t] = sum_j w_j * MLP_{e_j}(x_t)), torch matmul + F.silu for the dense
-E=1 case, torch.autograd in float64 for the backward, and algebraic
-invariants (identity experts, linearity, expert relabelling).
+E=1 case, torch.autograd in float64 for the backward, algebraic invariants
+(identity experts, linearity, expert relabelling), and a hand-worked
+two-token example in closed form (tests/golden/swiglu_layer_example.txt).
 """
+import math
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -269,3 +273,46 @@ def test_pre_rounding_outputs_round_to_the_stored_values():
     for e in range(cfg.E):
         lo, hi = int(off[e]), int(off[e + 1])
         assert np.allclose(f["y_pre"][lo:hi], f["h"][lo:hi] @ inp["w_down"][e], rtol=1e-13, atol=0)
+
+
+GOLDEN_LAYER = os.path.join(os.path.dirname(__file__), "golden", "swiglu_layer_example.txt")
+
+
+def _golden_layer():
+    """The fixture's 'let' names, evaluated in order, and its expected arrays."""
+    env = {"exp": math.exp, "log": math.log}
+    want = {}
+    for ln in open(GOLDEN_LAYER):
+        ln = ln.strip()
+        if not ln or ln.startswith("#"):
+            continue
+        if ln.startswith("let "):
+            k, e = ln[4:].split("=", 1)
+            env[k.strip()] = eval(e, {"__builtins__": {}}, env)
+        else:
+            k, e = ln.split("=", 1)
+            want[k.strip()] = np.array(eval(e, {"__builtins__": {}}, env), dtype=np.float64)
+    return want
+
+
+def test_layer_hand_worked_example():
+    """tests/golden/swiglu_layer_example.txt: two tokens, two experts with I = 1,
+    K = 2, worked by hand in closed form (sigmoid(1), sigmoid(2)) — routing with a
+    tie, renormalised weights, the SwiGLU expert and its backward, the combine,
+    the router gradient and the per-expert weight gradients; exact arithmetic."""
+    want = _golden_layer()
+    inp = {"logits": np.array([[0.0, math.log(3.0)], [0.0, 0.0]]),
+           "x": np.array([[1.0, 2.0], [0.0, 1.0]]),
+           "w_gate": np.array([[[1.0], [0.0]], [[0.0], [1.0]]]),
+           "w_up": np.array([[[0.0], [1.0]], [[1.0], [0.0]]]),
+           "w_down": np.array([[[3.0, -1.0]], [[1.0, 1.0]]])}
+    ref = O.layer_forward(inp, 2, 2, 1, exact=True)
+    rb = O.layer_backward(inp, ref, np.array([[1.0, 0.0], [0.0, 1.0]]), 2, 1, exact=True)
+    got = {"topk_idx": ref["topk_idx"], "topk_w": ref["topk_w"], "out": ref["out"],
+           "dx": rb["dx"], "dtopk_w": rb["dtopk_w"], "dlogits": rb["dlogits"],
+           "dw_gate": rb["dw_gate"], "dw_up": rb["dw_up"], "dw_down": rb["dw_down"]}
+    assert set(want) == set(got)
+    for k, w in want.items():
+        g = np.asarray(got[k], dtype=np.float64)
+        assert g.shape == w.shape, k
+        assert np.allclose(g, w, rtol=0, atol=1e-14), k
